@@ -1,0 +1,404 @@
+"""Benchmark of the NVFP4 block-scaled grouped GEMM on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--sf-path fused]
+                    [--impl ours|reference] [--all-configs]
+
+One step = one nvfp4_ggemm_run call over the whole grouped problem (scale
+permutation, tile scheduling, loads, block-scaled MMAs, fp16 epilogue), with
+inputs resident in HBM. L2 is flushed (a 256 MB write on the same stream)
+before every timed call; each call is timed with CUDA events on its stream.
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on
+the host cores instead (bounded samples of the same workload).
+
+N > 1 (torchrun): every rank runs its own replica of the workload (the
+operation needs no exchange); the reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_scaled_fp4_grouped_gb300 import synth  # noqa: E402
+
+METRIC = "µs/call, FP4 TFLOPS and GB/s as fraction of roofline, NVFP4 grouped GEMM"
+UNIT = "µs/call"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_PER_BF16 = 13.5 / 2.25  # nominal dense ratio
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["block_scaled_fp4_grouped_gb300/csrc/ggemm_kernels.cu",
+                  "block_scaled_fp4_grouped_gb300/csrc/ptx.cuh",
+                  "block_scaled_fp4_grouped_gb300/csrc/ggemm_internal.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def traffic_for(config: str, sf_path: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
+    if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(f"{config}/{sf_path}")
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index, self.period_ms = index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0, torch=None, flush=None,
+                want_e2e: bool = False):
+    """Device timing of one config. Returns a dict of measurements."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    prob = synth.make_problem(name, seed=seed)
+    K, N = prob.K, prob.N
+    dev = lambda arrs: [torch.from_numpy(a).cuda() for a in arrs]
+    A, B, SFA, SFB = dev(prob.A), dev(prob.B), dev(prob.SFA), dev(prob.SFB)
+    kw = dict(sf_layout="raw", sf_path="fused")
+    if sf_path == "relayout":
+        kw = dict(sf_layout="raw", sf_path="relayout")
+    elif sf_path == "relayout-cached":
+        kw = dict(sf_layout="raw", sf_path="relayout", cache_b_scales=True)
+    elif sf_path == "atom":
+        kw = dict(sf_layout="atom", sf_path="fused")
+        SFA = [_atom(torch, nb, s, m, K) for s, m in zip(SFA, prob.M)]
+        SFB = [_atom(torch, nb, s, N, K) for s in SFB]
+    C = [torch.empty((m, N), dtype=torch.float16, device="cuda") for m in prob.M]
+    gg = nb.GroupedGemm(prob.M, N, K, **kw)
+    info = gg.info()
+    if kw.get("cache_b_scales"):
+        gg.prepare_b_scales(SFB)
+        SFB_run = [None] * len(SFB)
+    else:
+        SFB_run = SFB
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        gg.run(A, B, SFA, SFB_run, C)
+    st, detail = gg.sync_status()
+    if st != nb.NVFP4_OK:
+        raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        gg.run(A, B, SFA, SFB_run, C)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    st, detail = gg.sync_status()
+    if st != nb.NVFP4_OK:
+        raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
+    us = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]
+    out = {
+        "prob": prob, "info": info, "us": us, "wall_s": wall,
+        "us_mean": statistics.fmean(us), "us_median": statistics.median(us),
+        "us_min": min(us), "us_p90": sorted(us)[int(0.9 * (len(us) - 1))],
+        "bytes": synth.algorithmic_bytes(prob.M, N, K), "flops": synth.algorithmic_flops(prob.M, N, K),
+        "launches_per_call": info.kernels_per_run,
+    }
+    if want_e2e:
+        out["e2e"] = time_e2e(prob, kw, steps, warmup, torch, nb)
+    gg.close()
+    return out
+
+
+def _atom(torch, nb, sf, rows, K):
+    out = torch.zeros(nb.nvfp4_sf_atom_bytes(rows, K), dtype=torch.uint8, device="cuda")
+    assert nb.nvfp4_sf_relayout(sf, out, rows, K) == nb.NVFP4_OK
+    return out
+
+
+def time_e2e(prob, kw, steps, warmup, torch, nb):
+    """Same metric through nvfp4_ggemm_run_host: pinned host inputs copied in,
+    C copied back, every step."""
+    kw = {k: v for k, v in kw.items() if k != "cache_b_scales"}
+    if kw.get("sf_layout") == "atom":
+        kw = dict(sf_layout="raw", sf_path="fused")
+    pin = lambda arrs: [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in arrs]
+    A, B, SFA, SFB = pin(prob.A), pin(prob.B), pin(prob.SFA), pin(prob.SFB)
+    C = [torch.empty((m, prob.N), dtype=torch.float16).pin_memory() for m in prob.M]
+    h2d = sum(t.numel() * t.element_size() for t in A + B + SFA + SFB)
+    d2h = sum(t.numel() * t.element_size() for t in C)
+    n = max(3, min(steps, 50))
+    with nb.GroupedGemm(prob.M, prob.N, prob.K, **kw) as gg:
+        for _ in range(max(1, min(warmup, 3))):
+            gg.run_host(A, B, SFA, SFB, C)
+        times = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            gg.run_host(A, B, SFA, SFB, C)
+            times.append((time.perf_counter() - t0) * 1e6)
+    return {"value": statistics.fmean(times), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "median": statistics.median(times)}
+
+
+def oracle_sample_time(prob, budget_s: float):
+    """Time the oracle (as it stands) on a bounded sample of `prob`: whole
+    groups while they fit the budget, else a row subset of one group.
+    Returns (µs per full call extrapolated by flops, threads, sample text)."""
+    import oracle as oracle_pkg
+    O = oracle_pkg.get()
+    threads = os.cpu_count() or 1
+    total_flops = synth.algorithmic_flops(prob.M, prob.N, prob.K)
+    g = int(np.argmax(prob.M))
+    rows = prob.M[g]
+    # probe with 8 rows to size the sample
+    t0 = time.perf_counter()
+    O.group_gemm(prob.A[g][:8], prob.B[g], prob.SFA[g][:8], prob.SFB[g], prob.K, nthreads=threads)
+    probe = time.perf_counter() - t0
+    per_row = max(probe / 8, 1e-6)
+    take = int(max(8, min(rows, budget_s / per_row)))
+    t0 = time.perf_counter()
+    O.group_gemm(prob.A[g][:take], prob.B[g], prob.SFA[g][:take], prob.SFB[g], prob.K, nthreads=threads)
+    dt = time.perf_counter() - t0
+    sample_flops = 2 * take * prob.N * prob.K
+    us_full = dt * 1e6 * total_flops / sample_flops
+    return us_full, threads, f"group {g}: {take} of {rows} rows x N={prob.N} x K={prob.K} ({dt:.2f} s), scaled by flops"
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    prob = synth.make_problem(args.config, seed=0)
+    per_step = []
+    cores = os.cpu_count() or 1
+    sample = ""
+    budget = max(0.5, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        us, cores, sample = oracle_sample_time(prob, budget)
+        if i >= args.warmup:
+            per_step.append(us)
+    value = statistics.fmean(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.config, prob),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name, prob):
+    spec = synth.CONFIGS.get(name)
+    desc = name
+    if spec is not None:
+        if spec.m_fixed:
+            mdesc = f"M={list(spec.m_fixed)}"
+        else:
+            mdesc = f"M_g multiples of {spec.m_step} in [{spec.m_lo},{spec.m_hi}]"
+        desc = f"{name}: g={spec.G} N={spec.N} K={spec.K} {mdesc}, seed 0"
+    return {"workload": desc, "M": list(prob.M), "N": prob.N, "K": prob.K,
+            "values": "E2M1 codes uniform over 16; E4M3 scales 2^e(1+u), e in [-4,2]",
+            "scales": "raw row-major [rows, K/16] E4M3 per call"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c4")
+    ap.add_argument("--sf-path", default="fused", choices=["fused", "relayout", "relayout-cached", "atom"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--all-configs", action="store_true", help="also time every config (extra key)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from block_scaled_fp4_grouped_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    hbm, bf16, peak_src = measured_peaks()
+    fp4_peak_tflops = bf16 * FP4_PER_BF16
+
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        r = time_config(args.config, args.sf_path, args.steps, args.warmup, torch=torch, flush=flush,
+                        want_e2e=not args.no_e2e)
+    barrier(world)
+    us = max_over_ranks(world, r["us_mean"], device)
+    prob = r["prob"]
+    bytes_, flops = r["bytes"], r["flops"]
+    achieved_gbs = bytes_ / (r["us_mean"] * 1e-6) / 1e9
+    tflops = flops / (r["us_mean"] * 1e-6) / 1e12
+    t_roof_us = max(flops / (fp4_peak_tflops * 1e12), bytes_ / (hbm * 1e9)) * 1e6
+    line = {
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
+        "config": dict(workload_config(args.config, prob), sf_path=args.sf_path,
+                       l2="flushed before every timed call (256 MB write)",
+                       tile_n=r["info"].tile_n, grid=r["info"].grid, units=r["info"].units,
+                       stages=r["info"].stages, parallelism=f"replicas x{world}"),
+        "us_median": r["us_median"], "us_min": r["us_min"], "us_p90": r["us_p90"],
+        "tflops_fp4": tflops, "gbs": achieved_gbs,
+        "roofline_fraction": t_roof_us / r["us_mean"],
+        "roofline_time_us": t_roof_us,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm, "traffic": traffic_for(args.config, args.sf_path),
+                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_,
+                     "kernel": "ggemm_kernel" if args.sf_path != "relayout" else "ggemm_kernel + sf_relayout_kernel"},
+        "gpu_launches": r["launches_per_call"] * args.steps,
+        "clocks": clocks.summary(),
+        "timed_wall_s": r["wall_s"],
+    }
+    if "e2e" in r:
+        e2e = r["e2e"]
+        line["e2e"] = {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                       "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}
+    if args.all_configs and rank == 0:
+        per = {}
+        for name in ["c0", "c1", "c2", "c3", "c4", "c1_page", "c2_page", "c3_page", "c4_page"]:
+            for path in ["fused", "relayout", "relayout-cached"]:
+                q = time_config(name, path, max(20, args.steps // 2), args.warmup, torch=torch, flush=flush)
+                t_roof = max(q["flops"] / (fp4_peak_tflops * 1e12), q["bytes"] / (hbm * 1e9)) * 1e6
+                per[f"{name}/{path}"] = {"us_mean": round(q["us_mean"], 2), "us_median": round(q["us_median"], 2),
+                                         "us_min": round(q["us_min"], 2),
+                                         "gbs": round(q["bytes"] / (q["us_mean"] * 1e-6) / 1e9, 1),
+                                         "tflops": round(q["flops"] / (q["us_mean"] * 1e-6) / 1e12, 1),
+                                         "roofline_fraction": round(t_roof / q["us_mean"], 3),
+                                         "tile_n": q["info"].tile_n, "units": q["info"].units}
+        line["per_config"] = per
+    if rank == 0 and not args.no_cpu_baseline:
+        us_cpu, cores, sample = oracle_sample_time(prob, budget_s=10.0)
+        line["cpu_baseline"] = {"value": us_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,687 @@
+// Host side of the C ABI: argument validation, the tile schedule (prefix
+// sums of work units), per-group TMA tensor maps in a device-resident
+// problem table, workspace for re-laid-out scales, kernel launches and the
+// device error word.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "ggemm_internal.h"
+#include "nvfp4_ggemm.h"
+
+using namespace nvfp4;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kMaxGroups = 1024;
+constexpr int32_t kMaxM = 1 << 20;
+constexpr int32_t kMaxN = 1 << 20;
+constexpr int32_t kMaxK = 1 << 18;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kSlots = 4;  // problem-table ring: a table is rewritten only after its last kernel finished
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+uint64_t atom_bytes(int64_t rows, int64_t K)
+{
+    return (uint64_t)((rows + 127) / 128) * (uint64_t)(K / 64) * (uint64_t)kSfAtomBytes;
+}
+
+// 2-D tensor map over a row-major [rows][cols] matrix of `esize`-byte elements.
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t cols, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Slot {
+    uint8_t *h_table = nullptr;  // pinned staging
+    uint8_t *d_table = nullptr;
+    cudaEvent_t ev = nullptr;
+    bool used = false;
+    std::vector<const void *> key;
+};
+
+}  // namespace
+
+struct nvfp4_ggemm_plan_s {
+    int device = 0;
+    int sm_count = 0;
+    int G = 0, N = 0, K = 0;
+    std::vector<int32_t> M;
+    nvfp4_ggemm_options_t opt{};
+    int variant = -1;
+    GemmVariant var{};
+    int grid = 0;
+    int total_units = 0;
+    int k_tiles = 0;
+    std::vector<int32_t> m_tiles, m_groups, unit_prefix;
+    size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
+    Slot slots[kSlots];
+    int cur = -1;
+    uint32_t *d_err = nullptr;
+    uint8_t *d_ws = nullptr;
+    std::vector<size_t> ws_sfa, ws_sfb;  // workspace offsets of each group's atom-layout scales
+    // prepare_b_scales job table
+    RelayoutJob *d_prep_jobs = nullptr;
+    RelayoutJob *h_prep_jobs = nullptr;
+    cudaEvent_t ev_prep = nullptr;
+    bool prep_used = false;
+    bool b_prepared = false;
+    // run_host device buffers
+    uint8_t *d_io = nullptr;
+    std::vector<size_t> io_a, io_b, io_sfa, io_sfb, io_c;
+    size_t io_bytes = 0;
+
+    bool raw() const { return opt.sf_layout == NVFP4_SF_RAW; }
+    bool relayout() const { return raw() && opt.sf_path == NVFP4_SF_RELAYOUT; }
+    bool fused() const { return raw() && opt.sf_path == NVFP4_SF_FUSED; }
+};
+
+namespace {
+
+void release(nvfp4_ggemm_plan_s *p)
+{
+    for (Slot &s : p->slots) {
+        if (s.ev) {
+            if (s.used) cudaEventSynchronize(s.ev);
+            cudaEventDestroy(s.ev);
+        }
+        if (s.h_table) cudaFreeHost(s.h_table);
+        if (s.d_table) cudaFree(s.d_table);
+    }
+    if (p->ev_prep) {
+        if (p->prep_used) cudaEventSynchronize(p->ev_prep);
+        cudaEventDestroy(p->ev_prep);
+    }
+    if (p->h_prep_jobs) cudaFreeHost(p->h_prep_jobs);
+    if (p->d_prep_jobs) cudaFree(p->d_prep_jobs);
+    if (p->d_err) cudaFree(p->d_err);
+    if (p->d_ws) cudaFree(p->d_ws);
+    if (p->d_io) cudaFree(p->d_io);
+    delete p;
+}
+
+nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_options_t *out)
+{
+    nvfp4_ggemm_default_options(out);
+    if (!in) return NVFP4_OK;
+    if (in->struct_size != sizeof(nvfp4_ggemm_options_t)) return NVFP4_ERR_INVALID_ARG;
+    *out = *in;
+    if (out->sf_layout != NVFP4_SF_RAW && out->sf_layout != NVFP4_SF_ATOM) return NVFP4_ERR_INVALID_ARG;
+    if (out->sf_path != NVFP4_SF_FUSED && out->sf_path != NVFP4_SF_RELAYOUT) return NVFP4_ERR_INVALID_ARG;
+    if (out->cache_b_scales != 0 && out->cache_b_scales != 1) return NVFP4_ERR_INVALID_ARG;
+    if (out->tile_n != 0 && out->tile_n != 64 && out->tile_n != 128) return NVFP4_ERR_INVALID_ARG;
+    if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
+    if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
+    return NVFP4_OK;
+}
+
+// Picks the tile width: among the kernel variants, the one whose units fill
+// the persistent grid in the fewest waves (ties: the wider tile, which reads
+// A fewer times).
+int choose_tile_n(const std::vector<int32_t> &M, int N, int sm_count)
+{
+    double best_cost = 1e300;
+    int best = 128;
+    for (int bn : {128, 64}) {
+        long units = 0;
+        for (int32_t m : M) {
+            const int mt = ceil_div(m, kTileM);
+            units += (long)ceil_div(mt, 2) * ceil_div(N, bn);
+        }
+        if (units == 0) return 128;
+        const long waves = (units + sm_count - 1) / sm_count;
+        // per-wave time ~ B strip bytes (bn) plus a fixed per-unit cost
+        const double cost = (double)waves * ((double)bn + 16.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *const *A, const void *const *B,
+                const void *const *SFA, const void *const *SFB, void *const *C, bool force_sfb, int *njobs_out)
+{
+    std::memset(tab, 0, p->table_bytes);
+    auto *groups = reinterpret_cast<GroupDesc *>(tab);
+    auto *prefix = reinterpret_cast<int32_t *>(tab + p->off_prefix);
+    auto *jobs = reinterpret_cast<RelayoutJob *>(tab + p->off_jobs);
+    const int K = p->K, N = p->N, BN = p->var.tile_n;
+    int njobs = 0, items = 0;
+    const int pieces = K / 256;
+    for (int g = 0; g <= p->G; ++g) prefix[g] = p->unit_prefix[g];
+    for (int g = 0; g < p->G; ++g) {
+        GroupDesc &d = groups[g];
+        d.M = p->M[g];
+        d.m_tiles = p->m_tiles[g];
+        d.m_groups = p->m_groups[g];
+        d.unit_begin = p->unit_prefix[g];
+        if (p->M[g] == 0) continue;
+        const uint64_t Mg = (uint64_t)p->M[g];
+        bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A[g], K / 2, Mg, K / 2, kTileK / 2, kTileM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  encode_2d(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B[g], K / 2, N, K / 2, kTileK / 2, BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  encode_2d(&d.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C[g], N, Mg, (uint64_t)N * 2, 64, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return false;
+        if (p->fused()) {
+            ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA[g], K / 16, Mg, K / 16, kTileK / 16, kTileM,
+                           CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 encode_2d(&d.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB[g], K / 16, N, K / 16, kTileK / 16, BN,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (!ok) return false;
+        } else if (p->relayout()) {
+            d.sfa_atoms = p->d_ws + p->ws_sfa[g];
+            d.sfb_atoms = p->d_ws + p->ws_sfb[g];
+            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFA[g]), p->d_ws + p->ws_sfa[g], p->M[g], items};
+            items += ceil_div(p->M[g], 128) * pieces;
+            ++njobs;
+        } else {
+            d.sfa_atoms = static_cast<const uint8_t *>(SFA[g]);
+            d.sfb_atoms = static_cast<const uint8_t *>(SFB[g]);
+        }
+    }
+    if (p->relayout() && (force_sfb || !p->opt.cache_b_scales)) {
+        for (int g = 0; g < p->G; ++g) {
+            if (p->M[g] == 0) continue;
+            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], N, items};
+            items += ceil_div(N, 128) * pieces;
+            ++njobs;
+        }
+    }
+    (void)dtab;
+    *njobs_out = njobs;
+    return true;
+}
+
+int relayout_items(nvfp4_ggemm_plan_s *p, bool with_sfb)
+{
+    const int pieces = p->K / 256;
+    int items = 0;
+    for (int g = 0; g < p->G; ++g) {
+        if (p->M[g] == 0) continue;
+        items += ceil_div(p->M[g], 128) * pieces;
+        if (with_sfb) items += ceil_div(p->N, 128) * pieces;
+    }
+    return items;
+}
+
+nvfp4_status_t check_group_ptrs(nvfp4_ggemm_plan_s *p, const void *const *A, const void *const *B,
+                                const void *const *SFA, const void *const *SFB, void *const *C, bool need_sfb)
+{
+    if (!A || !B || !SFA || !C || (need_sfb && !SFB)) return NVFP4_ERR_INVALID_ARG;
+    for (int g = 0; g < p->G; ++g) {
+        if (p->M[g] == 0) continue;
+        if (!A[g] || !B[g] || !SFA[g] || !C[g] || (need_sfb && !SFB[g])) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(C[g]) ||
+            (need_sfb && !aligned16(SFB[g])))
+            return NVFP4_ERR_ALIGNMENT;
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const void *const *B,
+                          const void *const *SFA, const void *const *SFB, void *const *C, cudaStream_t stream,
+                          bool force_sfb)
+{
+    const bool sfb_cached = p->relayout() && p->opt.cache_b_scales && !force_sfb;
+    if (sfb_cached && !p->b_prepared) return NVFP4_ERR_NOT_PREPARED;
+    nvfp4_status_t st = check_group_ptrs(p, A, B, SFA, SFB, C, !sfb_cached);
+    if (st != NVFP4_OK) return st;
+    if (p->total_units == 0) return NVFP4_OK;
+
+    std::vector<const void *> key;
+    key.reserve(5 * (size_t)p->G + 1);
+    for (int g = 0; g < p->G; ++g) {
+        const bool on = p->M[g] > 0;
+        key.push_back(on ? A[g] : nullptr);
+        key.push_back(on ? B[g] : nullptr);
+        key.push_back(on ? SFA[g] : nullptr);
+        key.push_back(on && !sfb_cached ? SFB[g] : nullptr);
+        key.push_back(on ? C[g] : nullptr);
+    }
+    key.push_back(reinterpret_cast<const void *>(static_cast<uintptr_t>(force_sfb ? 1 : 0)));
+
+    int slot = p->cur;
+    if (slot < 0 || p->slots[slot].key != key) {
+        slot = (p->cur + 1) % kSlots;
+        Slot &s = p->slots[slot];
+        if (s.used && cudaEventSynchronize(s.ev) != cudaSuccess) return NVFP4_ERR_CUDA;
+        int njobs = 0;
+        if (!fill_table(p, s.h_table, s.d_table, A, B, SFA, SFB, C, force_sfb, &njobs)) return NVFP4_ERR_CUDA;
+        if (cudaMemcpyAsync(s.d_table, s.h_table, p->table_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        s.key = key;
+        p->cur = slot;
+    }
+    Slot &s = p->slots[slot];
+
+    if (p->relayout()) {
+        RelayoutParams rp{};
+        rp.jobs = reinterpret_cast<const RelayoutJob *>(s.d_table + p->off_jobs);
+        int nj = 0;
+        for (int g = 0; g < p->G; ++g) nj += p->M[g] > 0 ? 1 : 0;
+        rp.njobs = sfb_cached ? nj : 2 * nj;
+        rp.K = p->K;
+        rp.total_items = relayout_items(p, !sfb_cached);
+        if (relayout_launch(rp, p->sm_count, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+
+    GemmParams gp{};
+    gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
+    gp.unit_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
+    gp.err = p->d_err;
+    gp.timeout_ns = p->opt.wait_timeout_ns;
+    gp.G = p->G;
+    gp.N = p->N;
+    gp.K = p->K;
+    gp.k_tiles = p->k_tiles;
+    gp.total_units = p->total_units;
+    gp.debug_skip_load = p->opt.debug_skip_load;
+    if (ggemm_launch(p->variant, gp, p->grid, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaEventRecord(s.ev, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    s.used = true;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
+{
+    if (!opt) return;
+    std::memset(opt, 0, sizeof(*opt));
+    opt->struct_size = sizeof(nvfp4_ggemm_options_t);
+    opt->sf_layout = NVFP4_SF_RAW;
+    opt->sf_path = NVFP4_SF_FUSED;
+    opt->cache_b_scales = 0;
+    opt->wait_timeout_ns = kDefaultTimeoutNs;
+    opt->tile_n = 0;
+    opt->max_ctas = 0;
+    opt->debug_skip_load = 0;
+}
+
+nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_groups, const int32_t *M, int32_t N,
+                                int32_t K, const nvfp4_ggemm_options_t *opt_in)
+{
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_groups < 1 || num_groups > kMaxGroups || !M || device < 0) return NVFP4_ERR_INVALID_ARG;
+    for (int g = 0; g < num_groups; ++g)
+        if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
+    if (N < 8 || N > kMaxN || K < 256 || K > kMaxK) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (N % 8 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    nvfp4_ggemm_options_t opt;
+    nvfp4_status_t st = validate_options(opt_in, &opt);
+    if (st != NVFP4_OK) return st;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+        cudaGetLastError();
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    }
+    DeviceGuard guard(device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (major != 10 || minor != 3) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (!load_encode()) return NVFP4_ERR_CUDA;
+
+    auto *p = new (std::nothrow) nvfp4_ggemm_plan_s();
+    if (!p) return NVFP4_ERR_CUDA;
+    p->device = device;
+    p->sm_count = sms;
+    p->G = num_groups;
+    p->N = N;
+    p->K = K;
+    p->M.assign(M, M + num_groups);
+    p->opt = opt;
+    p->k_tiles = K / kTileK;
+
+    const int tile_n = opt.tile_n ? opt.tile_n : choose_tile_n(p->M, N, sms);
+    p->variant = ggemm_variant_index(tile_n, p->fused());
+    if (p->variant < 0) {
+        release(p);
+        return NVFP4_ERR_INVALID_ARG;
+    }
+    p->var = ggemm_variant(p->variant);
+    if (ggemm_configure(p->variant) != cudaSuccess) {
+        release(p);
+        return NVFP4_ERR_CUDA;
+    }
+
+    const int MT = p->var.m_tiles;
+    const int strips = ceil_div(N, tile_n);
+    p->unit_prefix.assign(num_groups + 1, 0);
+    p->m_tiles.assign(num_groups, 0);
+    p->m_groups.assign(num_groups, 0);
+    long total = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        p->m_tiles[g] = ceil_div(M[g], kTileM);
+        p->m_groups[g] = ceil_div(p->m_tiles[g], MT);
+        p->unit_prefix[g] = (int32_t)total;
+        total += (long)p->m_groups[g] * strips;
+    }
+    if (total > 0x7FFFFFFF) {
+        release(p);
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    }
+    p->unit_prefix[num_groups] = (int32_t)total;
+    p->total_units = (int)total;
+    const int cap = opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms;
+    p->grid = std::max(1, std::min(p->total_units, cap));
+
+    p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
+    p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
+    p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
+
+    bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&
+              cudaMemset(p->d_err, 0, sizeof(uint32_t)) == cudaSuccess;
+    for (Slot &s : p->slots) {
+        ok = ok && cudaMallocHost(&s.h_table, p->table_bytes) == cudaSuccess &&
+             cudaMalloc(&s.d_table, p->table_bytes) == cudaSuccess &&
+             cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (ok && p->relayout()) {
+        size_t off = 0;
+        p->ws_sfa.assign(num_groups, 0);
+        p->ws_sfb.assign(num_groups, 0);
+        for (int g = 0; g < num_groups; ++g) {
+            p->ws_sfa[g] = off;
+            off = align_up(off + atom_bytes(M[g], K), 256);
+        }
+        for (int g = 0; g < num_groups; ++g) {
+            p->ws_sfb[g] = off;
+            off = align_up(off + atom_bytes(N, K), 256);
+        }
+        ok = cudaMalloc(&p->d_ws, std::max<size_t>(off, 256)) == cudaSuccess &&
+             cudaMalloc(&p->d_prep_jobs, sizeof(RelayoutJob) * (size_t)num_groups) == cudaSuccess &&
+             cudaMallocHost(&p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)num_groups) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->ev_prep, cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        release(p);
+        return NVFP4_ERR_CUDA;
+    }
+    *out = p;
+    return NVFP4_OK;
+}
+
+nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *const *A, const void *const *B,
+                               const void *const *SFA, const void *const *SFB, void *const *C, void *stream)
+{
+    if (!plan) return NVFP4_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    nvfp4_status_t st = run_device(plan, A, B, SFA, SFB, C, static_cast<cudaStream_t>(stream), false);
+    if (st == NVFP4_ERR_CUDA) cudaGetLastError();
+    return st;
+}
+
+nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *A, const void *const *B,
+                                    const void *const *SFA, const void *const *SFB, void *const *C, void *stream)
+{
+    if (!plan) return NVFP4_ERR_INVALID_ARG;
+    if (!A || !B || !SFA || !SFB || !C) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_ggemm_plan_s *p = plan;
+    for (int g = 0; g < p->G; ++g)
+        if (p->M[g] > 0 && (!A[g] || !B[g] || !SFA[g] || !SFB[g] || !C[g])) return NVFP4_ERR_INVALID_ARG;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t K = (size_t)p->K, N = (size_t)p->N;
+    auto sf_bytes = [&](size_t rows) -> size_t { return p->raw() ? rows * K / 16 : (size_t)atom_bytes(rows, K); };
+    if (!p->d_io) {
+        size_t off = 0;
+        p->io_a.assign(p->G, 0);
+        p->io_b.assign(p->G, 0);
+        p->io_sfa.assign(p->G, 0);
+        p->io_sfb.assign(p->G, 0);
+        p->io_c.assign(p->G, 0);
+        for (int g = 0; g < p->G; ++g) {
+            const size_t m = (size_t)p->M[g];
+            p->io_a[g] = off, off = align_up(off + m * K / 2, 256);
+            p->io_b[g] = off, off = align_up(off + N * K / 2, 256);
+            p->io_sfa[g] = off, off = align_up(off + sf_bytes(m), 256);
+            p->io_sfb[g] = off, off = align_up(off + sf_bytes(N), 256);
+            p->io_c[g] = off, off = align_up(off + m * N * 2, 256);
+        }
+        p->io_bytes = std::max<size_t>(off, 256);
+        if (cudaMalloc(&p->d_io, p->io_bytes) != cudaSuccess) {
+            p->d_io = nullptr;
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    std::vector<const void *> dA(p->G), dB(p->G), dSFA(p->G), dSFB(p->G);
+    std::vector<void *> dC(p->G);
+    for (int g = 0; g < p->G; ++g) {
+        const size_t m = (size_t)p->M[g];
+        dA[g] = p->d_io + p->io_a[g];
+        dB[g] = p->d_io + p->io_b[g];
+        dSFA[g] = p->d_io + p->io_sfa[g];
+        dSFB[g] = p->d_io + p->io_sfb[g];
+        dC[g] = p->d_io + p->io_c[g];
+        if (m == 0) continue;
+        if (cudaMemcpyAsync(const_cast<void *>(dA[g]), A[g], m * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(const_cast<void *>(dB[g]), B[g], N * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(const_cast<void *>(dSFA[g]), SFA[g], sf_bytes(m), cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(const_cast<void *>(dSFB[g]), SFB[g], sf_bytes(N), cudaMemcpyHostToDevice, s) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), s, true);
+    if (st != NVFP4_OK) {
+        cudaGetLastError();
+        return st;
+    }
+    for (int g = 0; g < p->G; ++g) {
+        const size_t m = (size_t)p->M[g];
+        if (m == 0) continue;
+        if (cudaMemcpyAsync(C[g], dC[g], m * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void *const *SFB, void *stream)
+{
+    if (!plan || !SFB) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_ggemm_plan_s *p = plan;
+    if (!p->relayout() || !p->opt.cache_b_scales) return NVFP4_ERR_INVALID_ARG;
+    for (int g = 0; g < p->G; ++g) {
+        if (p->M[g] == 0) continue;
+        if (!SFB[g]) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(SFB[g])) return NVFP4_ERR_ALIGNMENT;
+    }
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->prep_used && cudaEventSynchronize(p->ev_prep) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const int pieces = p->K / 256;
+    int nj = 0, items = 0;
+    for (int g = 0; g < p->G; ++g) {
+        if (p->M[g] == 0) continue;
+        p->h_prep_jobs[nj++] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N, items};
+        items += ceil_div(p->N, 128) * pieces;
+    }
+    if (nj > 0) {
+        if (cudaMemcpyAsync(p->d_prep_jobs, p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)nj, cudaMemcpyHostToDevice,
+                            s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        RelayoutParams rp{};
+        rp.jobs = p->d_prep_jobs;
+        rp.njobs = nj;
+        rp.K = p->K;
+        rp.total_items = items;
+        if (relayout_launch(rp, p->sm_count, s) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    if (cudaEventRecord(p->ev_prep, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    p->prep_used = true;
+    p->b_prepared = true;
+    return NVFP4_OK;
+}
+
+nvfp4_status_t nvfp4_ggemm_sync_status(nvfp4_ggemm_plan_t plan, void *stream, uint32_t *detail)
+{
+    if (detail) *detail = 0;
+    if (!plan) return NVFP4_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, plan->d_err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    if (detail) *detail = word;
+    if (word == 0) return NVFP4_OK;
+    if (cudaMemset(plan->d_err, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    const uint32_t code = word & 0xFFu;
+    return (code == NVFP4_ERR_TIMEOUT) ? NVFP4_ERR_TIMEOUT : NVFP4_ERR_DEVICE_FAULT;
+}
+
+nvfp4_status_t nvfp4_ggemm_destroy(nvfp4_ggemm_plan_t plan)
+{
+    if (!plan) return NVFP4_OK;
+    DeviceGuard guard(plan->device);
+    release(plan);
+    return NVFP4_OK;
+}
+
+nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_t K, void *stream)
+{
+    if (!in || !out || rows < 1 || rows > (1 << 24)) return NVFP4_ERR_INVALID_ARG;
+    if (K < 256 || K > kMaxK || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(in) || !aligned16(out)) return NVFP4_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    }
+    RelayoutParams rp{};
+    rp.jobs = nullptr;
+    rp.single = RelayoutJob{static_cast<const uint8_t *>(in), static_cast<uint8_t *>(out), rows, 0};
+    rp.njobs = 1;
+    rp.K = K;
+    rp.total_items = ceil_div(rows, 128) * (K / 256);
+    if (relayout_launch(rp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K)
+{
+    if (rows < 0 || K < 64 || K % 64 != 0) return 0;
+    return atom_bytes(rows, K);
+}
+
+nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info)
+{
+    if (!plan || !info) return NVFP4_ERR_INVALID_ARG;
+    info->tile_n = plan->var.tile_n;
+    info->m_tiles_per_unit = plan->var.m_tiles;
+    info->stages = plan->var.stages;
+    info->units = plan->total_units;
+    info->grid = plan->grid;
+    info->sm_count = plan->sm_count;
+    info->smem_bytes = ggemm_smem_bytes(plan->variant);
+    info->kernels_per_run = plan->total_units == 0 ? 0 : (plan->relayout() ? 2 : 1);
+    return NVFP4_OK;
+}
+
+const char *nvfp4_status_string(nvfp4_status_t status)
+{
+    switch (status) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need K % 256 == 0, N % 8 == 0, sizes in range)";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "no usable device (needs compute capability 10.3, GB300)";
+    case NVFP4_ERR_CUDA: return "CUDA call failed";
+    case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case NVFP4_ERR_DEVICE_FAULT: return "device-side check failed";
+    case NVFP4_ERR_NOT_PREPARED: return "B scales not prepared (call nvfp4_ggemm_prepare_b_scales)";
+    }
+    return "unknown status";
+}
+
+int nvfp4_ggemm_version(void) { return kVersion; }
+
+}  // extern "C"

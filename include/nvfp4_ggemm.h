@@ -1,0 +1,199 @@
+/*
+ * nvfp4_ggemm.h - C ABI of the NVFP4 block-scaled grouped GEMM for GB300
+ * (sm_103a).
+ *
+ * The operation (nvfp4_group_gemm leaderboard problem; custom_kernel
+ * docstring and kernel comment "C = A * SFA * B * SFB" of kernelindex
+ * submission 503584): for every group g = 0..G-1
+ *
+ *     C_g[m, n] = fp16( sum_{k<K} e2m1(A_g[m,k]) * e4m3(SFA_g[m, k/16])
+ *                                * e2m1(B_g[n,k]) * e4m3(SFB_g[n, k/16]) )
+ *
+ * for m < M_g, n < N. Products accumulate in fp32 on the tensor cores and
+ * the result is rounded to fp16 (round to nearest even) once.
+ *
+ * Layouts (all dense, row-major, K-major for the inputs; device memory):
+ *   A[g]    M_g x K/2 bytes. Two E2M1 codes per byte, the even k in the low
+ *           nibble (the pages' float4e2m1fn_x2 tensors [m, k//2]).
+ *   B[g]    N x K/2 bytes, same packing.
+ *   SFA[g]  E4M3 (FN: bias 7, no infinity) scale codes, one per 16 k.
+ *           NVFP4_SF_RAW: M_g x K/16 bytes, row-major.
+ *           NVFP4_SF_ATOM: the 128x4 atom layout the tensor cores read
+ *           (ceil(M_g/128) * (K/64) atoms of 512 bytes; see
+ *           nvfp4_sf_relayout), as the pages' pre-reordered scale tensors.
+ *   SFB[g]  N x K/16 bytes (raw) or ceil(N/128)*(K/64)*512 bytes (atom).
+ *   C[g]    M_g x N fp16, row-major (row stride N elements).
+ *
+ * Requirements (checked before anything is enqueued): 1 <= G <= 1024,
+ * 0 <= M_g <= 2^20, 8 <= N <= 2^20 with N % 8 == 0 (16-byte C rows), 256 <= K
+ * <= 2^18 with K % 256 == 0 (the kernel's k tile; the K % 256 rule is the one
+ * the TMA helper of submission 498317 enforces), every pointer of a group
+ * with M_g > 0 non-null and 16-byte aligned (the TMA rule). A group with
+ * M_g == 0 is skipped and its pointers are not read.
+ *
+ * Ownership: the caller owns every tensor and the host arrays of pointers;
+ * the arrays are read during the call only. A plan owns its device problem
+ * table, pinned staging, scale workspace and device error word.
+ *
+ * Execution: nvfp4_ggemm_run enqueues work on `stream` and returns; buffers
+ * must stay valid until the stream reaches that point. One plan may be used
+ * from one host thread at a time; calls on different streams must not
+ * overlap on the device (the plan's workspace is shared between calls).
+ *
+ * Errors: every call returns a status; nothing throws or aborts across the
+ * ABI. Argument errors return before any work is enqueued. Device-side
+ * failures (a pipeline wait that ran past the plan's timeout) are recorded
+ * in the plan's device error word and reported by nvfp4_ggemm_sync_status.
+ */
+#ifndef NVFP4_GGEMM_H
+#define NVFP4_GGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null, negative or out-of-range argument */
+    NVFP4_ERR_ALIGNMENT = 2,         /* a tensor pointer is not 16-byte aligned */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 3, /* K % 256 != 0, N % 8 != 0, size limits */
+    NVFP4_ERR_UNSUPPORTED_DEVICE = 4,/* no device, or not compute capability 10.3 */
+    NVFP4_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+    NVFP4_ERR_TIMEOUT = 6,           /* a device pipeline wait exceeded the timeout */
+    NVFP4_ERR_DEVICE_FAULT = 7,      /* a device-side consistency check failed */
+    NVFP4_ERR_NOT_PREPARED = 8       /* cache_b_scales set but scales not prepared */
+} nvfp4_status_t;
+
+/* Layout of the scale tensors passed to run / prepare. */
+enum { NVFP4_SF_RAW = 0, NVFP4_SF_ATOM = 1 };
+
+/* How raw scales reach the tensor cores. */
+enum {
+    NVFP4_SF_FUSED = 0,   /* one kernel: raw 128x16-byte scale tiles are loaded by TMA and
+                             permuted into the atom layout in shared memory */
+    NVFP4_SF_RELAYOUT = 1 /* the re-layout kernel writes atom-layout copies into the plan's
+                             workspace, then the GEMM kernel reads those */
+};
+
+typedef struct {
+    uint32_t struct_size;     /* sizeof(nvfp4_ggemm_options_t) */
+    int32_t sf_layout;        /* NVFP4_SF_RAW (default) or NVFP4_SF_ATOM */
+    int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only */
+    int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
+                                 nvfp4_ggemm_prepare_b_scales and run skips it */
+    uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
+    int32_t tile_n;           /* output tile width: 0 = automatic, else 64 or 128 */
+    int32_t max_ctas;         /* persistent grid size: 0 = number of SMs */
+    int32_t debug_skip_load;  /* test only: 0 = off; n > 0 = the producer of CTA 0 leaves the
+                                 n-th load of its first unit unissued, so the consumer's wait
+                                 runs into the timeout (exercises the error path) */
+    int32_t reserved[5];
+} nvfp4_ggemm_options_t;
+
+typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;
+
+/* Fill `opt` with the defaults listed above. */
+NVFP4_API void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt);
+
+/*
+ * Build a plan for G groups with row counts M[0..G-1] (host array), shared N
+ * and K, on CUDA device `device`. Validates the shape, computes the tile
+ * schedule (prefix sums of the per-group work units), and allocates the
+ * device problem table, scale workspace and error word. `opt` may be NULL
+ * (defaults). On success *out holds the plan; on failure *out is NULL.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_groups,
+                                const int32_t *M, int32_t N, int32_t K,
+                                const nvfp4_ggemm_options_t *opt);
+
+/*
+ * Grouped GEMM on device buffers. A, B, SFA, SFB, C are host arrays of G
+ * device pointers (layouts above; scales in the plan's sf_layout). `stream`
+ * is a cudaStream_t (NULL = legacy default stream). Encodes the per-group
+ * TMA tensor maps when the pointers differ from the previous call, uploads
+ * the problem table, and enqueues the kernels. Asynchronous.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *const *A, const void *const *B,
+                               const void *const *SFA, const void *const *SFB, void *const *C,
+                               void *stream);
+
+/*
+ * The same operation on HOST buffers: copies every input to plan-owned
+ * device buffers (allocated on the first call), runs, and copies C back,
+ * all on `stream`; returns after the stream has drained. Host buffers should
+ * be pinned for the copies to be asynchronous. Scales as in the plan's
+ * sf_layout (cache_b_scales is ignored here).
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *A,
+                                    const void *const *B, const void *const *SFA,
+                                    const void *const *SFB, void *const *C, void *stream);
+
+/*
+ * RELAYOUT path with cache_b_scales: re-lay out the G raw SFB tensors into
+ * the plan's workspace once (B's scales are fixed, e.g. MoE expert
+ * weights). Later runs read the cached copy and ignore their SFB argument.
+ * Asynchronous on `stream`.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void *const *SFB,
+                                            void *stream);
+
+/*
+ * Wait for `stream`, then read and clear the plan's device error word.
+ * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT or NVFP4_ERR_DEVICE_FAULT (or
+ * NVFP4_ERR_CUDA when the synchronisation itself failed). `detail` (may be
+ * NULL) receives the raw error word: bits 0-7 status, 8-15 wait site,
+ * 16-31 block index.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_sync_status(nvfp4_ggemm_plan_t plan, void *stream, uint32_t *detail);
+
+/* Release the plan and everything it owns. NULL is accepted. Synchronises the device. */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_destroy(nvfp4_ggemm_plan_t plan);
+
+/*
+ * Scale re-layout, one matrix: raw row-major E4M3 scales in[rows, K/16] ->
+ * the 128x4 atom layout out[ceil(rows/128) * (K/64) * 512 bytes]. Atom
+ * (rb, kb) covers rows [128rb, 128rb+128) and k in [64kb, 64kb+64) and sits
+ * at byte (rb*(K/64) + kb)*512; inside it the scale of row r, index j = k/16
+ * sits at byte (r%32)*16 + ((r%128)/32)*4 + j%4 (the scale-factor atom of
+ * the CuTe kernel of submission 402102, tiled as in the TMA issue code of
+ * submission 498317). Rows past `rows` are written as zero. in and out are
+ * device pointers, 16-byte aligned; K % 256 == 0; rows >= 1. Asynchronous.
+ */
+NVFP4_API nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_t K, void *stream);
+
+/* Bytes of the atom-layout copy of a [rows, K/16] scale matrix. */
+NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
+
+/* Plan introspection (for tests and benchmarks). */
+typedef struct {
+    int32_t tile_n;        /* output tile width used */
+    int32_t m_tiles_per_unit; /* 128-row tiles that share one B stage */
+    int32_t stages;        /* shared-memory pipeline depth */
+    int32_t units;         /* work units (group, row-tile pair, column strip) */
+    int32_t grid;          /* persistent CTAs launched */
+    int32_t sm_count;
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t kernels_per_run; /* kernel launches enqueued by one run */
+} nvfp4_ggemm_plan_info_t;
+
+NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info);
+
+/* Static string for a status code. */
+NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+NVFP4_API int nvfp4_ggemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GGEMM_H */
