@@ -3,8 +3,8 @@
  * (sm_103a).
  *
  * The operation (nvfp4_group_gemm leaderboard problem; custom_kernel
- * docstring and kernel comment "C = A * SFA * B * SFB" of kernelindex
- * submission 503584): for every group g = 0..G-1
+ * docstring and kernel-launch comment of kernelindex submission 503584):
+ * for every group g = 0..G-1
  *
  *     C_g[m, n] = fp16( sum_{k<K} e2m1(A_g[m,k]) * e4m3(SFA_g[m, k/16])
  *                                * e2m1(B_g[n,k]) * e4m3(SFB_g[n, k/16]) )

@@ -6,9 +6,9 @@
  * the benchmark do. It shares no code, header, table or constant with the
  * CUDA library.
  *
- * What it computes (the plain definition, nvfp4_group_gemm problem as stated
- * in the custom_kernel docstring of submission 503584 and its kernel comment
- * "C = A * SFA * B * SFB"):
+ * What it computes (the plain definition of the nvfp4_group_gemm problem as
+ * the custom_kernel docstring of kernelindex submission 503584 states it, and
+ * the product of A, SFA, B and SFB that its kernel-launch comment names):
  *
  *   C_g[m, n] = RN_fp16( sum_{k=0}^{K-1} e2m1(A_g[m,k]) * e4m3(SFA_g[m, k/16])
  *                                      * e2m1(B_g[n,k]) * e4m3(SFB_g[n, k/16]) )
