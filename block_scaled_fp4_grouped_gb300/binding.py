@@ -46,6 +46,7 @@ EXPORTED = (
     "nvfp4_ggemm_plan_info",
     "nvfp4_status_string",
     "nvfp4_ggemm_version",
+    "nvfp4_ggemm_run_noalloc",
 )
 
 
@@ -127,6 +128,10 @@ def lib() -> ctypes.CDLL:
     L.nvfp4_status_string.argtypes = [ctypes.c_int]
     L.nvfp4_ggemm_version.restype = ctypes.c_int
     L.nvfp4_ggemm_version.argtypes = []
+    L.nvfp4_ggemm_run_noalloc.restype = ctypes.c_int
+    L.nvfp4_ggemm_run_noalloc.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                          ctypes.c_int32, _VPP, _VPP, _VPP, _VPP, _VPP, _VP,
+                                          ctypes.POINTER(ctypes.c_uint32)]
     _lib = L
     return L
 
@@ -237,6 +242,19 @@ def nvfp4_status_string(status: int) -> str:
 
 def nvfp4_ggemm_version() -> int:
     return int(lib().nvfp4_ggemm_version())
+
+
+def nvfp4_ggemm_run_noalloc(M: Sequence[int], N: int, K: int, A, B, SFA, SFB, C, stream=None,
+                            wait: bool = False) -> Tuple[int, int]:
+    """The allocation-free grouped GEMM on the current device (raw scales).
+    With wait=True the call waits for the stream and also returns the device
+    error word. Returns (status, error word)."""
+    m = (ctypes.c_int32 * max(1, len(M)))(*[int(v) for v in M])
+    word = ctypes.c_uint32(0)
+    st = lib().nvfp4_ggemm_run_noalloc(len(M), m, int(N), int(K), _ptr_array(A), _ptr_array(B),
+                                       _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C), _stream(stream),
+                                       ctypes.byref(word) if wait else None)
+    return st, int(word.value)
 
 
 # -------------------------------------------------------------- convenience

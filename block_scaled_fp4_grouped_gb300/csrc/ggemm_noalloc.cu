@@ -1,0 +1,203 @@
+// A grouped-GEMM entry point that allocates nothing, for callers that may
+// not call cudaMalloc: code running under a fixed memory budget or a custom
+// device allocator, code inside a region where allocation would
+// synchronise the device, plugins that must not grow the process's device
+// footprint. The work it needs beyond the caller's inputs and outputs (the
+// per-group tensor maps the kernel reads and the device error word) lives in
+// one file-scope device array that every GPU loading the library holds
+// until the process exits. It runs the same persistent GEMM kernel as
+// nvfp4_ggemm_run on the raw-scale FUSED path with 128-column tiles.
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "ggemm_internal.h"
+#include "nvfp4_ggemm.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kNoAllocMaxGroups = 64;
+constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 48 KB
+constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
+constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
+constexpr size_t kScratchBytes = kErrOffset + 256;
+static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
+
+// The scratch: problem table, unit prefix sums, error word. In host code this
+// name is only a host-side stand-in; the device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+uint8_t *g_scratch_addr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_fn = nullptr;
+
+int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+bool aligned16_p(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t cols, uint64_t rows,
+                uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode_fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// First call on a device (that device current): look up the scratch array's
+// device address, raise the kernel's shared-memory limit, fetch the
+// tensor-map encoder.
+nvfp4_status_t setup_device(int dev, int variant)
+{
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (g_scratch_addr[dev]) return NVFP4_OK;
+    if (!g_encode_fn) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return NVFP4_ERR_CUDA;
+        g_encode_fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (ggemm_configure(variant) != cudaSuccess) return NVFP4_ERR_CUDA;
+    g_sm_count[dev] = sms;
+    g_scratch_addr[dev] = static_cast<uint8_t *>(ptr);
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, const int32_t *M, int32_t N, int32_t K,
+                                                             const void *const *A, const void *const *B,
+                                                             const void *const *SFA, const void *const *SFB,
+                                                             void *const *C, void *stream, uint32_t *status_out)
+{
+    if (status_out) *status_out = 0;
+    // --- arguments (nothing is enqueued before these pass)
+    if (num_groups < 1 || !M || !A || !B || !SFA || !SFB || !C) return NVFP4_ERR_INVALID_ARG;
+    if (num_groups > kNoAllocMaxGroups) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (N < 8 || N > (1 << 20) || N % 8 != 0 || K < 256 || K > (1 << 18) || K % 256 != 0)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    for (int g = 0; g < num_groups; ++g) {
+        if (M[g] < 0 || M[g] > (1 << 20)) return NVFP4_ERR_INVALID_ARG;
+        if (M[g] == 0) continue;
+        if (!A[g] || !B[g] || !SFA[g] || !SFB[g] || !C[g]) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16_p(A[g]) || !aligned16_p(B[g]) || !aligned16_p(SFA[g]) || !aligned16_p(SFB[g]) ||
+            !aligned16_p(C[g]))
+            return NVFP4_ERR_ALIGNMENT;
+    }
+    const int variant = ggemm_variant_index(128, true);
+    if (variant < 0) return NVFP4_ERR_CUDA;
+    const GemmVariant var = ggemm_variant(variant);
+
+    // --- device and one-time set-up
+    int dev = -1, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    nvfp4_status_t st = setup_device(dev, variant);
+    if (st != NVFP4_OK) {
+        cudaGetLastError();
+        return st;
+    }
+    uint8_t *scratch = g_scratch_addr[dev];
+
+    // --- schedule and tensor maps, built in a host buffer on this thread's stack
+    alignas(128) uint8_t table[kTableBytes + 512];
+    std::memset(table, 0, sizeof(table));
+    auto *groups = reinterpret_cast<GroupDesc *>(table);
+    auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
+    const int BN = var.tile_n, MT = var.m_tiles;
+    const int strips = ceil_div_i(N, BN);
+    long total = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        GroupDesc &d = groups[g];
+        d.M = M[g];
+        d.m_tiles = ceil_div_i(M[g], kTileM);
+        d.m_groups = ceil_div_i(d.m_tiles, MT);
+        d.unit_begin = (int32_t)total;
+        prefix[g] = (int32_t)total;
+        total += (long)d.m_groups * strips;
+        if (M[g] == 0) continue;
+        const uint64_t Mg = (uint64_t)M[g];
+        const bool ok =
+            encode_map(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A[g], K / 2, Mg, K / 2, kTileK / 2, kTileM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_map(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B[g], K / 2, N, K / 2, kTileK / 2, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_map(&d.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C[g], N, Mg, (uint64_t)N * 2, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_map(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA[g], K / 16, Mg, K / 16, kTileK / 16, kTileM,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_map(&d.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB[g], K / 16, N, K / 16, kTileK / 16, BN,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!ok) return NVFP4_ERR_CUDA;
+    }
+    prefix[num_groups] = (int32_t)total;
+    if (total == 0) return NVFP4_OK;
+    if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+
+    // --- upload (pageable source: the call returns once the bytes are staged,
+    //     so the stack buffer may go away), clear the error word, launch
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t used = sizeof(GroupDesc) * (size_t)num_groups;
+    if (cudaMemcpyAsync(scratch, table, used, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(scratch + kPrefixOffset, prefix, sizeof(int32_t) * (size_t)(num_groups + 1),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemsetAsync(scratch + kErrOffset, 0, sizeof(uint32_t), s) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    GemmParams gp{};
+    gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
+    gp.unit_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
+    gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
+    gp.timeout_ns = 2000000000ull;
+    gp.G = num_groups;
+    gp.N = N;
+    gp.K = K;
+    gp.k_tiles = K / kTileK;
+    gp.total_units = (int32_t)total;
+    gp.debug_skip_load = 0;
+    const int grid = (int)(total < g_sm_count[dev] ? total : g_sm_count[dev]);
+    if (ggemm_launch(variant, gp, grid, s) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+
+    // --- optional: wait and report the device error word
+    if (status_out) {
+        uint32_t word = 0;
+        if (cudaStreamSynchronize(s) != cudaSuccess ||
+            cudaMemcpy(&word, scratch + kErrOffset, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+        *status_out = word;
+        if (word != 0) return (word & 0xFFu) == NVFP4_ERR_TIMEOUT ? NVFP4_ERR_TIMEOUT : NVFP4_ERR_DEVICE_FAULT;
+    }
+    return NVFP4_OK;
+}

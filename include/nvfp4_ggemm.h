@@ -189,6 +189,39 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_gg
 /* Static string for a status code. */
 NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
 
+/*
+ * Grouped GEMM without any device allocation. There is no counterpart on the
+ * pages: this entry point exists for callers that may not call cudaMalloc
+ * (code under a fixed memory budget or its own device allocator, code in a
+ * region where an allocation would synchronise the device, plugins that must
+ * not grow the process's device footprint). It computes what
+ * nvfp4_ggemm_run computes for raw row-major scales, with the same kernel,
+ * but needs no plan: the per-group tensor maps and the device error word it
+ * needs live in a static device array of 64 KB that every GPU loading the
+ * library holds until the process exits.
+ *
+ * Arguments: as nvfp4_ggemm_plan + nvfp4_ggemm_run (M host array of G row
+ * counts, A/B/SFA/SFB/C host arrays of G device pointers, raw scales), on
+ * the current device. Limits: 1 <= num_groups <= 64, otherwise
+ * NVFP4_ERR_UNSUPPORTED_SHAPE before anything is enqueued; the other checks
+ * and status codes are those of plan/run.
+ *
+ * The first call on a device looks up the array's device address and
+ * configures the kernel; make that first call before any stream capture.
+ * Every call reuses the same array (it keeps the last call's contents; the
+ * error word is cleared at the start of each call), so calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race:
+ * serialise them on one stream. Asynchronous on `stream`; if `status_out`
+ * is not NULL the call waits for the stream and stores the device error
+ * word there (0 = fine), returning NVFP4_ERR_TIMEOUT or
+ * NVFP4_ERR_DEVICE_FAULT when it is not 0. Never calls cudaMalloc,
+ * cudaFree or any other allocating routine.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, const int32_t *M, int32_t N, int32_t K,
+                                                 const void *const *A, const void *const *B,
+                                                 const void *const *SFA, const void *const *SFB,
+                                                 void *const *C, void *stream, uint32_t *status_out);
+
 /* Library version, major*10000 + minor*100 + patch. */
 NVFP4_API int nvfp4_ggemm_version(void);
 
