@@ -160,7 +160,7 @@ def max_over_ranks(world, value: float, device) -> float:
 
 
 def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0, torch=None, flush=None,
-                want_e2e: bool = False):
+                want_e2e: bool = False, tuning=None):
     """Device timing of one config. Returns a dict of measurements."""
     from block_scaled_fp4_grouped_gb300 import binding as nb
     prob = synth.make_problem(name, seed=seed)
@@ -177,6 +177,7 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
         SFA = [_atom(torch, nb, s, m, K) for s, m in zip(SFA, prob.M)]
         SFB = [_atom(torch, nb, s, N, K) for s in SFB]
     C = [torch.empty((m, N), dtype=torch.float16, device="cuda") for m in prob.M]
+    kw.update(tuning or {})
     gg = nb.GroupedGemm(prob.M, N, K, **kw)
     info = gg.info()
     if kw.get("cache_b_scales"):
@@ -323,6 +324,9 @@ def main():
     ap.add_argument("--all-configs", action="store_true", help="also time every config (extra key)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tile-n", type=int, default=0, help="widest output tile (0 = library default)")
+    ap.add_argument("--b-stages", type=int, default=0)
+    ap.add_argument("--a-stages", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -344,8 +348,9 @@ def main():
 
     barrier(world)
     with ClockSampler(local) as clocks:
+        tuning = dict(tile_n=args.tile_n, b_stages=args.b_stages, a_stages=args.a_stages)
         r = time_config(args.config, args.sf_path, args.steps, args.warmup, torch=torch, flush=flush,
-                        want_e2e=not args.no_e2e)
+                        want_e2e=not args.no_e2e, tuning=tuning)
     barrier(world)
     us = max_over_ranks(world, r["us_mean"], device)
     prob = r["prob"]
@@ -359,8 +364,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
         "config": dict(workload_config(args.config, prob), sf_path=args.sf_path,
                        l2="flushed before every timed call (256 MB write)",
-                       tile_n=r["info"].tile_n, grid=r["info"].grid, units=r["info"].units,
-                       stages=r["info"].stages, parallelism=f"replicas x{world}"),
+                       max_tile_n=r["info"].tile_n, grid=r["info"].grid, chunks=r["info"].chunks,
+                       b_stages=r["info"].b_stages, a_stages=r["info"].a_stages,
+                       parallelism=f"replicas x{world}"),
         "us_median": r["us_median"], "us_min": r["us_min"], "us_p90": r["us_p90"],
         "tflops_fp4": tflops, "gbs": achieved_gbs,
         "roofline_fraction": t_roof_us / r["us_mean"],
@@ -381,14 +387,15 @@ def main():
         per = {}
         for name in ["c0", "c1", "c2", "c3", "c4", "c1_page", "c2_page", "c3_page", "c4_page"]:
             for path in ["fused", "relayout", "relayout-cached"]:
-                q = time_config(name, path, max(20, args.steps // 2), args.warmup, torch=torch, flush=flush)
+                q = time_config(name, path, max(20, args.steps // 2), args.warmup, torch=torch, flush=flush,
+                                tuning=tuning if path == args.sf_path else None)
                 t_roof = max(q["flops"] / (fp4_peak_tflops * 1e12), q["bytes"] / (hbm * 1e9)) * 1e6
                 per[f"{name}/{path}"] = {"us_mean": round(q["us_mean"], 2), "us_median": round(q["us_median"], 2),
                                          "us_min": round(q["us_min"], 2),
                                          "gbs": round(q["bytes"] / (q["us_mean"] * 1e-6) / 1e9, 1),
                                          "tflops": round(q["flops"] / (q["us_mean"] * 1e-6) / 1e12, 1),
                                          "roofline_fraction": round(t_roof / q["us_mean"], 3),
-                                         "tile_n": q["info"].tile_n, "units": q["info"].units}
+                                         "chunks": q["info"].chunks, "grid": q["info"].grid}
         line["per_config"] = per
     if rank == 0 and not args.no_cpu_baseline:
         us_cpu, cores, sample = oracle_sample_time(prob, budget_s=10.0)

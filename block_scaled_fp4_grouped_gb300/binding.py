@@ -60,16 +60,18 @@ class nvfp4_ggemm_options_t(ctypes.Structure):
         ("tile_n", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32),
         ("debug_skip_load", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("b_stages", ctypes.c_int32),
+        ("a_stages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
 class nvfp4_ggemm_plan_info_t(ctypes.Structure):
     _fields_ = [
         ("tile_n", ctypes.c_int32),
-        ("m_tiles_per_unit", ctypes.c_int32),
-        ("stages", ctypes.c_int32),
-        ("units", ctypes.c_int32),
+        ("b_stages", ctypes.c_int32),
+        ("a_stages", ctypes.c_int32),
+        ("chunks", ctypes.c_int32),
         ("grid", ctypes.c_int32),
         ("sm_count", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
@@ -261,7 +263,7 @@ def nvfp4_ggemm_run_noalloc(M: Sequence[int], N: int, K: int, A, B, SFA, SFB, C,
 
 def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales: bool = False,
                  wait_timeout_ns: int = 0, tile_n: int = 0, max_ctas: int = 0,
-                 debug_skip_load: int = 0) -> nvfp4_ggemm_options_t:
+                 debug_skip_load: int = 0, b_stages: int = 0, a_stages: int = 0) -> nvfp4_ggemm_options_t:
     opt = nvfp4_ggemm_default_options()
     opt.sf_layout = {"raw": NVFP4_SF_RAW, "atom": NVFP4_SF_ATOM}[sf_layout]
     opt.sf_path = {"fused": NVFP4_SF_FUSED, "relayout": NVFP4_SF_RELAYOUT}[sf_path]
@@ -271,6 +273,8 @@ def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales:
     opt.tile_n = int(tile_n)
     opt.max_ctas = int(max_ctas)
     opt.debug_skip_load = int(debug_skip_load)
+    opt.b_stages = int(b_stages)
+    opt.a_stages = int(a_stages)
     return opt
 
 

@@ -1,7 +1,7 @@
-// Host side of the C ABI: argument validation, the tile schedule (prefix
-// sums of work units), per-group TMA tensor maps in a device-resident
-// problem table, workspace for re-laid-out scales, kernel launches and the
-// device error word.
+// Host side of the C ABI: argument validation, the work decomposition
+// (prefix sums of column chunks), per-group TMA tensor maps in a
+// device-resident problem table, workspace for re-laid-out scales, kernel
+// launches and the device error word.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -24,6 +24,7 @@ constexpr int32_t kMaxN = 1 << 20;
 constexpr int32_t kMaxK = 1 << 18;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kSlots = 4;  // problem-table ring: a table is rewritten only after its last kernel finished
+constexpr int kDefaultTileN = 192;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -80,6 +81,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
     return r == CUDA_SUCCESS;
 }
 
+// Smallest kernel tile width (128 or 192) that holds `tile_n` columns.
+int variant_width(int tile_n) { return tile_n <= 128 ? 128 : 192; }
+
 struct Slot {
     uint8_t *h_table = nullptr;  // pinned staging
     uint8_t *d_table = nullptr;
@@ -90,6 +94,46 @@ struct Slot {
 
 }  // namespace
 
+namespace nvfp4 {
+
+TensorMapEncodeFn tensor_map_encoder()
+{
+    return load_encode() ? reinterpret_cast<TensorMapEncodeFn>(g_encode) : nullptr;
+}
+
+bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
+                     const void *SFB, void *C, bool sf_raw, int wide_rows)
+{
+    if (!load_encode()) return false;
+    const uint64_t Mg = (uint64_t)M;
+    d.M = M;
+    d.m_tiles = ceil_div(M, kTileM);
+    d.m_pairs = ceil_div(d.m_tiles, kRowTilesPerUnit);
+    d.b_keep = d.m_pairs > 1 ? 1 : 0;
+    d.C = static_cast<uint16_t *>(C);
+    bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kTileM,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&d.tmB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&d.tmBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, wide_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return false;
+    if (sf_raw) {
+        ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, kTileK / 16, kTileM,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
+             encode_2d(&d.tmSFB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, kTileK / 16, 32,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
+             encode_2d(&d.tmSFBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, kTileK / 16, wide_rows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        d.sfa_atoms = static_cast<const uint8_t *>(SFA);
+        d.sfb_atoms = static_cast<const uint8_t *>(SFB);
+    }
+    return ok;
+}
+
+}  // namespace nvfp4
+
 struct nvfp4_ggemm_plan_s {
     int device = 0;
     int sm_count = 0;
@@ -99,9 +143,11 @@ struct nvfp4_ggemm_plan_s {
     int variant = -1;
     GemmVariant var{};
     int grid = 0;
-    int total_units = 0;
+    int total_chunks = 0;
+    int n_chunks = 0;
+    int max_tile_chunks = 8;
     int k_tiles = 0;
-    std::vector<int32_t> m_tiles, m_groups, unit_prefix;
+    std::vector<int32_t> m_tiles, m_pairs, chunk_prefix;
     size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
     Slot slots[kSlots];
     int cur = -1;
@@ -157,35 +203,16 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
     if (out->sf_layout != NVFP4_SF_RAW && out->sf_layout != NVFP4_SF_ATOM) return NVFP4_ERR_INVALID_ARG;
     if (out->sf_path != NVFP4_SF_FUSED && out->sf_path != NVFP4_SF_RELAYOUT) return NVFP4_ERR_INVALID_ARG;
     if (out->cache_b_scales != 0 && out->cache_b_scales != 1) return NVFP4_ERR_INVALID_ARG;
-    if (out->tile_n != 0 && out->tile_n != 64 && out->tile_n != 128) return NVFP4_ERR_INVALID_ARG;
+    if (out->tile_n == 0) out->tile_n = kDefaultTileN;
+    if (out->tile_n < kChunkN || out->tile_n > kMaxTileN || out->tile_n % kChunkN != 0) return NVFP4_ERR_INVALID_ARG;
+    if (out->b_stages < 0 || out->a_stages < 0 || (out->b_stages == 0) != (out->a_stages == 0))
+        return NVFP4_ERR_INVALID_ARG;
+    const bool raw_fused = out->sf_layout == NVFP4_SF_RAW && out->sf_path == NVFP4_SF_FUSED;
+    if (ggemm_variant_index(variant_width(out->tile_n), out->b_stages, out->a_stages, raw_fused) < 0)
+        return NVFP4_ERR_INVALID_ARG;
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
     return NVFP4_OK;
-}
-
-// Picks the tile width: among the kernel variants, the one whose units fill
-// the persistent grid in the fewest waves (ties: the wider tile, which reads
-// A fewer times).
-int choose_tile_n(const std::vector<int32_t> &M, int N, int sm_count)
-{
-    double best_cost = 1e300;
-    int best = 128;
-    for (int bn : {128, 64}) {
-        long units = 0;
-        for (int32_t m : M) {
-            const int mt = ceil_div(m, kTileM);
-            units += (long)ceil_div(mt, 2) * ceil_div(N, bn);
-        }
-        if (units == 0) return 128;
-        const long waves = (units + sm_count - 1) / sm_count;
-        // per-wave time ~ B strip bytes (bn) plus a fixed per-unit cost
-        const double cost = (double)waves * ((double)bn + 16.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = bn;
-        }
-    }
-    return best;
 }
 
 bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *const *A, const void *const *B,
@@ -195,41 +222,28 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     auto *groups = reinterpret_cast<GroupDesc *>(tab);
     auto *prefix = reinterpret_cast<int32_t *>(tab + p->off_prefix);
     auto *jobs = reinterpret_cast<RelayoutJob *>(tab + p->off_jobs);
-    const int K = p->K, N = p->N, BN = p->var.tile_n;
+    const int K = p->K, N = p->N;
     int njobs = 0, items = 0;
     const int pieces = K / 256;
-    for (int g = 0; g <= p->G; ++g) prefix[g] = p->unit_prefix[g];
+    for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
         d.M = p->M[g];
         d.m_tiles = p->m_tiles[g];
-        d.m_groups = p->m_groups[g];
-        d.unit_begin = p->unit_prefix[g];
+        d.m_pairs = p->m_pairs[g];
+        d.chunk_begin = p->chunk_prefix[g];
         if (p->M[g] == 0) continue;
-        const uint64_t Mg = (uint64_t)p->M[g];
-        bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A[g], K / 2, Mg, K / 2, kTileK / 2, kTileM,
-                            CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_2d(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B[g], K / 2, N, K / 2, kTileK / 2, BN,
-                            CU_TENSOR_MAP_SWIZZLE_128B) &&
-                  encode_2d(&d.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C[g], N, Mg, (uint64_t)N * 2, 64, 32,
-                            CU_TENSOR_MAP_SWIZZLE_128B);
-        if (!ok) return false;
-        if (p->fused()) {
-            ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA[g], K / 16, Mg, K / 16, kTileK / 16, kTileM,
-                           CU_TENSOR_MAP_SWIZZLE_NONE) &&
-                 encode_2d(&d.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB[g], K / 16, N, K / 16, kTileK / 16, BN,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-            if (!ok) return false;
-        } else if (p->relayout()) {
-            d.sfa_atoms = p->d_ws + p->ws_sfa[g];
-            d.sfb_atoms = p->d_ws + p->ws_sfb[g];
+        const void *sfa = SFA[g];
+        const void *sfb = SFB ? SFB[g] : nullptr;
+        if (p->relayout()) {
+            sfa = p->d_ws + p->ws_sfa[g];
+            sfb = p->d_ws + p->ws_sfb[g];
             jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFA[g]), p->d_ws + p->ws_sfa[g], p->M[g], items};
             items += ceil_div(p->M[g], 128) * pieces;
             ++njobs;
-        } else {
-            d.sfa_atoms = static_cast<const uint8_t *>(SFA[g]);
-            d.sfb_atoms = static_cast<const uint8_t *>(SFB[g]);
         }
+        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->var.max_n)) return false;
+        d.chunk_begin = p->chunk_prefix[g];
     }
     if (p->relayout() && (force_sfb || !p->opt.cache_b_scales)) {
         for (int g = 0; g < p->G; ++g) {
@@ -278,7 +292,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     if (sfb_cached && !p->b_prepared) return NVFP4_ERR_NOT_PREPARED;
     nvfp4_status_t st = check_group_ptrs(p, A, B, SFA, SFB, C, !sfb_cached);
     if (st != NVFP4_OK) return st;
-    if (p->total_units == 0) return NVFP4_OK;
+    if (p->total_chunks == 0) return NVFP4_OK;
 
     std::vector<const void *> key;
     key.reserve(5 * (size_t)p->G + 1);
@@ -319,14 +333,17 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
 
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
-    gp.unit_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
+    gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
     gp.N = p->N;
     gp.K = p->K;
     gp.k_tiles = p->k_tiles;
-    gp.total_units = p->total_units;
+    gp.n_chunks = p->n_chunks;
+    gp.total_chunks = p->total_chunks;
+    gp.max_tile_chunks = p->max_tile_chunks;
+    gp.wide_rows = p->var.max_n;
     gp.debug_skip_load = p->opt.debug_skip_load;
     if (ggemm_launch(p->variant, gp, p->grid, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (cudaEventRecord(s.ev, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -350,6 +367,8 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->tile_n = 0;
     opt->max_ctas = 0;
     opt->debug_skip_load = 0;
+    opt->b_stages = 0;
+    opt->a_stages = 0;
 }
 
 nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_groups, const int32_t *M, int32_t N,
@@ -392,8 +411,7 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     p->opt = opt;
     p->k_tiles = K / kTileK;
 
-    const int tile_n = opt.tile_n ? opt.tile_n : choose_tile_n(p->M, N, sms);
-    p->variant = ggemm_variant_index(tile_n, p->fused());
+    p->variant = ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused());
     if (p->variant < 0) {
         release(p);
         return NVFP4_ERR_INVALID_ARG;
@@ -404,26 +422,27 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
         return NVFP4_ERR_CUDA;
     }
 
-    const int MT = p->var.m_tiles;
-    const int strips = ceil_div(N, tile_n);
-    p->unit_prefix.assign(num_groups + 1, 0);
+    // Work decomposition: m_pairs_g x ceil(N/32) chunks per group, prefix-summed.
+    p->max_tile_chunks = opt.tile_n / kChunkN;
+    p->n_chunks = ceil_div(N, kChunkN);
+    p->chunk_prefix.assign(num_groups + 1, 0);
     p->m_tiles.assign(num_groups, 0);
-    p->m_groups.assign(num_groups, 0);
+    p->m_pairs.assign(num_groups, 0);
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         p->m_tiles[g] = ceil_div(M[g], kTileM);
-        p->m_groups[g] = ceil_div(p->m_tiles[g], MT);
-        p->unit_prefix[g] = (int32_t)total;
-        total += (long)p->m_groups[g] * strips;
+        p->m_pairs[g] = ceil_div(p->m_tiles[g], kRowTilesPerUnit);
+        p->chunk_prefix[g] = (int32_t)total;
+        total += (long)p->m_pairs[g] * p->n_chunks;
     }
     if (total > 0x7FFFFFFF) {
         release(p);
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     }
-    p->unit_prefix[num_groups] = (int32_t)total;
-    p->total_units = (int)total;
+    p->chunk_prefix[num_groups] = (int32_t)total;
+    p->total_chunks = (int)total;
     const int cap = opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms;
-    p->grid = std::max(1, std::min(p->total_units, cap));
+    p->grid = std::max(1, std::min(p->total_chunks, cap));
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
     p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
@@ -655,14 +674,14 @@ uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K)
 nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info)
 {
     if (!plan || !info) return NVFP4_ERR_INVALID_ARG;
-    info->tile_n = plan->var.tile_n;
-    info->m_tiles_per_unit = plan->var.m_tiles;
-    info->stages = plan->var.stages;
-    info->units = plan->total_units;
+    info->tile_n = plan->max_tile_chunks * kChunkN;
+    info->b_stages = plan->var.b_stages;
+    info->a_stages = plan->var.a_stages;
+    info->chunks = plan->total_chunks;
     info->grid = plan->grid;
     info->sm_count = plan->sm_count;
     info->smem_bytes = ggemm_smem_bytes(plan->variant);
-    info->kernels_per_run = plan->total_units == 0 ? 0 : (plan->relayout() ? 2 : 1);
+    info->kernels_per_run = plan->total_chunks == 0 ? 0 : (plan->relayout() ? 2 : 1);
     return NVFP4_OK;
 }
 

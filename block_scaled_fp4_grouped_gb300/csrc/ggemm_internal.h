@@ -1,5 +1,5 @@
-// Shared between the host plan code and the kernels: the device problem
-// table, kernel parameters and launch entry points.
+// Shared between the host code and the kernels: the device problem table,
+// kernel parameters and launch entry points.
 #pragma once
 
 #include <cstddef>
@@ -9,50 +9,70 @@
 
 namespace nvfp4 {
 
-constexpr int kTileM = 128;  // rows of one MMA (cta_group::1, M = 128)
-constexpr int kTileK = 256;  // k per pipeline stage: one 128-byte swizzle row of E2M1
-constexpr int kMmaK = 64;    // k per tcgen05.mma of kind::mxf4nvf4
-constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k
+constexpr int kTileM = 128;        // rows of one MMA (cta_group::1, M = 128)
+constexpr int kTileK = 256;        // k per pipeline stage: one 128-byte swizzle row of E2M1
+constexpr int kMmaK = 64;          // k per tcgen05.mma of kind::mxf4nvf4
+constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k in the atom layout
+constexpr int kChunkN = 32;        // scheduling grain along N (columns)
+constexpr int kMaxTileN = 192;     // widest output tile any kernel variant supports
+constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
 
 // Wait sites recorded in the error word (bits 8-15).
 enum WaitSite : uint32_t {
-    kSiteEmpty = 1,      // producer waiting for a free stage
-    kSiteFull = 2,       // MMA (or scale permuter) waiting for loaded data
-    kSiteSfReady = 3,    // MMA waiting for permuted scales
-    kSiteAccEmpty = 4,   // MMA waiting for the epilogue to free TMEM
-    kSiteAccFull = 5,    // epilogue waiting for the accumulator
-    kSiteMmaDrain = 6,   // MMA thread waiting for its own tcgen05 work at exit
-    kSiteLoadDrain = 7,  // producer waiting for its own loads at exit
+    kSiteBEmpty = 1,     // B producer waiting for a free stage
+    kSiteBFull = 2,      // MMA waiting for a B stage
+    kSiteAEmpty = 3,     // A producer waiting for a free stage
+    kSiteAFull = 4,      // MMA waiting for an A stage
+    kSiteSfFree = 5,     // scale writers waiting for a scale buffer in TMEM
+    kSiteSfReady = 6,    // MMA waiting for the scales of a stage
+    kSiteAccEmpty = 7,   // MMA waiting for the epilogue to free the accumulator
+    kSiteAccFull = 8,    // epilogue waiting for the accumulator
+    kSiteMmaDrain = 9,   // MMA thread waiting for its own tcgen05 work at exit
+    kSiteLoadDrain = 10, // a producer waiting for its own loads at exit
+    kSiteSEmpty = 11,    // scale producer waiting for a free scale stage
+    kSiteSFull = 12,     // scale writers waiting for a scale stage
 };
 
-// One entry of the device-resident problem table. Tensor maps must be
-// 64-byte aligned (CUtensorMap itself is declared 128-byte aligned); every map describes one group's buffer exactly, so the
-// TMA zero-fills rows past M_g / N on loads and drops them on stores.
+// One entry of the device-resident problem table. Every tensor map
+// describes one group's buffer exactly, so the TMA zero-fills rows past
+// M_g / N. Two B maps: boxes as wide as the kernel's widest tile for
+// full-width tiles, 32-row boxes for the rest.
 struct alignas(128) GroupDesc {
-    CUtensorMap tmA;    // A_g as bytes [M_g][K/2]; box 128 B x 128 rows; 128-byte swizzle
-    CUtensorMap tmB;    // B_g as bytes [N][K/2];   box 128 B x BN rows;  128-byte swizzle
-    CUtensorMap tmC;    // C_g fp16 [M_g][N];       box 64 x 32;          128-byte swizzle
-    CUtensorMap tmSFA;  // raw SFA_g bytes [M_g][K/16]; box 16 B x 128 rows (fused path)
-    CUtensorMap tmSFB;  // raw SFB_g bytes [N][K/16];   box 16 B x BN rows  (fused path)
+    CUtensorMap tmA;       // A_g bytes [M_g][K/2];   box 128 B x 128 rows; 128-byte swizzle
+    CUtensorMap tmB32;     // B_g bytes [N][K/2];     box 128 B x 32 rows;  128-byte swizzle
+    CUtensorMap tmBw;      // B_g bytes [N][K/2];     box 128 B x wide rows; 128-byte swizzle
+    CUtensorMap tmSFA;     // raw SFA_g [M_g][K/16];  box 16 B x 128 rows   (raw-scale path)
+    CUtensorMap tmSFB32;   // raw SFB_g [N][K/16];    box 16 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFBw;    // raw SFB_g [N][K/16];    box 16 B x wide rows  (raw-scale path)
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
     const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
+    uint16_t *C;               // C_g fp16 [M_g][N]
     int32_t M;
-    int32_t m_tiles;   // ceil(M / 128)
-    int32_t m_groups;  // ceil(m_tiles / tiles per unit)
-    int32_t unit_begin;
-    int32_t pad[8];
+    int32_t m_tiles;      // ceil(M / 128)
+    int32_t m_pairs;      // ceil(m_tiles / 2): passes over B
+    int32_t chunk_begin;  // first scheduling chunk of this group (prefix sum)
+    int32_t b_keep;       // 1: B is read by more than one pair of row tiles (keep it in L2)
+    int32_t pad[3];
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
+// Work decomposition: group g owns m_pairs_g * ceil(N/32) chunks (32 columns
+// of one pair of 128-row tiles), numbered after the chunks of groups 0..g-1
+// (chunk_prefix), pair by pair. CTA c takes the chunk range
+// [c*W/grid, (c+1)*W/grid) and walks it as tiles of up to max_tile_chunks
+// chunks inside one pair.
 struct GemmParams {
-    const GroupDesc *groups;      // [G]
-    const int32_t *unit_prefix;   // [G+1]: first work unit of each group
-    uint32_t *err;                // device error word
+    const GroupDesc *groups;       // [G]
+    const int32_t *chunk_prefix;   // [G+1]
+    uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
-    int32_t k_tiles;              // K / 256
-    int32_t total_units;
-    int32_t debug_skip_load;      // test-only fault injection (0 = off)
+    int32_t k_tiles;               // K / 256
+    int32_t n_chunks;              // ceil(N / 32)
+    int32_t total_chunks;
+    int32_t max_tile_chunks;       // 1..6
+    int32_t wide_rows;             // rows of the wide B boxes (the kernel's widest tile)
+    int32_t debug_skip_load;       // test-only fault injection (0 = off)
 };
 
 // One matrix for the scale re-layout kernel.
@@ -71,16 +91,17 @@ struct RelayoutParams {
     int32_t total_items;
 };
 
-// GEMM kernel variants (tile width, row tiles per unit, stages, scale path).
+// GEMM kernel variants: widest tile, B ring depth, A ring depth, scale path.
 struct GemmVariant {
-    int tile_n;
-    int m_tiles;
-    int stages;
+    int max_n;
+    int b_stages;
+    int a_stages;
     bool sf_raw;
 };
 
-// Returns the variant index for (tile_n, sf_raw), or -1.
-int ggemm_variant_index(int tile_n, bool sf_raw);
+// Returns the variant index, or -1. b_stages / a_stages 0 pick the default
+// depths for (max_n, sf_raw).
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw);
 GemmVariant ggemm_variant(int index);
 int ggemm_smem_bytes(int index);
 int ggemm_threads();
@@ -88,5 +109,17 @@ cudaError_t ggemm_configure(int index);  // raises the dynamic shared-memory lim
 cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream);
 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream);
+
+// Host helpers shared by the plan path and the allocation-free entry point.
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                       const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                       CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();  // nullptr when the driver has none
+
+// Fills one table entry (tensor maps, pointers, counts) for group g with
+// M_g > 0. sf_raw: encode the raw-scale maps; else store the atom pointers.
+bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
+                     const void *SFB, void *C, bool sf_raw, int wide_rows);
 
 }  // namespace nvfp4

@@ -1,22 +1,33 @@
 // Device code: the persistent warp-specialised NVFP4 grouped GEMM and the
 // scale re-layout kernel, for sm_103a.
 //
-// GEMM structure (one CTA per SM, persistent):
-//   warp 0      TMA producer: per 256-k stage loads MT A tiles (128 x 128 B),
-//               one B tile (BN x 128 B, 128-byte swizzle) and their scales
-//               into a ring of NS shared-memory stages on mbarriers.
-//   warp 1      allocates TMEM; one lane copies scales to TMEM
-//               (tcgen05.cp) and issues kind::mxf4nvf4 block16 MMAs into
-//               the accumulator, committing each stage back to the producer.
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, RN to fp16,
-//               swizzled staging in shared memory, TMA stores clipped to
-//               M_g x N.
-//   warp 6      (raw-scale path only) permutes raw 128-row x 16-byte scale
-//               tiles into the 512-byte atoms the scale copy expects.
-// A work unit is (group, MT consecutive 128-row tiles, one BN-column strip):
-// the MT row tiles share every B stage, so a B strip is streamed from HBM
-// once for up to 2*128 rows of A. Units of all groups are numbered through
-// the per-group prefix sums and dealt to CTAs round-robin.
+// GEMM structure (one CTA per SM, persistent, 12 warps):
+//   warp 0      B producer: per 256-k stage, TMA loads of the tile's B rows
+//               (128-byte swizzle) into a ring of NB stages. B is the operand
+//               streamed from HBM; its stages hold nothing else, so a stage
+//               is refilled as soon as its MMAs have read it.
+//   warp 6      A producer: the unit's one or two 128-row A tiles into a ring
+//               of NA stages (A is small and re-read from L2).
+//   warp 7      scale producer: the stage's A and B scales into a ring of NS
+//               small stages, running ahead of the operands.
+//   warps 8-11  scale writers: each turns a scale stage into the TMEM layout
+//               the block-scaled MMA reads (32 lanes x 4 columns per 128
+//               rows, the same in every lane quarter) and writes its quarter
+//               with tcgen05.st into one of NT TMEM scale buffers. Raw
+//               row-major and atom-layout scales are both handled here, off
+//               the tensor pipe and ahead of the MMAs.
+//   warp 1      allocates TMEM; one lane issues kind::mxf4nvf4 block16 MMAs
+//               (M = 128 per row tile, N = tile width up to MAXN) into fp32
+//               accumulators and releases the A stage, the B stage and the
+//               scale buffer with tcgen05.commit.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulators (one lane quarter
+//               each), RN to fp16, 16-byte stores of each row straight to C.
+// Work: group g owns m_pairs_g x ceil(N/32) chunks (32 columns of one pair
+// of 128-row tiles); the chunks of all groups are numbered through prefix
+// sums and split into equal contiguous ranges, one per CTA, so every SM
+// streams the same amount of B. A CTA walks its range as tiles of up to MAXN
+// columns. Both row tiles of a pair share every B stage, so each B strip is
+// read from HBM once, by one SM (groups of up to 256 rows).
 //
 // Every mbarrier wait is bounded by the plan's timeout: on expiry the waiter
 // records (status, site, block) in the error word, raises a CTA-wide abort
@@ -32,72 +43,95 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kWarpProducer = 0;
+constexpr int kWarpBProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpEpi0 = 2;
 constexpr int kNumEpiWarps = 4;
-constexpr int kWarpPermute = 6;
-constexpr int kThreads = 7 * 32;
+constexpr int kWarpAProducer = 6;
+constexpr int kWarpSProducer = 7;
+constexpr int kWarpSf0 = 8;
+constexpr int kNumSfWarps = 4;
+constexpr int kThreads = 12 * 32;
 
-constexpr int kATileBytes = kTileM * (kTileK / 2);  // 16384
-constexpr int kSfTileBytes = 4 * kSfAtomBytes;       // 2048: 128 rows x 256 k of scales
-constexpr int kStagingBytes = 32 * 128;              // 32 rows x 64 fp16
+constexpr int kATileBytes = kTileM * (kTileK / 2);  // 16384: 128 rows x 128 B
+constexpr int kSfTileBytes = 4 * kSfAtomBytes;       // 2048: scales of 128 rows x 256 k
+constexpr int kBRowBoxBytes = 32 * (kTileK / 2);     // 4096: one 32-row B box
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStatusTimeout = 6;  // NVFP4_ERR_TIMEOUT
+constexpr int kSfCols = 32 + 32;        // TMEM scale columns per stage: SFA 2 tiles x 4 x 4, SFB 4 x 8
 
-template <int BN, int MT, int NS, bool RAW>
+constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
+
+template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Cfg {
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "one scale atom column group covers at most 128 rows");
-    static_assert(MT >= 1 && MT <= 2, "at most two row tiles per unit");
-    static constexpr int kBBytes = BN * (kTileK / 2);
-    static constexpr int kOffA = 0;
-    static constexpr int kOffB = MT * kATileBytes;
-    static constexpr int kOffSfa = kOffB + kBBytes;
-    static constexpr int kOffSfb = kOffSfa + MT * kSfTileBytes;
-    static constexpr int kStageBytes = kOffSfb + kSfTileBytes;
-    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-    static constexpr int kOffStaging = NS * kStageBytes;
-    static constexpr int kOffBars = kOffStaging + kNumEpiWarps * 2 * kStagingBytes;
-    static constexpr int kNumBars = 3 * NS + 2 + 2 + 1;
-    static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
-    static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
-    static constexpr int kAccCols = MT * BN;                  // fp32 accumulator columns per buffer
-    static constexpr int kSfCols = (MT + 1) * 16;             // scale columns per buffer
+    static_assert(MAXN % 32 == 0 && MAXN >= 32 && MAXN <= kMaxTileN, "tile width");
+    static constexpr int kBStage = MAXN * (kTileK / 2);
+    static constexpr int kAStage = kRowTilesPerUnit * kATileBytes;
+    // scale stage: SFA (2 KB per row tile) then SFB: raw MAXN rows x 16 B, or
+    // up to three 128-row atom groups covering the tile
+    static constexpr int kSfaBytes = kRowTilesPerUnit * kSfTileBytes;
+    static constexpr int kSfbRegion = RAW ? MAXN * 16 : 3 * kSfTileBytes;
+    static constexpr int kSStage = align1k(kSfaBytes + kSfbRegion);
+    static constexpr int kOffARing = 0;
+    static constexpr int kOffBRing = NA * kAStage;
+    static constexpr int kOffSRing = kOffBRing + NB * kBStage;
+    static constexpr int kAccCols = kRowTilesPerUnit * MAXN;  // one accumulator: both row tiles
     static constexpr int kNumAcc = (2 * kAccCols + 2 * kSfCols <= (int)kTmemCols) ? 2 : 1;
     static constexpr int kSfBase = kNumAcc * kAccCols;
-    static_assert(kSfBase + 2 * kSfCols <= (int)kTmemCols, "TMEM budget");
-    static constexpr uint32_t kIdesc = idesc_mxf4nvf4_m128(BN);
-    static constexpr uint32_t kSfbBytes = RAW ? BN * 16 : kSfTileBytes;
+    static constexpr int kNT0 = ((int)kTmemCols - kSfBase) / kSfCols;
+    static constexpr int kNT = kNT0 > 6 ? 6 : kNT0;  // TMEM scale buffers
+    static constexpr int kOffBars = kOffSRing + NS * kSStage;
+    static constexpr int kNumBars = 2 * NB + 2 * NA + 2 * NS + 2 * kNT + 2 + 2 + 1;
+    static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
+    static_assert(kNT >= 2, "at least two TMEM scale buffers");
+    static_assert(kSfBase + kNT * kSfCols <= (int)kTmemCols, "TMEM budget");
+    static_assert(kBStage % 1024 == 0 && kAStage % 1024 == 0, "stages keep 1024-byte swizzle alignment");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Unit {
     int g;
-    int mtile0;  // first 128-row tile of the unit
-    int mtu;     // row tiles in this unit (1..MT)
-    int n0;      // first column
+    int mt0;    // first 128-row tile of the unit
+    int mtu;    // row tiles in the unit (1 or 2)
+    int n0;     // first column
+    int ncols;  // tile width: a multiple of 32
 };
 
-template <int BN, int MT>
-__device__ __forceinline__ Unit decode_unit(const GemmParams &p, int u)
-{
-    int lo = 0, hi = p.G;  // prefix[lo] <= u < prefix[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.unit_prefix + mid) <= u) lo = mid;
-        else hi = mid;
+// Walks this CTA's contiguous range of chunks as tiles.
+struct Walker {
+    int pos, end;
+
+    __device__ __forceinline__ explicit Walker(const GemmParams &p)
+    {
+        const long long W = p.total_chunks;
+        pos = (int)((long long)blockIdx.x * W / gridDim.x);
+        end = (int)((long long)(blockIdx.x + 1) * W / gridDim.x);
     }
-    const GroupDesc *gd = p.groups + lo;
-    const int l = u - __ldg(p.unit_prefix + lo);
-    const int mg = gd->m_groups;
-    Unit t;
-    t.g = lo;
-    t.mtile0 = (l % mg) * MT;
-    t.n0 = (l / mg) * BN;
-    t.mtu = min(MT, gd->m_tiles - t.mtile0);
-    return t;
-}
+
+    __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
+    {
+        if (pos >= end) return false;
+        int lo = 0, hi = p.G;  // prefix[lo] <= pos < prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.chunk_prefix + mid) <= pos) lo = mid;
+            else hi = mid;
+        }
+        const int local = pos - __ldg(p.chunk_prefix + lo);
+        const int mp = local / p.n_chunks;
+        const int ch = local - mp * p.n_chunks;
+        const int w = min(min(p.max_tile_chunks, p.n_chunks - ch), end - pos);
+        t.g = lo;
+        t.mt0 = mp * kRowTilesPerUnit;
+        t.mtu = min(kRowTilesPerUnit, p.groups[lo].m_tiles - t.mt0);
+        t.n0 = ch * kChunkN;
+        t.ncols = w * kChunkN;
+        pos += w;
+        return true;
+    }
+};
 
 __device__ __forceinline__ void record_error(uint32_t *err, uint32_t status, uint32_t site)
 {
@@ -152,38 +186,37 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int c>
-__device__ __forceinline__ uint32_t word_of(const uint4 &v)
+__device__ __forceinline__ uint32_t word_at(const uint4 &v, int c)
 {
     return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
 
-// In-place permutation of one raw scale tile ([rows][16 B], row r at 16r)
-// into four 512-byte atoms: atom c holds the 4 scales of k in [64c, 64c+64)
-// of row r at byte (r%32)*16 + (r/32)*4. Lane i owns rows i, i+32, i+64, i+96.
-__device__ __forceinline__ void permute_sf_tile(uint8_t *tile, int rows, int lane)
-{
-    uint4 w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int r = lane + 32 * j;
-        w[j] = (r < rows) ? *reinterpret_cast<const uint4 *>(tile + 16 * r) : make_uint4(0u, 0u, 0u, 0u);
+// A ring of mbarrier-guarded stages: position (stage, phase) advanced in step.
+struct RingPos {
+    int stage = 0;
+    uint32_t phase = 0;
+    template <int N>
+    __device__ __forceinline__ void advance()
+    {
+        if (++stage == N) {
+            stage = 0;
+            phase ^= 1u;
+        }
     }
-    __syncwarp();
-    *reinterpret_cast<uint4 *>(tile + 0 * 512 + 16 * lane) =
-        make_uint4(word_of<0>(w[0]), word_of<0>(w[1]), word_of<0>(w[2]), word_of<0>(w[3]));
-    *reinterpret_cast<uint4 *>(tile + 1 * 512 + 16 * lane) =
-        make_uint4(word_of<1>(w[0]), word_of<1>(w[1]), word_of<1>(w[2]), word_of<1>(w[3]));
-    *reinterpret_cast<uint4 *>(tile + 2 * 512 + 16 * lane) =
-        make_uint4(word_of<2>(w[0]), word_of<2>(w[1]), word_of<2>(w[2]), word_of<2>(w[3]));
-    *reinterpret_cast<uint4 *>(tile + 3 * 512 + 16 * lane) =
-        make_uint4(word_of<3>(w[0]), word_of<3>(w[1]), word_of<3>(w[2]), word_of<3>(w[3]));
-    __syncwarp();
+};
+
+// First and count of the 128-row scale blocks that cover columns [n0, n0+ncols) of N.
+__device__ __forceinline__ void sfb_blocks(int n0, int ncols, int N, int &b0, int &nblk)
+{
+    b0 = n0 / 128;
+    const int last = min(n0 + ncols, N) - 1;
+    nblk = last / 128 - b0 + 1;
 }
 
-template <int BN, int MT, int NS, bool RAW>
+template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Roles {
-    using C = Cfg<BN, MT, NS, RAW>;
+    using C = Cfg<MAXN, NB, NA, NS, RAW>;
+    static constexpr int NT = C::kNT;
 
     uint8_t *smem;
     uint32_t sbase;
@@ -195,283 +228,416 @@ struct Roles {
     {
     }
 
-    __device__ __forceinline__ uint32_t bar_full(int s) const { return sbase + C::kOffBars + 8 * s; }
-    __device__ __forceinline__ uint32_t bar_empty(int s) const { return sbase + C::kOffBars + 8 * (NS + s); }
-    __device__ __forceinline__ uint32_t bar_sf(int s) const { return sbase + C::kOffBars + 8 * (2 * NS + s); }
-    __device__ __forceinline__ uint32_t bar_acc_full(int a) const { return sbase + C::kOffBars + 8 * (3 * NS + a); }
-    __device__ __forceinline__ uint32_t bar_acc_empty(int a) const
+    __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBars + 8 * i; }
+    __device__ __forceinline__ uint32_t b_full(int s) const { return bar(s); }
+    __device__ __forceinline__ uint32_t b_empty(int s) const { return bar(NB + s); }
+    __device__ __forceinline__ uint32_t a_full(int s) const { return bar(2 * NB + s); }
+    __device__ __forceinline__ uint32_t a_empty(int s) const { return bar(2 * NB + NA + s); }
+    __device__ __forceinline__ uint32_t s_full(int s) const { return bar(2 * NB + 2 * NA + s); }
+    __device__ __forceinline__ uint32_t s_empty(int s) const { return bar(2 * NB + 2 * NA + NS + s); }
+    __device__ __forceinline__ uint32_t sf_ready(int b) const { return bar(2 * NB + 2 * NA + 2 * NS + b); }
+    __device__ __forceinline__ uint32_t sf_free(int b) const { return bar(2 * NB + 2 * NA + 2 * NS + NT + b); }
+    __device__ __forceinline__ uint32_t acc_full(int a) const { return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + a); }
+    __device__ __forceinline__ uint32_t acc_empty(int a) const
     {
-        return sbase + C::kOffBars + 8 * (3 * NS + 2 + a);
+        return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + 2 + a);
     }
-    __device__ __forceinline__ uint32_t bar_drain() const { return sbase + C::kOffBars + 8 * (3 * NS + 4); }
-    __device__ __forceinline__ uint32_t stage_addr(int s) const { return sbase + s * C::kStageBytes; }
+    __device__ __forceinline__ uint32_t drain() const { return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + 4); }
+    __device__ __forceinline__ uint32_t b_stage(int s) const { return sbase + C::kOffBRing + s * C::kBStage; }
+    __device__ __forceinline__ uint32_t a_stage(int s) const { return sbase + C::kOffARing + s * C::kAStage; }
+    __device__ __forceinline__ uint32_t s_stage(int s) const { return sbase + C::kOffSRing + s * C::kSStage; }
 
     __device__ void init_barriers()
     {
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(b_full(s), 1);
+            mbar_init(b_empty(s), 1);
+        }
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(a_full(s), 1);
+            mbar_init(a_empty(s), 1);
+        }
         for (int s = 0; s < NS; ++s) {
-            mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), 1);
-            mbar_init(bar_sf(s), 1);
+            mbar_init(s_full(s), 1);
+            mbar_init(s_empty(s), kNumSfWarps);
+        }
+        for (int b = 0; b < NT; ++b) {
+            mbar_init(sf_ready(b), kNumSfWarps);
+            mbar_init(sf_free(b), 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(bar_acc_full(a), 1);
-            mbar_init(bar_acc_empty(a), kNumEpiWarps);
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), kNumEpiWarps);
         }
-        mbar_init(bar_drain(), 1);
+        mbar_init(drain(), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
 
-    // ---------------------------------------------------------------- producer
-    __device__ void producer()
+    // ------------------------------------------------------------- B producer
+    __device__ void b_producer()
     {
-        const uint64_t pol_a = policy_evict_last();   // A tiles are re-read by every column strip
-        const uint64_t pol_b = policy_evict_first();  // B streams through once
-        int stage = 0;
-        uint32_t phase = 0;
+        const uint64_t pol_stream = policy_evict_first();  // read by one row tile only
+        const uint64_t pol_keep = policy_evict_normal();    // read again by the group's other row tiles
+        RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1;
-        int loads = 0;
+        int last_g = -1, loads = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-            const Unit t = decode_unit<BN, MT>(p, u);
+        Walker wk(p);
+        Unit t;
+        while (ok && wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
             if (t.g != last_g) {
-                fence_tensormap_acquire(&gd->tmA);
-                fence_tensormap_acquire(&gd->tmB);
-                if (RAW) {
-                    fence_tensormap_acquire(&gd->tmSFA);
-                    fence_tensormap_acquire(&gd->tmSFB);
-                }
+                fence_tensormap_acquire(&gd->tmB32);
+                fence_tensormap_acquire(&gd->tmBw);
                 last_g = t.g;
             }
-            const uint32_t bytes = (uint32_t)t.mtu * (kATileBytes + kSfTileBytes) + C::kBBytes + C::kSfbBytes;
-            const size_t katoms = (size_t)(p.K / 64);
+            const uint64_t pol = gd->b_keep ? pol_keep : pol_stream;
+            const bool wide = (t.ncols == p.wide_rows);
+            const int boxes = t.ncols / 32;
+            const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_phase(bar_empty(stage), phase ^ 1u, abort_flag, p, kSiteEmpty)) {
+                if (!wait_phase(b_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteBEmpty)) {
                     ok = false;
                     break;
                 }
                 ++loads;
                 const bool skip = (p.debug_skip_load > 0 && blockIdx.x == 0 && loads == p.debug_skip_load);
                 if (!skip) {
-                    const uint32_t bar = bar_full(stage);
-                    const uint32_t st = stage_addr(stage);
-                    mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-                        if (mt < t.mtu)
-                            tma_load_2d(st + C::kOffA + mt * kATileBytes, &gd->tmA, kt * (kTileK / 2),
-                                        (t.mtile0 + mt) * kTileM, bar, pol_a);
-                    tma_load_2d(st + C::kOffB, &gd->tmB, kt * (kTileK / 2), t.n0, bar, pol_b);
-                    if (RAW) {
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-                            if (mt < t.mtu)
-                                tma_load_2d(st + C::kOffSfa + mt * kSfTileBytes, &gd->tmSFA, kt * (kTileK / 16),
-                                            (t.mtile0 + mt) * kTileM, bar, pol_a);
-                        tma_load_2d(st + C::kOffSfb, &gd->tmSFB, kt * (kTileK / 16), t.n0, bar, pol_b);
+                    const uint32_t fb = b_full(r.stage);
+                    const uint32_t st = b_stage(r.stage);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    if (wide) {
+                        tma_load_2d(st, &gd->tmBw, kt * (kTileK / 2), t.n0, fb, pol);
                     } else {
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-                            if (mt < t.mtu)
-                                bulk_load(st + C::kOffSfa + mt * kSfTileBytes,
-                                          gd->sfa_atoms + ((size_t)(t.mtile0 + mt) * katoms + (size_t)kt * 4) *
-                                                              kSfAtomBytes,
-                                          kSfTileBytes, bar, pol_a);
-                        bulk_load(st + C::kOffSfb,
-                                  gd->sfb_atoms + ((size_t)(t.n0 / 128) * katoms + (size_t)kt * 4) * kSfAtomBytes,
-                                  kSfTileBytes, bar, pol_b);
+                        for (int i = 0; i < boxes; ++i)
+                            tma_load_2d(st + i * kBRowBoxBytes, &gd->tmB32, kt * (kTileK / 2), t.n0 + 32 * i, fb,
+                                        pol);
                     }
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    issued_mask |= 1u << r.stage;
+                    issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
                 } else {
-                    issued_mask &= ~(1u << stage);  // nothing in flight for this stage
+                    issued_mask &= ~(1u << r.stage);  // nothing in flight for this stage
                 }
-                if (++stage == NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                r.advance<NB>();
             }
         }
-        // Every load issued here must have landed before the CTA may exit.
+        for (int s = 0; s < NB; ++s)
+            if ((issued_mask >> s) & 1u) wait_drain(b_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+    }
+
+    // ------------------------------------------------------------- A producer
+    __device__ void a_producer()
+    {
+        const uint64_t pol = policy_evict_last();  // A tiles are re-read by every column tile
+        RingPos r;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        int last_g = -1;
+        bool ok = true;
+        Walker wk(p);
+        Unit t;
+        while (ok && wk.next(p, t)) {
+            const GroupDesc *gd = p.groups + t.g;
+            if (t.g != last_g) {
+                fence_tensormap_acquire(&gd->tmA);
+                last_g = t.g;
+            }
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!wait_phase(a_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteAEmpty)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = a_full(r.stage);
+                mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
+#pragma unroll
+                for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+                    if (mt < t.mtu)
+                        tma_load_2d(a_stage(r.stage) + mt * kATileBytes, &gd->tmA, kt * (kTileK / 2),
+                                    (t.mt0 + mt) * kTileM, fb, pol);
+                issued_mask |= 1u << r.stage;
+                issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
+                r.advance<NA>();
+            }
+        }
+        for (int s = 0; s < NA; ++s)
+            if ((issued_mask >> s) & 1u) wait_drain(a_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+    }
+
+    // --------------------------------------------------------- scale producer
+    __device__ void s_producer()
+    {
+        const uint64_t pol = policy_evict_normal();
+        RingPos r;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        int last_g = -1;
+        bool ok = true;
+        const size_t katoms = (size_t)(p.K / 64);
+        Walker wk(p);
+        Unit t;
+        while (ok && wk.next(p, t)) {
+            const GroupDesc *gd = p.groups + t.g;
+            if (RAW && t.g != last_g) {
+                fence_tensormap_acquire(&gd->tmSFA);
+                fence_tensormap_acquire(&gd->tmSFB32);
+                fence_tensormap_acquire(&gd->tmSFBw);
+                last_g = t.g;
+            }
+            const bool wide = (t.ncols == p.wide_rows);
+            const int boxes = t.ncols / 32;
+            int b0 = 0, nblk = 0;
+            sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
+            const uint32_t bytes = (uint32_t)t.mtu * kSfTileBytes +
+                                   (RAW ? (uint32_t)t.ncols * 16u : (uint32_t)nblk * kSfTileBytes);
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = s_full(r.stage);
+                const uint32_t st = s_stage(r.stage);
+                mbar_arrive_expect_tx(fb, bytes);
+                if (RAW) {
+#pragma unroll
+                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+                        if (mt < t.mtu)
+                            tma_load_2d(st + mt * kSfTileBytes, &gd->tmSFA, kt * (kTileK / 16), (t.mt0 + mt) * kTileM,
+                                        fb, pol);
+                    if (wide) {
+                        tma_load_2d(st + C::kSfaBytes, &gd->tmSFBw, kt * (kTileK / 16), t.n0, fb, pol);
+                    } else {
+                        for (int i = 0; i < boxes; ++i)
+                            tma_load_2d(st + C::kSfaBytes + i * 512, &gd->tmSFB32, kt * (kTileK / 16),
+                                        t.n0 + 32 * i, fb, pol);
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+                        if (mt < t.mtu)
+                            bulk_load(st + mt * kSfTileBytes,
+                                      gd->sfa_atoms + ((size_t)(t.mt0 + mt) * katoms + (size_t)kt * 4) * kSfAtomBytes,
+                                      kSfTileBytes, fb, pol);
+                    for (int b = 0; b < nblk; ++b)
+                        bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
+                                  gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)kt * 4) * kSfAtomBytes,
+                                  kSfTileBytes, fb, pol);
+                }
+                issued_mask |= 1u << r.stage;
+                issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
+                r.advance<NS>();
+            }
+        }
         for (int s = 0; s < NS; ++s)
-            if ((issued_mask >> s) & 1u) wait_drain(bar_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+            if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+    }
+
+    // ------------------------------------------------------------ scale writers
+    // TMEM scale layout for one stage (scale buffer b at column S = base + 64b):
+    //   SFA, row tile mt, 64-k slice kk: columns S + 16mt + 4kk + c (c = 0..3),
+    //   lane i holds the four 16-k scales of the tile's row 32c + i;
+    //   SFB, 64-k slice kk: columns S + 32 + 8kk + c (c = 0..7), lane i holds
+    //   those of tile column 32c + i.
+    // Every lane quarter holds the same values; warp q writes quarter q.
+    __device__ void sf_writer(uint32_t tmem, int warp, int lane)
+    {
+        const int q = warp & 3;
+        RingPos rs, rt;
+        bool ok = true;
+        Walker wk(p);
+        Unit t;
+        while (ok && wk.next(p, t)) {
+            int b0 = 0, nblk = 0;
+            sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
+            const int s0 = (t.n0 % 128) / 32;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!warp_wait_phase(sf_free(rt.stage), rt.phase ^ 1u, abort_flag, p, kSiteSfFree) ||
+                    !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *sa = smem + C::kOffSRing + rs.stage * C::kSStage;
+                const uint8_t *sb = sa + C::kSfaBytes;
+                uint32_t va[32], vb[32];
+                if (RAW) {
+                    // raw tiles: row r's 16 bytes at 16r, word kk = the 64-k slice kk
+#pragma unroll
+                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 w = (mt < t.mtu) ? *reinterpret_cast<const uint4 *>(
+                                                               sa + mt * kSfTileBytes + 16 * (32 * c + lane))
+                                                         : make_uint4(0u, 0u, 0u, 0u);
+                            va[16 * mt + 0 + c] = w.x;
+                            va[16 * mt + 4 + c] = w.y;
+                            va[16 * mt + 8 + c] = w.z;
+                            va[16 * mt + 12 + c] = w.w;
+                        }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        // rows past the widest tile lie outside this stage's scale region
+                        const uint4 w = (32 * c < MAXN) ? *reinterpret_cast<const uint4 *>(sb + 16 * (32 * c + lane))
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+                        vb[0 + c] = w.x;
+                        vb[8 + c] = w.y;
+                        vb[16 + c] = w.z;
+                        vb[24 + c] = w.w;
+                    }
+                } else {
+                    // atom groups: atom kk row i holds rows i, i+32, i+64, i+96 (words 0..3)
+#pragma unroll
+                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint4 w = (mt < t.mtu) ? *reinterpret_cast<const uint4 *>(
+                                                               sa + mt * kSfTileBytes + kk * kSfAtomBytes + 16 * lane)
+                                                         : make_uint4(0u, 0u, 0u, 0u);
+                            va[16 * mt + 4 * kk + 0] = w.x;
+                            va[16 * mt + 4 * kk + 1] = w.y;
+                            va[16 * mt + 4 * kk + 2] = w.z;
+                            va[16 * mt + 4 * kk + 3] = w.w;
+                        }
+                    // tile column 32c + i is row n0 + 32c + i: block (s0 + c) / 4, word (s0 + c) % 4
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint4 src[3];
+#pragma unroll
+                        for (int b = 0; b < 3; ++b)
+                            src[b] = (b < nblk) ? *reinterpret_cast<const uint4 *>(sb + b * kSfTileBytes +
+                                                                                     kk * kSfAtomBytes + 16 * lane)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int idx = s0 + c;
+                            const int blk = idx >> 2;
+                            const uint4 v = blk == 0 ? src[0] : (blk == 1 ? src[1] : src[2]);
+                            vb[8 * kk + c] = word_at(v, idx & 3);
+                        }
+                    }
+                }
+                const uint32_t col = (uint32_t)(C::kSfBase + rt.stage * kSfCols);
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + col;
+                tmem_st_32x32b_x32(taddr, va);
+                tmem_st_32x32b_x32(taddr + 32, vb);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(s_empty(rs.stage));
+                    mbar_arrive(sf_ready(rt.stage));
+                }
+                rs.advance<NS>();
+                rt.advance<NT>();
+            }
+        }
+        tmem_st_wait();
     }
 
     // ------------------------------------------------------------- MMA issuer
     __device__ void mma_issuer(uint32_t tmem)
     {
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        uint32_t sf_buf = 0;
+        RingPos ra, rb, rt, racc;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-            const Unit t = decode_unit<BN, MT>(p, u);
-            if (!wait_phase(bar_acc_empty(acc), acc_phase ^ 1u, abort_flag, p, kSiteAccEmpty)) break;
+        Walker wk(p);
+        Unit t;
+        while (ok && wk.next(p, t)) {
+            if (!wait_phase(acc_empty(racc.stage), racc.phase ^ 1u, abort_flag, p, kSiteAccEmpty)) break;
             tc_fence_after_sync();
-            const uint32_t d0 = tmem + (uint32_t)(acc * C::kAccCols);
-            // atom layout: a 64-row strip inside a 128-row atom uses its upper columns
-            const uint32_t sfb_sub = RAW ? 0u : (uint32_t)((t.n0 % 128) / 32);
+            const uint32_t d = tmem + (uint32_t)(racc.stage * C::kAccCols);
+            const uint32_t idesc = idesc_mxf4nvf4_m128((uint32_t)t.ncols);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                const bool got = RAW ? wait_phase(bar_sf(stage), phase, abort_flag, p, kSiteSfReady)
-                                     : wait_phase(bar_full(stage), phase, abort_flag, p, kSiteFull);
-                if (!got) {
+                if (!wait_phase(b_full(rb.stage), rb.phase, abort_flag, p, kSiteBFull) ||
+                    !wait_phase(a_full(ra.stage), ra.phase, abort_flag, p, kSiteAFull) ||
+                    !wait_phase(sf_ready(rt.stage), rt.phase, abort_flag, p, kSiteSfReady)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t st = stage_addr(stage);
-                const uint32_t sf = tmem + (uint32_t)(C::kSfBase + sf_buf * C::kSfCols);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    if (mt < t.mtu)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_cp_sf_atom(sf + mt * 16 + kk * 4,
-                                          desc_sf_atom(st + C::kOffSfa + mt * kSfTileBytes + kk * kSfAtomBytes));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_cp_sf_atom(sf + MT * 16 + kk * 4, desc_sf_atom(st + C::kOffSfb + kk * kSfAtomBytes));
+                const uint32_t sa = a_stage(ra.stage);
+                const uint32_t sb = b_stage(rb.stage);
+                const uint32_t sf = tmem + (uint32_t)(C::kSfBase + rt.stage * kSfCols);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bdesc = desc_sw128_kmajor(st + C::kOffB + kk * 32);
+                    const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
+                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
                         if (mt < t.mtu)
-                            tc_mma_nvf4(d0 + mt * BN, desc_sw128_kmajor(st + C::kOffA + mt * kATileBytes + kk * 32),
-                                        bdesc, C::kIdesc, sf + mt * 16 + kk * 4, sf + MT * 16 + kk * 4 + sfb_sub,
+                            tc_mma_nvf4(d + (uint32_t)(mt * MAXN), desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32),
+                                        bdesc, idesc, sf + mt * 16 + kk * 4, sf + 32 + kk * 8,
                                         (kt | kk) != 0 ? 1u : 0u);
                 }
-                tc_commit(bar_empty(stage));  // frees the stage once these MMAs have read it
-                sf_buf ^= 1u;
-                if (++stage == NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                // the stages and the scale buffer are free once these MMAs have read them
+                tc_commit(b_empty(rb.stage));
+                tc_commit(a_empty(ra.stage));
+                tc_commit(sf_free(rt.stage));
+                ra.advance<NA>();
+                rb.advance<NB>();
+                rt.advance<NT>();
             }
             if (!ok) break;
-            tc_commit(bar_acc_full(acc));
-            if (++acc == C::kNumAcc) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
+            tc_commit(acc_full(racc.stage));
+            racc.advance<C::kNumAcc>();
         }
         // All tcgen05 work issued by this thread completes before TMEM is released.
-        tc_commit(bar_drain());
-        wait_drain(bar_drain(), 0, p, kSiteMmaDrain);
+        tc_commit(drain());
+        wait_drain(drain(), 0, p, kSiteMmaDrain);
     }
 
     // --------------------------------------------------------------- epilogue
     __device__ void epilogue(uint32_t tmem, int warp, int lane)
     {
         const int q = warp & 3;  // the TMEM lane quarter this warp may read
-        const int e = warp - kWarpEpi0;
-        uint8_t *stage_ptr = smem + C::kOffStaging + e * 2 * kStagingBytes;
-        const uint32_t stage_sa = sbase + C::kOffStaging + e * 2 * kStagingBytes;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        int sb = 0;
-        int last_g = -1;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Unit t = decode_unit<BN, MT>(p, u);
+        RingPos racc;
+        Walker wk(p);
+        Unit t;
+        while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
-            if (t.g != last_g) {
-                if (lane == 0) fence_tensormap_acquire(&gd->tmC);
-                last_g = t.g;
-            }
-            if (!warp_wait_phase(bar_acc_full(acc), acc_phase, abort_flag, p, kSiteAccFull)) break;
+            if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
             tc_fence_after_sync();
-            const int M = gd->M;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int row0 = (t.mtile0 + mt) * kTileM + 32 * q;
-                if (mt >= t.mtu || row0 >= M) continue;
+            for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
+                const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
+                if (mt >= t.mtu || row0 >= gd->M) continue;
+                const int row = row0 + lane;
+                const bool live = row < gd->M;
+                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)p.N;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 64; ++cc) {
-                    const int col0 = t.n0 + cc * 64;
+                for (int c = 0; c < t.ncols / 32; ++c) {
+                    const int col0 = t.n0 + c * 32;
                     if (col0 >= p.N) break;
-                    uint32_t v0[32], v1[32];
-                    const uint32_t taddr =
-                        tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * C::kAccCols + mt * BN + cc * 64);
-                    tmem_ld_32x32b_x32(taddr, v0);
-                    tmem_ld_32x32b_x32(taddr + 32, v1);
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) +
+                                           (uint32_t)(racc.stage * C::kAccCols + mt * MAXN + c * 32),
+                                       v);
                     tmem_ld_wait();
-                    // staging buffer sb is free once at most one store (the other buffer's) still reads smem
-                    if (lane == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                    uint8_t *row_ptr = stage_ptr + sb * kStagingBytes + lane * 128;
+                    if (live) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t *src = (j < 4) ? &v0[8 * j] : &v1[8 * (j - 4)];
-                        uint4 pk;
-                        pk.x = pack_half2(src[0], src[1]);
-                        pk.y = pack_half2(src[2], src[3]);
-                        pk.z = pack_half2(src[4], src[5]);
-                        pk.w = pack_half2(src[6], src[7]);
-                        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-                        *reinterpret_cast<uint4 *>(row_ptr + ((j ^ (lane & 7)) * 16)) = pk;
+                        for (int j = 0; j < 4; ++j) {
+                            if (col0 + 8 * j < p.N) {
+                                uint4 pk;
+                                pk.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
+                                pk.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
+                                pk.z = pack_half2(v[8 * j + 4], v[8 * j + 5]);
+                                pk.w = pack_half2(v[8 * j + 6], v[8 * j + 7]);
+                                *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) = pk;
+                            }
+                        }
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&gd->tmC, col0, row0, stage_sa + sb * kStagingBytes);
-                        bulk_commit_group();
-                    }
-                    sb ^= 1;
                 }
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty(acc));
-            if (++acc == C::kNumAcc) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
-        }
-        if (lane == 0) bulk_wait_group<0>();
-        __syncwarp();
-    }
-
-    // ----------------------------------------------------------- scale permuter
-    __device__ void sf_permuter(int lane)
-    {
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-            const Unit t = decode_unit<BN, MT>(p, u);
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!warp_wait_phase(bar_full(stage), phase, abort_flag, p, kSiteFull)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *st = smem + stage * C::kStageBytes;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    if (mt < t.mtu) permute_sf_tile(st + C::kOffSfa + mt * kSfTileBytes, kTileM, lane);
-                permute_sf_tile(st + C::kOffSfb, BN, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_sf(stage));
-                if (++stage == NS) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
+            if (lane == 0) mbar_arrive(acc_empty(racc.stage));
+            racc.advance<C::kNumAcc>();
         }
     }
 };
 
-template <int BN, int MT, int NS, bool RAW>
+template <int MAXN, int NB, int NA, int NS, bool RAW>
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ GemmParams p)
 {
-    using C = Cfg<BN, MT, NS, RAW>;
+    using C = Cfg<MAXN, NB, NA, NS, RAW>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Roles<BN, MT, NS, RAW> r(smem, p);
+    Roles<MAXN, NB, NA, NS, RAW> r(smem, p);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
@@ -485,14 +651,18 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
 
-    if (warp == kWarpProducer) {
-        if (lane == 0) r.producer();
+    if (warp == kWarpBProducer) {
+        if (lane == 0) r.b_producer();
+    } else if (warp == kWarpAProducer) {
+        if (lane == 0) r.a_producer();
+    } else if (warp == kWarpSProducer) {
+        if (lane == 0) r.s_producer();
     } else if (warp == kWarpMma) {
         if (lane == 0) r.mma_issuer(tmem);
-    } else if (warp < kWarpEpi0 + kNumEpiWarps) {
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
         r.epilogue(tmem, warp, lane);
-    } else if (RAW && warp == kWarpPermute) {
-        r.sf_permuter(lane);
+    } else if (warp >= kWarpSf0 && warp < kWarpSf0 + kNumSfWarps) {
+        r.sf_writer(tmem, warp, lane);
     }
     __syncwarp();
     tc_fence_before_sync();
@@ -540,14 +710,10 @@ __global__ void __launch_bounds__(256) sf_relayout_kernel(const __grid_constant_
                                   : make_uint4(0u, 0u, 0u, 0u);
         }
         uint8_t *dst = job.dst + ((size_t)rb * katoms + (size_t)pc * 4) * kSfAtomBytes + 16 * lane;
-        *reinterpret_cast<uint4 *>(dst + 0 * kSfAtomBytes) =
-            make_uint4(word_of<0>(w[0]), word_of<0>(w[1]), word_of<0>(w[2]), word_of<0>(w[3]));
-        *reinterpret_cast<uint4 *>(dst + 1 * kSfAtomBytes) =
-            make_uint4(word_of<1>(w[0]), word_of<1>(w[1]), word_of<1>(w[2]), word_of<1>(w[3]));
-        *reinterpret_cast<uint4 *>(dst + 2 * kSfAtomBytes) =
-            make_uint4(word_of<2>(w[0]), word_of<2>(w[1]), word_of<2>(w[2]), word_of<2>(w[3]));
-        *reinterpret_cast<uint4 *>(dst + 3 * kSfAtomBytes) =
-            make_uint4(word_of<3>(w[0]), word_of<3>(w[1]), word_of<3>(w[2]), word_of<3>(w[3]));
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(dst + c * kSfAtomBytes) =
+                make_uint4(word_at(w[0], c), word_at(w[1], c), word_at(w[2], c), word_at(w[3], c));
     }
 }
 
@@ -557,30 +723,36 @@ using KernelFn = void (*)(GemmParams);
 
 struct VariantEntry {
     GemmVariant v;
+    bool is_default;
     KernelFn fn;
     int smem;
 };
 
-template <int BN, int MT, int NS, bool RAW>
-constexpr VariantEntry make_entry()
+template <int MAXN, int NB, int NA, int NS, bool RAW>
+constexpr VariantEntry make_entry(bool is_default)
 {
-    return VariantEntry{GemmVariant{BN, MT, NS, RAW}, &ggemm_kernel<BN, MT, NS, RAW>, Cfg<BN, MT, NS, RAW>::kSmemBytes};
+    return VariantEntry{GemmVariant{MAXN, NB, NA, RAW}, is_default, &ggemm_kernel<MAXN, NB, NA, NS, RAW>,
+                        Cfg<MAXN, NB, NA, NS, RAW>::kSmemBytes};
 }
 
+// (MAXN, B stages, A stages, scale stages, raw scales)
 const VariantEntry kVariants[] = {
-    make_entry<128, 2, 3, false>(),
-    make_entry<128, 2, 3, true>(),
-    make_entry<64, 2, 4, false>(),
-    make_entry<64, 2, 4, true>(),
+    make_entry<192, 5, 2, 4, true>(true),  make_entry<192, 5, 2, 3, false>(true),
+    make_entry<192, 4, 3, 4, true>(false), make_entry<192, 6, 2, 2, true>(false),
+    make_entry<128, 7, 2, 4, true>(true),  make_entry<128, 6, 2, 3, false>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 }  // namespace
 
-int ggemm_variant_index(int tile_n, bool sf_raw)
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw)
 {
-    for (int i = 0; i < kNumVariants; ++i)
-        if (kVariants[i].v.tile_n == tile_n && kVariants[i].v.sf_raw == sf_raw) return i;
+    for (int i = 0; i < kNumVariants; ++i) {
+        const GemmVariant &v = kVariants[i].v;
+        if (v.max_n != max_n || v.sf_raw != sf_raw) continue;
+        if (b_stages == 0 && a_stages == 0 && kVariants[i].is_default) return i;
+        if (v.b_stages == b_stages && v.a_stages == a_stages) return i;
+    }
     return -1;
 }
 

@@ -6,7 +6,7 @@
 // per-group tensor maps the kernel reads and the device error word) lives in
 // one file-scope device array that every GPU loading the library holds
 // until the process exits. It runs the same persistent GEMM kernel as
-// nvfp4_ggemm_run on the raw-scale FUSED path with 128-column tiles.
+// nvfp4_ggemm_run on the raw-scale FUSED path with its default tiles.
 #include <cstring>
 #include <mutex>
 
@@ -19,11 +19,12 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kNoAllocMaxGroups = 64;
-constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 48 KB
+constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 56 KB
 constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
 constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
 constexpr size_t kScratchBytes = kErrOffset + 256;
 static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
+static_assert(kScratchBytes <= 64 * 1024, "the array stays within 64 KB");
 
 // The scratch: problem table, unit prefix sums, error word. In host code this
 // name is only a host-side stand-in; the device address comes from
@@ -34,23 +35,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 uint8_t *g_scratch_addr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
-PFN_cuTensorMapEncodeTiled_v12000 g_encode_fn = nullptr;
 
 int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
 bool aligned16_p(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t cols, uint64_t rows,
-                uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
-{
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode_fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // First call on a device (that device current): look up the scratch array's
 // device address, raise the kernel's shared-memory limit, fetch the
@@ -59,15 +47,7 @@ nvfp4_status_t setup_device(int dev, int variant)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_scratch_addr[dev]) return NVFP4_OK;
-    if (!g_encode_fn) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return NVFP4_ERR_CUDA;
-        g_encode_fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    if (!tensor_map_encoder()) return NVFP4_ERR_CUDA;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
     int sms = 0;
@@ -102,9 +82,8 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
             !aligned16_p(C[g]))
             return NVFP4_ERR_ALIGNMENT;
     }
-    const int variant = ggemm_variant_index(128, true);
+    const int variant = ggemm_variant_index(kMaxTileN, 0, 0, true);
     if (variant < 0) return NVFP4_ERR_CUDA;
-    const GemmVariant var = ggemm_variant(variant);
 
     // --- device and one-time set-up
     int dev = -1, major = 0, minor = 0;
@@ -130,31 +109,20 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     std::memset(table, 0, sizeof(table));
     auto *groups = reinterpret_cast<GroupDesc *>(table);
     auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
-    const int BN = var.tile_n, MT = var.m_tiles;
-    const int strips = ceil_div_i(N, BN);
+    const int n_chunks = ceil_div_i(N, kChunkN);
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         GroupDesc &d = groups[g];
         d.M = M[g];
         d.m_tiles = ceil_div_i(M[g], kTileM);
-        d.m_groups = ceil_div_i(d.m_tiles, MT);
-        d.unit_begin = (int32_t)total;
+        d.m_pairs = ceil_div_i(d.m_tiles, kRowTilesPerUnit);
+        d.chunk_begin = (int32_t)total;
         prefix[g] = (int32_t)total;
-        total += (long)d.m_groups * strips;
+        total += (long)d.m_pairs * n_chunks;
         if (M[g] == 0) continue;
-        const uint64_t Mg = (uint64_t)M[g];
-        const bool ok =
-            encode_map(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A[g], K / 2, Mg, K / 2, kTileK / 2, kTileM,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_map(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B[g], K / 2, N, K / 2, kTileK / 2, BN,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_map(&d.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C[g], N, Mg, (uint64_t)N * 2, 64, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_map(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA[g], K / 16, Mg, K / 16, kTileK / 16, kTileM,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_map(&d.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB[g], K / 16, N, K / 16, kTileK / 16, BN,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (!ok) return NVFP4_ERR_CUDA;
+        if (!fill_group_desc(d, M[g], N, K, A[g], B[g], SFA[g], SFB[g], C[g], true, kMaxTileN))
+            return NVFP4_ERR_CUDA;
+        d.chunk_begin = prefix[g];
     }
     prefix[num_groups] = (int32_t)total;
     if (total == 0) return NVFP4_OK;
@@ -173,14 +141,17 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     }
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
-    gp.unit_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
+    gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
     gp.N = N;
     gp.K = K;
     gp.k_tiles = K / kTileK;
-    gp.total_units = (int32_t)total;
+    gp.n_chunks = n_chunks;
+    gp.total_chunks = (int32_t)total;
+    gp.max_tile_chunks = kMaxTileN / kChunkN;
+    gp.wide_rows = kMaxTileN;
     gp.debug_skip_load = 0;
     const int grid = (int)(total < g_sm_count[dev] ? total : g_sm_count[dev]);
     if (ggemm_launch(variant, gp, grid, s) != cudaSuccess) {

@@ -90,12 +90,22 @@ typedef struct {
     int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
                                  nvfp4_ggemm_prepare_b_scales and run skips it */
     uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
-    int32_t tile_n;           /* output tile width: 0 = automatic, else 64 or 128 */
+    int32_t tile_n;           /* widest output tile in columns: 0 = 192, else a multiple of 32
+                                 up to 192 (kernels exist for 128 and 192; a smaller value
+                                 caps the tiles of the next wider kernel). Each tile covers
+                                 up to two 128-row tiles of one group, which share every
+                                 B stage */
     int32_t max_ctas;         /* persistent grid size: 0 = number of SMs */
-    int32_t debug_skip_load;  /* test only: 0 = off; n > 0 = the producer of CTA 0 leaves the
-                                 n-th load of its first unit unissued, so the consumer's wait
-                                 runs into the timeout (exercises the error path) */
-    int32_t reserved[5];
+    int32_t debug_skip_load;  /* test only: 0 = off; n > 0 = the B producer of CTA 0 leaves its
+                                 n-th stage load unissued, so the consumers' waits run into the
+                                 timeout (exercises the error path) */
+    int32_t b_stages;         /* shared-memory stages of the B ring; 0 (with a_stages 0) = the
+                                 default for the tile width and scale path. Kernels exist for
+                                 (tile width, b_stages, a_stages) = (192,5,2), (192,4,3),
+                                 (192,6,2) with raw scales and the defaults (192,5,2),
+                                 (128,7,2) raw and (192,5,2), (128,6,2) atom */
+    int32_t a_stages;         /* shared-memory stages of the A ring (see b_stages) */
+    int32_t reserved[3];
 } nvfp4_ggemm_options_t;
 
 typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;
@@ -174,10 +184,10 @@ NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
 
 /* Plan introspection (for tests and benchmarks). */
 typedef struct {
-    int32_t tile_n;        /* output tile width used */
-    int32_t m_tiles_per_unit; /* 128-row tiles that share one B stage */
-    int32_t stages;        /* shared-memory pipeline depth */
-    int32_t units;         /* work units (group, row-tile pair, column strip) */
+    int32_t tile_n;        /* widest output tile (columns) */
+    int32_t b_stages;      /* shared-memory stages of the B ring */
+    int32_t a_stages;      /* shared-memory stages of the A ring */
+    int32_t chunks;        /* scheduling chunks: 32 columns of one 128-row tile */
     int32_t grid;          /* persistent CTAs launched */
     int32_t sm_count;
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
@@ -197,7 +207,7 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  * not grow the process's device footprint). It computes what
  * nvfp4_ggemm_run computes for raw row-major scales, with the same kernel,
  * but needs no plan: the per-group tensor maps and the device error word it
- * needs live in a static device array of 64 KB that every GPU loading the
+ * needs live in a static device array of under 64 KB that every GPU loading the
  * library holds until the process exits.
  *
  * Arguments: as nvfp4_ggemm_plan + nvfp4_ggemm_run (M host array of G row

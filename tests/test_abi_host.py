@@ -49,6 +49,7 @@ def test_default_options(L):
     assert opt.struct_size == ctypes.sizeof(nb.nvfp4_ggemm_options_t)
     assert opt.sf_layout == nb.NVFP4_SF_RAW and opt.sf_path == nb.NVFP4_SF_FUSED
     assert opt.wait_timeout_ns == 2_000_000_000 and opt.tile_n == 0 and opt.debug_skip_load == 0
+    assert (opt.b_stages, opt.a_stages) == (0, 0)
 
 
 @pytest.mark.parametrize("M,N,K,want", [
@@ -68,8 +69,9 @@ def test_plan_rejects_bad_shapes(L, M, N, K, want):
 
 
 def test_plan_rejects_bad_options(L):
-    for field, val in [("sf_layout", 2), ("sf_path", 5), ("cache_b_scales", 3), ("tile_n", 96),
-                       ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8)]:
+    for field, val in [("sf_layout", 2), ("sf_path", 5), ("cache_b_scales", 3), ("tile_n", 80),
+                       ("tile_n", 224), ("tile_n", 256), ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8),
+                       ("b_stages", 3), ("a_stages", 9)]:
         opt = nb.nvfp4_ggemm_default_options()
         setattr(opt, field, val)
         st, h = nb.nvfp4_ggemm_plan(0, [64], 256, 256, opt)

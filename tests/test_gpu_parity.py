@@ -46,7 +46,7 @@ RAGGED = dict(M=[1, 127, 129, 0, 200, 384, 64], N=328, K=768)
 
 
 @pytest.mark.parametrize("layout,path", PATHS)
-@pytest.mark.parametrize("tile_n", [128, 64])
+@pytest.mark.parametrize("tile_n", [192, 160, 128, 96, 64, 32])
 def test_ragged_full(O, layout, path, tile_n):
     prob = synth.make_problem("custom", seed=5, **RAGGED)
     ref, _ = O.grouped(prob)
@@ -287,6 +287,27 @@ def test_narrow_n(O, N):
         got = run_gpu(prob, sf_layout=layout, sf_path=path)
         for g in range(prob.G):
             assert_close(got[g], ref[g], f"N={N} {layout}/{path} group {g}")
+
+
+@pytest.mark.parametrize("tile_n,b_stages,a_stages", [(192, 5, 2), (192, 4, 3), (192, 6, 2), (128, 7, 2)])
+def test_pipeline_depth_variants(O, tile_n, b_stages, a_stages):
+    prob = synth.make_problem("custom", seed=13, M=[200, 64, 256], N=392, K=2048)
+    ref, _ = O.grouped(prob)
+    got = run_gpu(prob, tile_n=tile_n, b_stages=b_stages, a_stages=a_stages)
+    for g in range(prob.G):
+        assert_close(got[g], ref[g], f"{tile_n}: {b_stages}/{a_stages} group {g}")
+
+
+@pytest.mark.parametrize("grid", [1, 3, 37])
+def test_small_grids_split_the_chunks(O, grid):
+    """Fewer CTAs than chunks: each CTA walks a longer range, crossing groups
+    and row tiles."""
+    prob = synth.make_problem("custom", seed=14, M=[130, 0, 520, 1], N=264, K=512)
+    ref, _ = O.grouped(prob)
+    for layout, path in PATHS:
+        got = run_gpu(prob, sf_layout=layout, sf_path=path, max_ctas=grid)
+        for g in range(prob.G):
+            assert_close(got[g], ref[g], f"grid {grid} {layout}/{path} group {g}")
 
 
 def test_single_group_plain_gemm_and_one_cta(O):
