@@ -47,6 +47,7 @@ EXPORTED = (
     "nvfp4_status_string",
     "nvfp4_ggemm_version",
     "nvfp4_ggemm_run_noalloc",
+    "nvfp4_ggemm_schedule",
 )
 
 
@@ -134,6 +135,10 @@ def lib() -> ctypes.CDLL:
     L.nvfp4_ggemm_run_noalloc.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                           ctypes.c_int32, _VPP, _VPP, _VPP, _VPP, _VPP, _VP,
                                           ctypes.POINTER(ctypes.c_uint32)]
+    L.nvfp4_ggemm_schedule.restype = ctypes.c_int
+    L.nvfp4_ggemm_schedule.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32)]
     _lib = L
     return L
 
@@ -257,6 +262,18 @@ def nvfp4_ggemm_run_noalloc(M: Sequence[int], N: int, K: int, A, B, SFA, SFB, C,
                                        _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C), _stream(stream),
                                        ctypes.byref(word) if wait else None)
     return st, int(word.value)
+
+
+def nvfp4_ggemm_schedule(M: Sequence[int], N: int, tile_n: int = 0, max_ctas: int = 148) -> Tuple[int, List[int]]:
+    """Per-CTA chunk ranges a plan would use (host only). Returns
+    (status, cta_begin[0..grid])."""
+    m = (ctypes.c_int32 * max(1, len(M)))(*[int(v) for v in M])
+    out = (ctypes.c_int32 * (max(1, int(max_ctas)) + 1))()
+    grid = ctypes.c_int32(0)
+    st = lib().nvfp4_ggemm_schedule(len(M), m, int(N), int(tile_n), int(max_ctas), out, ctypes.byref(grid))
+    if st != NVFP4_OK:
+        return st, []
+    return st, [int(out[i]) for i in range(grid.value + 1)] if grid.value > 0 else [0]
 
 
 # -------------------------------------------------------------- convenience

@@ -24,7 +24,7 @@ constexpr int32_t kMaxN = 1 << 20;
 constexpr int32_t kMaxK = 1 << 18;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kSlots = 4;  // problem-table ring: a table is rewritten only after its last kernel finished
-constexpr int kDefaultTileN = 192;
+constexpr int kDefaultTileN = 256;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -81,8 +81,8 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
     return r == CUDA_SUCCESS;
 }
 
-// Smallest kernel tile width (128 or 192) that holds `tile_n` columns.
-int variant_width(int tile_n) { return tile_n <= 128 ? 128 : 192; }
+// Smallest kernel tile width (128 or 256) that holds `tile_n` columns.
+int variant_width(int tile_n) { return tile_n <= 128 ? 128 : 256; }
 
 struct Slot {
     uint8_t *h_table = nullptr;  // pinned staging
@@ -99,6 +99,70 @@ namespace nvfp4 {
 TensorMapEncodeFn tensor_map_encoder()
 {
     return load_encode() ? reinterpret_cast<TensorMapEncodeFn>(g_encode) : nullptr;
+}
+
+int pair_cap_chunks(int max_n) { return (max_n >= 192 ? 192 : max_n) / kChunkN; }
+
+int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair, int max_ctas,
+                  int32_t *cta_begin, int32_t *counts)
+{
+    max_ctas = std::max(1, std::min(max_ctas, kMaxCtas));
+    // segments: pairs of row tiles; the last pair of a group with an odd tile count has one
+    long seg1 = 0, seg2 = 0;
+    for (int g = 0; g < G; ++g) {
+        seg2 += m_tiles[g] / 2;
+        seg1 += m_tiles[g] % 2;
+    }
+    const long nseg = seg1 + seg2;
+    const long total = nseg * (long)n_chunks;
+    if (total == 0) {
+        cta_begin[0] = 0;
+        return 0;
+    }
+    auto tiles_for = [&](int cap) { return (long)ceil_div(n_chunks, cap); };
+    const int cap_max = std::max(cap_single, cap_pair);
+    const long fewest = seg1 * tiles_for(cap_single) + seg2 * tiles_for(cap_pair);
+    if (fewest > max_ctas) {
+        // more tiles than CTAs: equal contiguous chunk ranges
+        const int grid = (int)std::min<long>(total, max_ctas);
+        for (int c = 0; c <= grid; ++c) cta_begin[c] = (int32_t)((long)c * total / grid);
+        return grid;
+    }
+    // one tile per CTA: the smallest per-CTA width X (chunks) that fits the grid
+    int X = cap_max;
+    for (int x = 1; x <= cap_max; ++x) {
+        const long need = seg1 * tiles_for(std::min(x, cap_single)) + seg2 * tiles_for(std::min(x, cap_pair));
+        if (need <= max_ctas) {
+            X = x;
+            break;
+        }
+    }
+    int grid = 0;
+    {
+        long s = 0;
+        for (int g = 0; g < G; ++g)
+            for (int t = 0; t < m_tiles[g]; t += 2, ++s)
+                counts[s] = (int32_t)tiles_for(std::min(X, (m_tiles[g] - t) >= 2 ? cap_pair : cap_single));
+        for (long i = 0; i < nseg; ++i) grid += counts[i];
+    }
+    // spare CTAs narrow the widest tiles further
+    for (; grid < max_ctas; ++grid) {
+        long best = -1;
+        for (long i = 0; i < nseg; ++i) {
+            if (counts[i] >= n_chunks) continue;
+            // compare n/counts[i] > n/counts[best]  <=>  counts[i] < counts[best]
+            if (best < 0 || counts[i] < counts[best]) best = i;
+        }
+        if (best < 0) break;
+        ++counts[best];
+    }
+    int c = 0;
+    for (long i = 0; i < nseg; ++i) {
+        const long base = i * (long)n_chunks;
+        for (int j = 0; j < counts[i]; ++j) cta_begin[c++] = (int32_t)(base + (long)j * n_chunks / counts[i]);
+    }
+    cta_begin[c] = (int32_t)total;
+    return c;
 }
 
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
@@ -145,10 +209,10 @@ struct nvfp4_ggemm_plan_s {
     int grid = 0;
     int total_chunks = 0;
     int n_chunks = 0;
-    int max_tile_chunks = 8;
+    int cap_single = 8, cap_pair = 6;
     int k_tiles = 0;
-    std::vector<int32_t> m_tiles, m_pairs, chunk_prefix;
-    size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
+    std::vector<int32_t> m_tiles, m_pairs, chunk_prefix, cta_begin;
+    size_t off_prefix = 0, off_cta = 0, off_jobs = 0, table_bytes = 0;
     Slot slots[kSlots];
     int cur = -1;
     uint32_t *d_err = nullptr;
@@ -226,6 +290,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     int njobs = 0, items = 0;
     const int pieces = K / 256;
     for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
+    std::memcpy(tab + p->off_cta, p->cta_begin.data(), sizeof(int32_t) * p->cta_begin.size());
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
         d.M = p->M[g];
@@ -334,6 +399,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
+    gp.cta_begin = reinterpret_cast<const int32_t *>(s.d_table + p->off_cta);
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
@@ -342,7 +408,8 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     gp.k_tiles = p->k_tiles;
     gp.n_chunks = p->n_chunks;
     gp.total_chunks = p->total_chunks;
-    gp.max_tile_chunks = p->max_tile_chunks;
+    gp.cap_single = p->cap_single;
+    gp.cap_pair = p->cap_pair;
     gp.wide_rows = p->var.max_n;
     gp.debug_skip_load = p->opt.debug_skip_load;
     if (ggemm_launch(p->variant, gp, p->grid, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -369,6 +436,30 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->debug_skip_load = 0;
     opt->b_stages = 0;
     opt->a_stages = 0;
+}
+
+nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, int32_t N, int32_t tile_n, int32_t max_ctas,
+                                    int32_t *cta_begin, int32_t *grid)
+{
+    if (!M || !cta_begin || !grid || num_groups < 1 || num_groups > kMaxGroups) return NVFP4_ERR_INVALID_ARG;
+    if (max_ctas < 1 || max_ctas > kMaxCtas) return NVFP4_ERR_INVALID_ARG;
+    if (N < 8 || N > kMaxN || N % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (tile_n == 0) tile_n = kDefaultTileN;
+    if (tile_n < kChunkN || tile_n > kMaxTileN || tile_n % kChunkN != 0) return NVFP4_ERR_INVALID_ARG;
+    std::vector<int32_t> m_tiles(num_groups), counts(kMaxCtas, 0);
+    long total = 0;
+    const int n_chunks = ceil_div(N, kChunkN);
+    for (int g = 0; g < num_groups; ++g) {
+        if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
+        m_tiles[g] = ceil_div(M[g], kTileM);
+        total += (long)ceil_div(m_tiles[g], kRowTilesPerUnit) * n_chunks;
+    }
+    if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int cap_single = tile_n / kChunkN;
+    const int cap_pair = std::min(cap_single, pair_cap_chunks(variant_width(tile_n)));
+    *grid = schedule_ctas(m_tiles.data(), num_groups, n_chunks, cap_single, cap_pair, max_ctas, cta_begin,
+                          counts.data());
+    return NVFP4_OK;
 }
 
 nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_groups, const int32_t *M, int32_t N,
@@ -423,7 +514,8 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     }
 
     // Work decomposition: m_pairs_g x ceil(N/32) chunks per group, prefix-summed.
-    p->max_tile_chunks = opt.tile_n / kChunkN;
+    p->cap_single = opt.tile_n / kChunkN;
+    p->cap_pair = std::min(p->cap_single, pair_cap_chunks(p->var.max_n));
     p->n_chunks = ceil_div(N, kChunkN);
     p->chunk_prefix.assign(num_groups + 1, 0);
     p->m_tiles.assign(num_groups, 0);
@@ -441,11 +533,18 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     }
     p->chunk_prefix[num_groups] = (int32_t)total;
     p->total_chunks = (int)total;
-    const int cap = opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms;
-    p->grid = std::max(1, std::min(p->total_chunks, cap));
+    const int cap = std::min(opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms, kMaxCtas);
+    p->cta_begin.assign(cap + 1, 0);
+    {
+        std::vector<int32_t> counts(kMaxCtas, 0);
+        p->grid = schedule_ctas(p->m_tiles.data(), num_groups, p->n_chunks, p->cap_single, p->cap_pair, cap,
+                                p->cta_begin.data(), counts.data());
+    }
+    p->cta_begin.resize(p->grid + 1);
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
-    p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
+    p->off_cta = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
+    p->off_jobs = align_up(p->off_cta + sizeof(int32_t) * (size_t)(p->grid + 1), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
     bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&
@@ -674,7 +773,7 @@ uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K)
 nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info)
 {
     if (!plan || !info) return NVFP4_ERR_INVALID_ARG;
-    info->tile_n = plan->max_tile_chunks * kChunkN;
+    info->tile_n = plan->cap_single * kChunkN;
     info->b_stages = plan->var.b_stages;
     info->a_stages = plan->var.a_stages;
     info->chunks = plan->total_chunks;

@@ -14,7 +14,8 @@ constexpr int kTileK = 256;        // k per pipeline stage: one 128-byte swizzle
 constexpr int kMmaK = 64;          // k per tcgen05.mma of kind::mxf4nvf4
 constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k in the atom layout
 constexpr int kChunkN = 32;        // scheduling grain along N (columns)
-constexpr int kMaxTileN = 192;     // widest output tile any kernel variant supports
+constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
+constexpr int kMaxCtas = 1024;     // largest persistent grid the schedule describes
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
 
 // Wait sites recorded in the error word (bits 8-15).
@@ -58,19 +59,22 @@ static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-
 
 // Work decomposition: group g owns m_pairs_g * ceil(N/32) chunks (32 columns
 // of one pair of 128-row tiles), numbered after the chunks of groups 0..g-1
-// (chunk_prefix), pair by pair. CTA c takes the chunk range
-// [c*W/grid, (c+1)*W/grid) and walks it as tiles of up to max_tile_chunks
-// chunks inside one pair.
+// (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N/32) chunks.
+// CTA c takes the chunk range [cta_begin[c], cta_begin[c+1]) and walks it as
+// tiles inside one segment of up to cap_pair chunks (segments with two row
+// tiles, whose accumulators share TMEM) or cap_single chunks (one row tile).
 struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
+    const int32_t *cta_begin;      // [grid+1]
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
     int32_t k_tiles;               // K / 256
     int32_t n_chunks;              // ceil(N / 32)
     int32_t total_chunks;
-    int32_t max_tile_chunks;       // 1..6
+    int32_t cap_single;            // chunks per tile, one row tile (1..MAXN/32)
+    int32_t cap_pair;              // chunks per tile, two row tiles
     int32_t wide_rows;             // rows of the wide B boxes (the kernel's widest tile)
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
 };
@@ -111,6 +115,20 @@ cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream);
 
 // Host helpers shared by the plan path and the allocation-free entry point.
+
+// Widest tile, in chunks, of a unit with two row tiles for a kernel whose
+// widest tile is max_n columns (their accumulators share TMEM).
+int pair_cap_chunks(int max_n);
+
+// Splits the chunks of all segments into per-CTA ranges, written to
+// cta_begin[0..grid], and returns grid (<= max_ctas <= kMaxCtas). When every
+// segment can be covered by tiles of at most its cap with no more than
+// max_ctas CTAs in total, each CTA gets one tile inside one segment, and the
+// tiles are sized to balance the columns (B bytes) per CTA; otherwise the
+// chunks are split into equal contiguous ranges. m_tiles[g] = ceil(M_g/128);
+// counts is scratch for kMaxCtas ints.
+int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair, int max_ctas,
+                  int32_t *cta_begin, int32_t *counts);
 using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                        const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                        CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,

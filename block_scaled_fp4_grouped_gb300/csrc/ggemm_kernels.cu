@@ -18,16 +18,18 @@
 //               the tensor pipe and ahead of the MMAs.
 //   warp 1      allocates TMEM; one lane issues kind::mxf4nvf4 block16 MMAs
 //               (M = 128 per row tile, N = tile width up to MAXN) into fp32
-//               accumulators and releases the A stage, the B stage and the
-//               scale buffer with tcgen05.commit.
+//               accumulators, then commits one stage-completion barrier that
+//               frees the stage's A and B slots and its TMEM scale buffer.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulators (one lane quarter
 //               each), RN to fp16, 16-byte stores of each row straight to C.
 // Work: group g owns m_pairs_g x ceil(N/32) chunks (32 columns of one pair
 // of 128-row tiles); the chunks of all groups are numbered through prefix
-// sums and split into equal contiguous ranges, one per CTA, so every SM
-// streams the same amount of B. A CTA walks its range as tiles of up to MAXN
-// columns. Both row tiles of a pair share every B stage, so each B strip is
-// read from HBM once, by one SM (groups of up to 256 rows).
+// sums, and the host gives every CTA a contiguous chunk range (cta_begin).
+// A CTA walks its range as tiles inside one pair: up to 192 columns when the
+// pair has two row tiles (their accumulators share TMEM) and up to MAXN when
+// it has one. Both row tiles of a pair share every B stage, so each B strip
+// is read from HBM once, by one SM. Where the grid allows, the host makes
+// each range a single tile, so a CTA streams its B strip in one pass over K.
 //
 // Every mbarrier wait is bounded by the plan's timeout: on expiry the waiter
 // records (status, site, block) in the error word, raises a CTA-wide abort
@@ -62,9 +64,18 @@ constexpr int kSfCols = 32 + 32;        // TMEM scale columns per stage: SFA 2 t
 
 constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 
+// Stage-completion ring: the MMA thread commits one barrier per stage, done[s %
+// kDoneRing], and every ring the MMAs read (A, B, TMEM scale buffers) takes
+// its "slot free" signal from it: the slot that stage s reuses in a ring of
+// depth D was last read by stage s - D. A ring is at most kDoneRing deep, so
+// a producer waiting for stage s - D can never see that barrier two phases on.
+constexpr int kDoneRing = 8;
+
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Cfg {
     static_assert(MAXN % 32 == 0 && MAXN >= 32 && MAXN <= kMaxTileN, "tile width");
+    // widest tile of a unit with two row tiles: both accumulators share TMEM
+    static constexpr int kPairN = MAXN >= 192 ? 192 : MAXN;
     static constexpr int kBStage = MAXN * (kTileK / 2);
     static constexpr int kAStage = kRowTilesPerUnit * kATileBytes;
     // scale stage: SFA (2 KB per row tile) then SFB: raw MAXN rows x 16 B, or
@@ -75,17 +86,19 @@ struct Cfg {
     static constexpr int kOffARing = 0;
     static constexpr int kOffBRing = NA * kAStage;
     static constexpr int kOffSRing = kOffBRing + NB * kBStage;
-    static constexpr int kAccCols = kRowTilesPerUnit * MAXN;  // one accumulator: both row tiles
+    static constexpr int kAccCols = kRowTilesPerUnit * kPairN;  // one accumulator: both row tiles
+    static_assert(MAXN <= kAccCols, "a one-row-tile unit uses the whole accumulator");
     static constexpr int kNumAcc = (2 * kAccCols + 2 * kSfCols <= (int)kTmemCols) ? 2 : 1;
     static constexpr int kSfBase = kNumAcc * kAccCols;
     static constexpr int kNT0 = ((int)kTmemCols - kSfBase) / kSfCols;
     static constexpr int kNT = kNT0 > 6 ? 6 : kNT0;  // TMEM scale buffers
     static constexpr int kOffBars = kOffSRing + NS * kSStage;
-    static constexpr int kNumBars = 2 * NB + 2 * NA + 2 * NS + 2 * kNT + 2 + 2 + 1;
+    static constexpr int kNumBars = NB + NA + 2 * NS + kNT + kDoneRing + 2 + 2 + 1;
     static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
     static_assert(kNT >= 2, "at least two TMEM scale buffers");
+    static_assert(NB <= kDoneRing && NA <= kDoneRing && kNT <= kDoneRing, "rings no deeper than the done ring");
     static_assert(kSfBase + kNT * kSfCols <= (int)kTmemCols, "TMEM budget");
     static_assert(kBStage % 1024 == 0 && kAStage % 1024 == 0, "stages keep 1024-byte swizzle alignment");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -105,9 +118,8 @@ struct Walker {
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
-        const long long W = p.total_chunks;
-        pos = (int)((long long)blockIdx.x * W / gridDim.x);
-        end = (int)((long long)(blockIdx.x + 1) * W / gridDim.x);
+        pos = __ldg(p.cta_begin + blockIdx.x);
+        end = __ldg(p.cta_begin + blockIdx.x + 1);
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
@@ -122,10 +134,10 @@ struct Walker {
         const int local = pos - __ldg(p.chunk_prefix + lo);
         const int mp = local / p.n_chunks;
         const int ch = local - mp * p.n_chunks;
-        const int w = min(min(p.max_tile_chunks, p.n_chunks - ch), end - pos);
         t.g = lo;
         t.mt0 = mp * kRowTilesPerUnit;
         t.mtu = min(kRowTilesPerUnit, p.groups[lo].m_tiles - t.mt0);
+        const int w = min(min(t.mtu == 2 ? p.cap_pair : p.cap_single, p.n_chunks - ch), end - pos);
         t.n0 = ch * kChunkN;
         t.ncols = w * kChunkN;
         pos += w;
@@ -139,12 +151,11 @@ __device__ __forceinline__ void record_error(uint32_t *err, uint32_t status, uin
     atomicCAS(err, 0u, word);
 }
 
-// Bounded wait for phase `parity` of `bar`. False when another warp aborted
-// or the timeout expired (then this thread records the error and aborts).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                        const GemmParams &p, uint32_t site)
+// Slow path of wait_phase, kept out of line so that the common case (the
+// phase has already completed) costs one try_wait and no call.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             const GemmParams &p, uint32_t site)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -155,6 +166,15 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
             return false;
         }
     }
+}
+
+// Bounded wait for phase `parity` of `bar`. False when another warp aborted
+// or the timeout expired (then this thread records the error and aborts).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          const GemmParams &p, uint32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, p, site);
 }
 
 // Bounded wait that ignores the abort flag: used at exit for a thread's own
@@ -189,6 +209,31 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
 __device__ __forceinline__ uint32_t word_at(const uint4 &v, int c)
 {
     return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+// Orders every later use of v after the preceding tcgen05.wait::ld (the
+// registers of a tcgen05.ld are written asynchronously).
+__device__ __forceinline__ void pin_registers(uint32_t (&v)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i]));
+}
+
+// RN to fp16 and 16-byte stores of 32 accumulator columns of one C row,
+// starting at column col0 (a multiple of 8); columns >= N are not written.
+__device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N, const uint32_t (&v)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (col0 + 8 * j < N) {
+            uint4 pk;
+            pk.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
+            pk.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
+            pk.z = pack_half2(v[8 * j + 4], v[8 * j + 5]);
+            pk.w = pack_half2(v[8 * j + 6], v[8 * j + 7]);
+            *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) = pk;
+        }
+    }
 }
 
 // A ring of mbarrier-guarded stages: position (stage, phase) advanced in step.
@@ -228,43 +273,43 @@ struct Roles {
     {
     }
 
+    static constexpr int kBarDone = NB + NA + 2 * NS + NT;
     __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBars + 8 * i; }
     __device__ __forceinline__ uint32_t b_full(int s) const { return bar(s); }
-    __device__ __forceinline__ uint32_t b_empty(int s) const { return bar(NB + s); }
-    __device__ __forceinline__ uint32_t a_full(int s) const { return bar(2 * NB + s); }
-    __device__ __forceinline__ uint32_t a_empty(int s) const { return bar(2 * NB + NA + s); }
-    __device__ __forceinline__ uint32_t s_full(int s) const { return bar(2 * NB + 2 * NA + s); }
-    __device__ __forceinline__ uint32_t s_empty(int s) const { return bar(2 * NB + 2 * NA + NS + s); }
-    __device__ __forceinline__ uint32_t sf_ready(int b) const { return bar(2 * NB + 2 * NA + 2 * NS + b); }
-    __device__ __forceinline__ uint32_t sf_free(int b) const { return bar(2 * NB + 2 * NA + 2 * NS + NT + b); }
-    __device__ __forceinline__ uint32_t acc_full(int a) const { return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + a); }
-    __device__ __forceinline__ uint32_t acc_empty(int a) const
+    __device__ __forceinline__ uint32_t a_full(int s) const { return bar(NB + s); }
+    __device__ __forceinline__ uint32_t s_full(int s) const { return bar(NB + NA + s); }
+    __device__ __forceinline__ uint32_t s_empty(int s) const { return bar(NB + NA + NS + s); }
+    __device__ __forceinline__ uint32_t sf_ready(int b) const { return bar(NB + NA + 2 * NS + b); }
+    __device__ __forceinline__ uint32_t done(int d) const { return bar(kBarDone + d); }
+    __device__ __forceinline__ uint32_t acc_full(int a) const { return bar(kBarDone + kDoneRing + a); }
+    __device__ __forceinline__ uint32_t acc_empty(int a) const { return bar(kBarDone + kDoneRing + 2 + a); }
+    __device__ __forceinline__ uint32_t drain() const { return bar(kBarDone + kDoneRing + 4); }
+
+    // Wait until the MMAs of stage j (< 0: none) have completed.
+    __device__ __forceinline__ bool wait_done(int j, uint32_t site) const
     {
-        return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + 2 + a);
+        if (j < 0) return true;
+        return wait_phase(done(j % kDoneRing), (uint32_t)(j / kDoneRing) & 1u, abort_flag, p, site);
     }
-    __device__ __forceinline__ uint32_t drain() const { return bar(2 * NB + 2 * NA + 2 * NS + 2 * NT + 4); }
+    __device__ __forceinline__ bool warp_wait_done(int j, uint32_t site) const
+    {
+        if (j < 0) return true;
+        return warp_wait_phase(done(j % kDoneRing), (uint32_t)(j / kDoneRing) & 1u, abort_flag, p, site);
+    }
     __device__ __forceinline__ uint32_t b_stage(int s) const { return sbase + C::kOffBRing + s * C::kBStage; }
     __device__ __forceinline__ uint32_t a_stage(int s) const { return sbase + C::kOffARing + s * C::kAStage; }
     __device__ __forceinline__ uint32_t s_stage(int s) const { return sbase + C::kOffSRing + s * C::kSStage; }
 
     __device__ void init_barriers()
     {
-        for (int s = 0; s < NB; ++s) {
-            mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), 1);
-        }
-        for (int s = 0; s < NA; ++s) {
-            mbar_init(a_full(s), 1);
-            mbar_init(a_empty(s), 1);
-        }
+        for (int s = 0; s < NB; ++s) mbar_init(b_full(s), 1);
+        for (int s = 0; s < NA; ++s) mbar_init(a_full(s), 1);
+        for (int d = 0; d < kDoneRing; ++d) mbar_init(done(d), 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(s_full(s), 1);
             mbar_init(s_empty(s), kNumSfWarps);
         }
-        for (int b = 0; b < NT; ++b) {
-            mbar_init(sf_ready(b), kNumSfWarps);
-            mbar_init(sf_free(b), 1);
-        }
+        for (int b = 0; b < NT; ++b) mbar_init(sf_ready(b), kNumSfWarps);
         for (int a = 0; a < 2; ++a) {
             mbar_init(acc_full(a), 1);
             mbar_init(acc_empty(a), kNumEpiWarps);
@@ -281,7 +326,7 @@ struct Roles {
         const uint64_t pol_keep = policy_evict_normal();    // read again by the group's other row tiles
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1, loads = 0;
+        int last_g = -1, loads = 0, seq = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
@@ -297,10 +342,11 @@ struct Roles {
             const int boxes = t.ncols / 32;
             const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_phase(b_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteBEmpty)) {
+                if (!wait_done(seq - NB, kSiteBEmpty)) {
                     ok = false;
                     break;
                 }
+                ++seq;
                 ++loads;
                 const bool skip = (p.debug_skip_load > 0 && blockIdx.x == 0 && loads == p.debug_skip_load);
                 if (!skip) {
@@ -332,7 +378,7 @@ struct Roles {
         const uint64_t pol = policy_evict_last();  // A tiles are re-read by every column tile
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1;
+        int last_g = -1, seq = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
@@ -343,10 +389,11 @@ struct Roles {
                 last_g = t.g;
             }
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_phase(a_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteAEmpty)) {
+                if (!wait_done(seq - NA, kSiteAEmpty)) {
                     ok = false;
                     break;
                 }
+                ++seq;
                 const uint32_t fb = a_full(r.stage);
                 mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
 #pragma unroll
@@ -441,6 +488,7 @@ struct Roles {
     {
         const int q = warp & 3;
         RingPos rs, rt;
+        int seq = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
@@ -449,11 +497,12 @@ struct Roles {
             sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
             const int s0 = (t.n0 % 128) / 32;
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!warp_wait_phase(sf_free(rt.stage), rt.phase ^ 1u, abort_flag, p, kSiteSfFree) ||
+                if (!warp_wait_done(seq - NT, kSiteSfFree) ||
                     !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull)) {
                     ok = false;
                     break;
                 }
+                ++seq;
                 const uint8_t *sa = smem + C::kOffSRing + rs.stage * C::kSStage;
                 const uint8_t *sb = sa + C::kSfaBytes;
                 uint32_t va[32], vb[32];
@@ -535,6 +584,7 @@ struct Roles {
     __device__ void mma_issuer(uint32_t tmem)
     {
         RingPos ra, rb, rt, racc;
+        int seq = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
@@ -560,14 +610,13 @@ struct Roles {
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
                         if (mt < t.mtu)
-                            tc_mma_nvf4(d + (uint32_t)(mt * MAXN), desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32),
+                            tc_mma_nvf4(d + (uint32_t)(mt * C::kPairN), desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32),
                                         bdesc, idesc, sf + mt * 16 + kk * 4, sf + 32 + kk * 8,
                                         (kt | kk) != 0 ? 1u : 0u);
                 }
                 // the stages and the scale buffer are free once these MMAs have read them
-                tc_commit(b_empty(rb.stage));
-                tc_commit(a_empty(ra.stage));
-                tc_commit(sf_free(rt.stage));
+                tc_commit(done(seq % kDoneRing));
+                ++seq;
                 ra.advance<NA>();
                 rb.advance<NB>();
                 rt.advance<NT>();
@@ -592,6 +641,9 @@ struct Roles {
             const GroupDesc *gd = p.groups + t.g;
             if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
             tc_fence_after_sync();
+            // columns [n0, n0 + 32 * nblk) hold live data; two tcgen05.ld in
+            // flight: block c + 1 is read while block c is converted and stored
+            const int nblk = (min(t.ncols, p.N - t.n0) + 31) / 32;
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
@@ -599,27 +651,21 @@ struct Roles {
                 const int row = row0 + lane;
                 const bool live = row < gd->M;
                 uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)p.N;
+                const uint32_t tbase =
+                    tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN);
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(tbase, v0);
 #pragma unroll 1
-                for (int c = 0; c < t.ncols / 32; ++c) {
-                    const int col0 = t.n0 + c * 32;
-                    if (col0 >= p.N) break;
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) +
-                                           (uint32_t)(racc.stage * C::kAccCols + mt * MAXN + c * 32),
-                                       v);
+                for (int c = 0; c < nblk; c += 2) {
                     tmem_ld_wait();
-                    if (live) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (col0 + 8 * j < p.N) {
-                                uint4 pk;
-                                pk.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
-                                pk.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
-                                pk.z = pack_half2(v[8 * j + 4], v[8 * j + 5]);
-                                pk.w = pack_half2(v[8 * j + 6], v[8 * j + 7]);
-                                *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) = pk;
-                            }
-                        }
+                    pin_registers(v0);
+                    if (c + 1 < nblk) tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (c + 1)), v1);
+                    if (live) store_row_block(crow, t.n0 + 32 * c, p.N, v0);
+                    if (c + 1 < nblk) {
+                        tmem_ld_wait();
+                        pin_registers(v1);
+                        if (c + 2 < nblk) tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (c + 2)), v0);
+                        if (live) store_row_block(crow, t.n0 + 32 * (c + 1), p.N, v1);
                     }
                 }
             }
@@ -737,9 +783,9 @@ constexpr VariantEntry make_entry(bool is_default)
 
 // (MAXN, B stages, A stages, scale stages, raw scales)
 const VariantEntry kVariants[] = {
-    make_entry<192, 5, 2, 4, true>(true),  make_entry<192, 5, 2, 3, false>(true),
-    make_entry<192, 4, 3, 4, true>(false), make_entry<192, 6, 2, 2, true>(false),
-    make_entry<128, 7, 2, 4, true>(true),  make_entry<128, 6, 2, 3, false>(true),
+    make_entry<256, 4, 2, 4, true>(true),  make_entry<256, 4, 2, 3, false>(true),
+    make_entry<256, 3, 3, 4, true>(false), make_entry<128, 8, 2, 4, true>(true),
+    make_entry<128, 8, 2, 3, false>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 

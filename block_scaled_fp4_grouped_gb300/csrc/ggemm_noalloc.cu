@@ -7,6 +7,7 @@
 // one file-scope device array that every GPU loading the library holds
 // until the process exits. It runs the same persistent GEMM kernel as
 // nvfp4_ggemm_run on the raw-scale FUSED path with its default tiles.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -21,12 +22,15 @@ namespace {
 constexpr int kNoAllocMaxGroups = 64;
 constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 56 KB
 constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
-constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
+constexpr size_t kCtaOffset = kPrefixOffset + 512;                              // int32[grid+1]
+constexpr size_t kCtaBytes = 4352;
+constexpr size_t kErrOffset = kCtaOffset + kCtaBytes;                           // uint32 error word
 constexpr size_t kScratchBytes = kErrOffset + 256;
 static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
+static_assert(sizeof(int32_t) * (kMaxCtas + 1) <= kCtaBytes, "CTA range area");
 static_assert(kScratchBytes <= 64 * 1024, "the array stays within 64 KB");
 
-// The scratch: problem table, unit prefix sums, error word. In host code this
+// The scratch: problem table, chunk prefix sums, per-CTA chunk ranges, error word. In host code this
 // name is only a host-side stand-in; the device address comes from
 // cudaGetSymbolAddress, once per device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
@@ -110,12 +114,14 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     auto *groups = reinterpret_cast<GroupDesc *>(table);
     auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
     const int n_chunks = ceil_div_i(N, kChunkN);
+    int32_t m_tiles[kNoAllocMaxGroups];
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         GroupDesc &d = groups[g];
         d.M = M[g];
         d.m_tiles = ceil_div_i(M[g], kTileM);
         d.m_pairs = ceil_div_i(d.m_tiles, kRowTilesPerUnit);
+        m_tiles[g] = d.m_tiles;
         d.chunk_begin = (int32_t)total;
         prefix[g] = (int32_t)total;
         total += (long)d.m_pairs * n_chunks;
@@ -127,6 +133,13 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     prefix[num_groups] = (int32_t)total;
     if (total == 0) return NVFP4_OK;
     if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    const int cap_single = kMaxTileN / kChunkN;
+    const int cap_pair = pair_cap_chunks(kMaxTileN);
+    int32_t cta_begin[kMaxCtas + 1];
+    int32_t counts[kMaxCtas];
+    const int grid = schedule_ctas(m_tiles, num_groups, n_chunks, cap_single, cap_pair,
+                                   std::min(g_sm_count[dev], kMaxCtas), cta_begin, counts);
+    if (grid < 1) return NVFP4_OK;
 
     // --- upload (pageable source: the call returns once the bytes are staged,
     //     so the stack buffer may go away), clear the error word, launch
@@ -135,6 +148,8 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     if (cudaMemcpyAsync(scratch, table, used, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(scratch + kPrefixOffset, prefix, sizeof(int32_t) * (size_t)(num_groups + 1),
                         cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(scratch + kCtaOffset, cta_begin, sizeof(int32_t) * (size_t)(grid + 1), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess ||
         cudaMemsetAsync(scratch + kErrOffset, 0, sizeof(uint32_t), s) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
@@ -142,6 +157,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
+    gp.cta_begin = reinterpret_cast<const int32_t *>(scratch + kCtaOffset);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
@@ -150,10 +166,10 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.k_tiles = K / kTileK;
     gp.n_chunks = n_chunks;
     gp.total_chunks = (int32_t)total;
-    gp.max_tile_chunks = kMaxTileN / kChunkN;
+    gp.cap_single = cap_single;
+    gp.cap_pair = cap_pair;
     gp.wide_rows = kMaxTileN;
     gp.debug_skip_load = 0;
-    const int grid = (int)(total < g_sm_count[dev] ? total : g_sm_count[dev]);
     if (ggemm_launch(variant, gp, grid, s) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;

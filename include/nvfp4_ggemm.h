@@ -90,20 +90,21 @@ typedef struct {
     int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
                                  nvfp4_ggemm_prepare_b_scales and run skips it */
     uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
-    int32_t tile_n;           /* widest output tile in columns: 0 = 192, else a multiple of 32
-                                 up to 192 (kernels exist for 128 and 192; a smaller value
-                                 caps the tiles of the next wider kernel). Each tile covers
-                                 up to two 128-row tiles of one group, which share every
-                                 B stage */
+    int32_t tile_n;           /* widest output tile in columns: 0 = 256, else a multiple of 32
+                                 up to 256 (kernels exist for 128 and 256; a smaller value
+                                 caps the tiles of the next wider kernel). A tile covers one
+                                 or two 128-row tiles of one group, which share every B
+                                 stage; with two row tiles it is at most 192 columns wide
+                                 (128 for the 128 kernel), as both accumulators share TMEM */
     int32_t max_ctas;         /* persistent grid size: 0 = number of SMs */
     int32_t debug_skip_load;  /* test only: 0 = off; n > 0 = the B producer of CTA 0 leaves its
                                  n-th stage load unissued, so the consumers' waits run into the
                                  timeout (exercises the error path) */
     int32_t b_stages;         /* shared-memory stages of the B ring; 0 (with a_stages 0) = the
                                  default for the tile width and scale path. Kernels exist for
-                                 (tile width, b_stages, a_stages) = (192,5,2), (192,4,3),
-                                 (192,6,2) with raw scales and the defaults (192,5,2),
-                                 (128,7,2) raw and (192,5,2), (128,6,2) atom */
+                                 (tile width, b_stages, a_stages) = (256,4,2) (default),
+                                 (256,3,3) and (128,8,2) (default) with raw scales, and the
+                                 defaults (256,4,2), (128,8,2) with atom-layout scales */
     int32_t a_stages;         /* shared-memory stages of the A ring (see b_stages) */
     int32_t reserved[3];
 } nvfp4_ggemm_options_t;
@@ -181,6 +182,23 @@ NVFP4_API nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t ro
 
 /* Bytes of the atom-layout copy of a [rows, K/16] scale matrix. */
 NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
+
+/*
+ * The work split a plan would use, computed on the host alone (no device,
+ * no allocation). Every group with M_g > 0 has ceil(ceil(M_g/128)/2) pairs
+ * of 128-row tiles; each pair owns ceil(N/32) consecutive 32-column chunks,
+ * numbered group by group. CTA c of the persistent grid takes chunks
+ * [cta_begin[c], cta_begin[c+1]). tile_n (0 = 256) and the kernel width it
+ * selects cap the tiles as in nvfp4_ggemm_options_t. When every pair can be
+ * covered by such tiles with at most max_ctas CTAs, each CTA gets one tile
+ * inside one pair and the tiles are sized to even out the columns per CTA;
+ * otherwise the chunks are cut into equal contiguous ranges. cta_begin must
+ * hold max_ctas + 1 entries (max_ctas 1..1024); *grid receives the CTA
+ * count (0 when every M_g is 0). This is not an operation of the pages; it
+ * exposes the scheduling step for inspection and testing.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, int32_t N, int32_t tile_n,
+                                    int32_t max_ctas, int32_t *cta_begin, int32_t *grid);
 
 /* Plan introspection (for tests and benchmarks). */
 typedef struct {

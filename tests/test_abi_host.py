@@ -70,7 +70,7 @@ def test_plan_rejects_bad_shapes(L, M, N, K, want):
 
 def test_plan_rejects_bad_options(L):
     for field, val in [("sf_layout", 2), ("sf_path", 5), ("cache_b_scales", 3), ("tile_n", 80),
-                       ("tile_n", 224), ("tile_n", 256), ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8),
+                       ("tile_n", 288), ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8),
                        ("b_stages", 3), ("a_stages", 9)]:
         opt = nb.nvfp4_ggemm_default_options()
         setattr(opt, field, val)

@@ -46,7 +46,7 @@ RAGGED = dict(M=[1, 127, 129, 0, 200, 384, 64], N=328, K=768)
 
 
 @pytest.mark.parametrize("layout,path", PATHS)
-@pytest.mark.parametrize("tile_n", [192, 160, 128, 96, 64, 32])
+@pytest.mark.parametrize("tile_n", [256, 224, 192, 160, 128, 96, 64, 32])
 def test_ragged_full(O, layout, path, tile_n):
     prob = synth.make_problem("custom", seed=5, **RAGGED)
     ref, _ = O.grouped(prob)
@@ -289,7 +289,7 @@ def test_narrow_n(O, N):
             assert_close(got[g], ref[g], f"N={N} {layout}/{path} group {g}")
 
 
-@pytest.mark.parametrize("tile_n,b_stages,a_stages", [(192, 5, 2), (192, 4, 3), (192, 6, 2), (128, 7, 2)])
+@pytest.mark.parametrize("tile_n,b_stages,a_stages", [(256, 4, 2), (256, 3, 3), (128, 8, 2)])
 def test_pipeline_depth_variants(O, tile_n, b_stages, a_stages):
     prob = synth.make_problem("custom", seed=13, M=[200, 64, 256], N=392, K=2048)
     ref, _ = O.grouped(prob)

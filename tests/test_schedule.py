@@ -1,0 +1,122 @@
+"""The work split (nvfp4_ggemm_schedule), checked on the host.
+
+Every group's pairs of 128-row tiles own ceil(N/32) consecutive chunks of 32
+columns; CTA c takes chunks [cta_begin[c], cta_begin[c+1]). These tests
+check the split against properties fixed by that definition: the ranges
+partition the chunks; when the grid holds one tile per CTA, each range lies
+in one pair and is no wider than that pair's cap (192 columns for two row
+tiles, tile_n for one), and no narrower cap would have fitted the grid;
+otherwise the ranges are equal to within one chunk."""
+import random
+
+import pytest
+
+from block_scaled_fp4_grouped_gb300 import binding as nb
+from block_scaled_fp4_grouped_gb300 import build as nbuild
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nbuild.build()
+
+
+def pairs_of(M):
+    """(chunk offset, row tiles in the pair) of every pair, in chunk order."""
+    out = []
+    for m in M:
+        tiles = -(-m // 128)
+        for t in range(0, tiles, 2):
+            out.append(min(2, tiles - t))
+    return out
+
+
+def caps(tile_n):
+    tile_n = tile_n or 256
+    kernel = 128 if tile_n <= 128 else 256
+    single = tile_n // 32
+    pair = min(single, (192 if kernel >= 192 else kernel) // 32)
+    return single, pair
+
+
+def fewest_ctas(M, N, tile_n, width=None):
+    single, pair = caps(tile_n)
+    n = -(-N // 32)
+    total = 0
+    for rows in pairs_of(M):
+        cap = pair if rows == 2 else single
+        if width is not None:
+            cap = min(cap, width)
+        total += -(-n // cap)
+    return total
+
+
+def check(M, N, tile_n, max_ctas):
+    st, cb = nb.nvfp4_ggemm_schedule(M, N, tile_n, max_ctas)
+    assert st == nb.NVFP4_OK
+    n = -(-N // 32)
+    segs = pairs_of(M)
+    total = len(segs) * n
+    grid = len(cb) - 1
+    if total == 0:
+        assert grid == 0
+        return cb
+    assert 1 <= grid <= max_ctas
+    assert cb[0] == 0 and cb[-1] == total
+    assert all(b > a for a, b in zip(cb, cb[1:])), "every CTA gets at least one chunk"
+    single, pair = caps(tile_n)
+    if fewest_ctas(M, N, tile_n) <= max_ctas:
+        widest = 0
+        for a, b in zip(cb, cb[1:]):
+            s = a // n
+            assert (b - 1) // n == s, f"range [{a},{b}) crosses a pair boundary"
+            cap = pair if segs[s] == 2 else single
+            assert b - a <= cap
+            widest = max(widest, b - a)
+        # no narrower widest tile would have fitted the grid
+        if widest > 1:
+            assert fewest_ctas(M, N, tile_n, widest - 1) > max_ctas
+    else:
+        sizes = [b - a for a, b in zip(cb, cb[1:])]
+        assert grid == min(total, max_ctas)
+        assert max(sizes) - min(sizes) <= 1
+    return cb
+
+
+def test_page_shape_gets_one_tile_per_cta():
+    # four-group-pairs-and-singles shape of the largest timed workload
+    M = [80, 176, 128, 72, 64, 248, 96, 160]
+    cb = check(M, 4096, 0, 152)
+    assert len(cb) - 1 == 152
+    widths = [b - a for a, b in zip(cb, cb[1:])]
+    assert max(widths) == 8  # 128 chunks over 17 CTAs per one-tile group
+
+
+def test_skinny_wide_shape_falls_back_to_equal_ranges():
+    M = [40, 76, 168, 72, 164, 148, 196, 160]
+    cb = check(M, 7168, 0, 152)
+    assert len(cb) - 1 == 152
+
+
+@pytest.mark.parametrize("tile_n", [0, 256, 224, 192, 128, 96, 32])
+def test_random_shapes(tile_n):
+    rng = random.Random(1234 + tile_n)
+    for _ in range(200):
+        G = rng.randint(1, 12)
+        M = [rng.choice([0, rng.randint(1, 700)]) for _ in range(G)]
+        N = 8 * rng.randint(1, 1200)
+        max_ctas = rng.choice([1, 3, 37, 148, 152, 1024])
+        check(M, N, tile_n, max_ctas)
+
+
+def test_empty_problem_has_no_ctas():
+    st, cb = nb.nvfp4_ggemm_schedule([0, 0], 256, 0, 152)
+    assert st == nb.NVFP4_OK and cb == [0]
+
+
+@pytest.mark.parametrize("kw", [dict(tile_n=80), dict(tile_n=288), dict(max_ctas=0), dict(max_ctas=1025),
+                                dict(N=12), dict(M=[-1])])
+def test_bad_arguments(kw):
+    args = dict(M=[64], N=256, tile_n=0, max_ctas=152)
+    args.update(kw)
+    st, _ = nb.nvfp4_ggemm_schedule(args["M"], args["N"], args["tile_n"], args["max_ctas"])
+    assert st in (nb.NVFP4_ERR_INVALID_ARG, nb.NVFP4_ERR_UNSUPPORTED_SHAPE)
