@@ -119,40 +119,44 @@ int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, i
         cta_begin[0] = 0;
         return 0;
     }
-    auto tiles_for = [&](int cap) { return (long)ceil_div(n_chunks, cap); };
-    const int cap_max = std::max(cap_single, cap_pair);
-    const long fewest = seg1 * tiles_for(cap_single) + seg2 * tiles_for(cap_pair);
-    if (fewest > max_ctas) {
-        // more tiles than CTAs: equal contiguous chunk ranges
+    // CTAs a segment needs when a CTA may take `passes` tiles of at most cap chunks
+    auto ctas_for = [&](int cap, long passes) { return (n_chunks + passes * cap - 1) / (passes * cap); };
+    auto need = [&](long passes) { return seg1 * ctas_for(cap_single, passes) + seg2 * ctas_for(cap_pair, passes); };
+    // the fewest passes per CTA with every CTA's range inside one segment
+    long P = 1;
+    if (nseg <= max_ctas)
+        while (need(P) > max_ctas) ++P;  // ends by P = n_chunks, where need(P) = nseg
+    if (nseg > max_ctas) {
+        // more segments than CTAs: equal contiguous chunk ranges
         const int grid = (int)std::min<long>(total, max_ctas);
         for (int c = 0; c <= grid; ++c) cta_begin[c] = (int32_t)((long)c * total / grid);
         return grid;
-    }
-    // one tile per CTA: the smallest per-CTA width X (chunks) that fits the grid
-    int X = cap_max;
-    for (int x = 1; x <= cap_max; ++x) {
-        const long need = seg1 * tiles_for(std::min(x, cap_single)) + seg2 * tiles_for(std::min(x, cap_pair));
-        if (need <= max_ctas) {
-            X = x;
-            break;
-        }
     }
     int grid = 0;
     {
         long s = 0;
         for (int g = 0; g < G; ++g)
             for (int t = 0; t < m_tiles[g]; t += 2, ++s)
-                counts[s] = (int32_t)tiles_for(std::min(X, (m_tiles[g] - t) >= 2 ? cap_pair : cap_single));
+                counts[s] = (int32_t)ctas_for((m_tiles[g] - t) >= 2 ? cap_pair : cap_single, P);
         for (long i = 0; i < nseg; ++i) grid += counts[i];
     }
-    // spare CTAs narrow the widest tiles further
+    // spare CTAs shorten the longest ranges, measured in passes, then in chunks
     for (; grid < max_ctas; ++grid) {
         long best = -1;
-        for (long i = 0; i < nseg; ++i) {
-            if (counts[i] >= n_chunks) continue;
-            // compare n/counts[i] > n/counts[best]  <=>  counts[i] < counts[best]
-            if (best < 0 || counts[i] < counts[best]) best = i;
-        }
+        long best_pass = 0, best_len = 0;
+        long s = 0;
+        for (int g = 0; g < G; ++g)
+            for (int t = 0; t < m_tiles[g]; t += 2, ++s) {
+                if (counts[s] >= n_chunks) continue;
+                const int cap = (m_tiles[g] - t) >= 2 ? cap_pair : cap_single;
+                const long len = (n_chunks + counts[s] - 1) / counts[s];  // longest range of this segment
+                const long pass = (len + cap - 1) / cap;
+                if (best < 0 || pass > best_pass || (pass == best_pass && len > best_len)) {
+                    best = s;
+                    best_pass = pass;
+                    best_len = len;
+                }
+            }
         if (best < 0) break;
         ++counts[best];
     }
@@ -175,7 +179,7 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
     d.m_pairs = ceil_div(d.m_tiles, kRowTilesPerUnit);
     d.b_keep = d.m_pairs > 1 ? 1 : 0;
     d.C = static_cast<uint16_t *>(C);
-    bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kTileM,
+    bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kBoxRows,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_2d(&d.tmB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, 32,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -183,11 +187,12 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return false;
     if (sf_raw) {
-        ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, kTileK / 16, kTileM,
+        const uint32_t sf_box = kSfKTiles * (kTileK / 16);  // bytes of one scale row per box
+        ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, sf_box, kBoxRows,
                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
-             encode_2d(&d.tmSFB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, kTileK / 16, 32,
+             encode_2d(&d.tmSFB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, 32,
                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
-             encode_2d(&d.tmSFBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, kTileK / 16, wide_rows,
+             encode_2d(&d.tmSFBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, wide_rows,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
         d.sfa_atoms = static_cast<const uint8_t *>(SFA);

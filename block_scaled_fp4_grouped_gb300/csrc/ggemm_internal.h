@@ -17,6 +17,8 @@ constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
 constexpr int kMaxCtas = 1024;     // largest persistent grid the schedule describes
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
+constexpr int kBoxRows = 32;       // rows of the A and scale TMA boxes (partial row tiles load only live boxes)
+constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
 
 // Wait sites recorded in the error word (bits 8-15).
 enum WaitSite : uint32_t {
@@ -39,12 +41,12 @@ enum WaitSite : uint32_t {
 // M_g / N. Two B maps: boxes as wide as the kernel's widest tile for
 // full-width tiles, 32-row boxes for the rest.
 struct alignas(128) GroupDesc {
-    CUtensorMap tmA;       // A_g bytes [M_g][K/2];   box 128 B x 128 rows; 128-byte swizzle
+    CUtensorMap tmA;       // A_g bytes [M_g][K/2];   box 128 B x 32 rows;  128-byte swizzle
     CUtensorMap tmB32;     // B_g bytes [N][K/2];     box 128 B x 32 rows;  128-byte swizzle
     CUtensorMap tmBw;      // B_g bytes [N][K/2];     box 128 B x wide rows; 128-byte swizzle
-    CUtensorMap tmSFA;     // raw SFA_g [M_g][K/16];  box 16 B x 128 rows   (raw-scale path)
-    CUtensorMap tmSFB32;   // raw SFB_g [N][K/16];    box 16 B x 32 rows    (raw-scale path)
-    CUtensorMap tmSFBw;    // raw SFB_g [N][K/16];    box 16 B x wide rows  (raw-scale path)
+    CUtensorMap tmSFA;     // raw SFA_g [M_g][K/16];  box 32 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFB32;   // raw SFB_g [N][K/16];    box 32 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFBw;    // raw SFB_g [N][K/16];    box 32 B x wide rows  (raw-scale path)
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
     const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
     uint16_t *C;               // C_g fp16 [M_g][N]

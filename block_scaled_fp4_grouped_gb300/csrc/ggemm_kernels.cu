@@ -47,13 +47,14 @@ using namespace ptx;
 
 constexpr int kWarpBProducer = 0;
 constexpr int kWarpMma = 1;
-constexpr int kWarpEpi0 = 2;
-constexpr int kNumEpiWarps = 4;
+constexpr int kWarpEpi0 = 2;    // epilogue warps 2-5: even 32-column blocks
+constexpr int kWarpEpi1 = 12;   // epilogue warps 12-15: odd 32-column blocks
+constexpr int kNumEpiWarps = 8;
 constexpr int kWarpAProducer = 6;
 constexpr int kWarpSProducer = 7;
 constexpr int kWarpSf0 = 8;
 constexpr int kNumSfWarps = 4;
-constexpr int kThreads = 12 * 32;
+constexpr int kThreads = 16 * 32;
 
 constexpr int kATileBytes = kTileM * (kTileK / 2);  // 16384: 128 rows x 128 B
 constexpr int kSfTileBytes = 4 * kSfAtomBytes;       // 2048: scales of 128 rows x 256 k
@@ -78,10 +79,15 @@ struct Cfg {
     static constexpr int kPairN = MAXN >= 192 ? 192 : MAXN;
     static constexpr int kBStage = MAXN * (kTileK / 2);
     static constexpr int kAStage = kRowTilesPerUnit * kATileBytes;
-    // scale stage: SFA (2 KB per row tile) then SFB: raw MAXN rows x 16 B, or
-    // up to three 128-row atom groups covering the tile
-    static constexpr int kSfaBytes = kRowTilesPerUnit * kSfTileBytes;
-    static constexpr int kSfbRegion = RAW ? MAXN * 16 : 3 * kSfTileBytes;
+    // scale stage: raw scales cover kKS k tiles (rows of 16 * kKS bytes): SFA
+    // (128 rows per row tile) then SFB (MAXN rows); atom-layout scales cover
+    // one k tile: SFA (2 KB per row tile) then up to three 128-row atom
+    // groups covering the tile's columns
+    static constexpr int kKS = RAW ? kSfKTiles : 1;
+    static constexpr int kSfRow = 16 * kKS;
+    static constexpr int kSfaTile = RAW ? kTileM * kSfRow : kSfTileBytes;
+    static constexpr int kSfaBytes = kRowTilesPerUnit * kSfaTile;
+    static constexpr int kSfbRegion = RAW ? MAXN * kSfRow : 3 * kSfTileBytes;
     static constexpr int kSStage = align1k(kSfaBytes + kSfbRegion);
     static constexpr int kOffARing = 0;
     static constexpr int kOffBRing = NA * kAStage;
@@ -115,6 +121,10 @@ struct Unit {
 // Walks this CTA's contiguous range of chunks as tiles.
 struct Walker {
     int pos, end;
+    // the part of the range inside the current pair: [pb, pb + plen) cut
+    // into pt tiles of equal width (to within one chunk); pi = next tile
+    int pb = 0, plen = 0, pt = 0, pi = 0;
+    int g = 0, mt0 = 0, mtu = 0, ch0 = 0;
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
@@ -124,23 +134,35 @@ struct Walker {
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
     {
-        if (pos >= end) return false;
-        int lo = 0, hi = p.G;  // prefix[lo] <= pos < prefix[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(p.chunk_prefix + mid) <= pos) lo = mid;
-            else hi = mid;
+        if (pi == pt) {
+            if (pos >= end) return false;
+            int lo = 0, hi = p.G;  // prefix[lo] <= pos < prefix[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(p.chunk_prefix + mid) <= pos) lo = mid;
+                else hi = mid;
+            }
+            const int local = pos - __ldg(p.chunk_prefix + lo);
+            const int mp = local / p.n_chunks;
+            ch0 = local - mp * p.n_chunks;
+            g = lo;
+            mt0 = mp * kRowTilesPerUnit;
+            mtu = min(kRowTilesPerUnit, p.groups[lo].m_tiles - mt0);
+            pb = pos;
+            plen = min(p.n_chunks - ch0, end - pos);
+            const int cap = mtu == 2 ? p.cap_pair : p.cap_single;
+            pt = (plen + cap - 1) / cap;
+            pi = 0;
+            pos += plen;
         }
-        const int local = pos - __ldg(p.chunk_prefix + lo);
-        const int mp = local / p.n_chunks;
-        const int ch = local - mp * p.n_chunks;
-        t.g = lo;
-        t.mt0 = mp * kRowTilesPerUnit;
-        t.mtu = min(kRowTilesPerUnit, p.groups[lo].m_tiles - t.mt0);
-        const int w = min(min(t.mtu == 2 ? p.cap_pair : p.cap_single, p.n_chunks - ch), end - pos);
-        t.n0 = ch * kChunkN;
-        t.ncols = w * kChunkN;
-        pos += w;
+        const int c0 = (int)((long long)plen * pi / pt);
+        const int c1 = (int)((long long)plen * (pi + 1) / pt);
+        ++pi;
+        t.g = g;
+        t.mt0 = mt0;
+        t.mtu = mtu;
+        t.n0 = (ch0 + c0) * kChunkN;
+        t.ncols = (c1 - c0) * kChunkN;
         return true;
     }
 };
@@ -219,20 +241,29 @@ __device__ __forceinline__ void pin_registers(uint32_t (&v)[32])
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i]));
 }
 
-// RN to fp16 and 16-byte stores of 32 accumulator columns of one C row,
-// starting at column col0 (a multiple of 8); columns >= N are not written.
-__device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N, const uint32_t (&v)[32])
+// RN to fp16 and stores of 32 accumulator columns of one C row, starting at
+// column col0 (a multiple of 32); columns >= N are not written. wide: the row
+// is 32-byte aligned and N % 16 == 0, so two 32-byte stores cover the block;
+// otherwise four 16-byte stores (N % 8 == 0).
+__device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N, const uint32_t (&v)[32], bool wide)
 {
+    uint32_t h[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (col0 + 8 * j < N) {
-            uint4 pk;
-            pk.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
-            pk.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
-            pk.z = pack_half2(v[8 * j + 4], v[8 * j + 5]);
-            pk.w = pack_half2(v[8 * j + 6], v[8 * j + 7]);
-            *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) = pk;
-        }
+    for (int i = 0; i < 16; ++i) h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+    if (wide) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (col0 + 16 * j < N)
+                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(crow + col0 + 16 * j),
+                             "r"(h[8 * j + 0]), "r"(h[8 * j + 1]), "r"(h[8 * j + 2]), "r"(h[8 * j + 3]),
+                             "r"(h[8 * j + 4]), "r"(h[8 * j + 5]), "r"(h[8 * j + 6]), "r"(h[8 * j + 7])
+                             : "memory");
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (col0 + 8 * j < N)
+                *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) =
+                    make_uint4(h[4 * j + 0], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
     }
 }
 
@@ -256,6 +287,20 @@ __device__ __forceinline__ void sfb_blocks(int n0, int ncols, int N, int &b0, in
     b0 = n0 / 128;
     const int last = min(n0 + ncols, N) - 1;
     nblk = last / 128 - b0 + 1;
+}
+
+// Per row tile of unit t: the 32-row boxes that hold rows < M (written to
+// live[]); returns their total.
+__device__ __forceinline__ int row_boxes(const Unit &t, int M, int (&live)[kRowTilesPerUnit])
+{
+    int total = 0;
+#pragma unroll
+    for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
+        const int rows = mt < t.mtu ? min(kTileM, M - (t.mt0 + mt) * kTileM) : 0;
+        live[mt] = (rows + kBoxRows - 1) / kBoxRows;
+        total += live[mt];
+    }
+    return total;
 }
 
 template <int MAXN, int NB, int NA, int NS, bool RAW>
@@ -388,19 +433,23 @@ struct Roles {
                 fence_tensormap_acquire(&gd->tmA);
                 last_g = t.g;
             }
+            int live_boxes[kRowTilesPerUnit];
+            const int boxes = row_boxes(t, gd->M, live_boxes);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!wait_done(seq - NA, kSiteAEmpty)) {
                     ok = false;
                     break;
                 }
                 ++seq;
+                // only the 32-row boxes that hold rows < M_g; the MMA rows past
+                // them read stale data and their accumulator rows are never stored
                 const uint32_t fb = a_full(r.stage);
-                mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
+                mbar_arrive_expect_tx(fb, (uint32_t)boxes * (kBoxRows * (kTileK / 2)));
 #pragma unroll
                 for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                    if (mt < t.mtu)
-                        tma_load_2d(a_stage(r.stage) + mt * kATileBytes, &gd->tmA, kt * (kTileK / 2),
-                                    (t.mt0 + mt) * kTileM, fb, pol);
+                    for (int b = 0; b < live_boxes[mt]; ++b)
+                        tma_load_2d(a_stage(r.stage) + mt * kATileBytes + b * (kBoxRows * (kTileK / 2)), &gd->tmA,
+                                    kt * (kTileK / 2), (t.mt0 + mt) * kTileM + b * kBoxRows, fb, pol);
                 issued_mask |= 1u << r.stage;
                 issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
                 r.advance<NA>();
@@ -419,6 +468,7 @@ struct Roles {
         int last_g = -1;
         bool ok = true;
         const size_t katoms = (size_t)(p.K / 64);
+        const int s_tiles = (p.k_tiles + C::kKS - 1) / C::kKS;  // scale stages per tile
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
@@ -430,12 +480,15 @@ struct Roles {
                 last_g = t.g;
             }
             const bool wide = (t.ncols == p.wide_rows);
-            const int boxes = t.ncols / 32;
+            const int bboxes = t.ncols / 32;
             int b0 = 0, nblk = 0;
             sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
-            const uint32_t bytes = (uint32_t)t.mtu * kSfTileBytes +
-                                   (RAW ? (uint32_t)t.ncols * 16u : (uint32_t)nblk * kSfTileBytes);
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            int live_boxes[kRowTilesPerUnit];
+            const int aboxes = row_boxes(t, gd->M, live_boxes);
+            const uint32_t bytes =
+                RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
+                    : (uint32_t)t.mtu * kSfTileBytes + (uint32_t)nblk * kSfTileBytes;
+            for (int ks = 0; ks < s_tiles; ++ks) {
                 if (!wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
                     ok = false;
                     break;
@@ -444,28 +497,30 @@ struct Roles {
                 const uint32_t st = s_stage(r.stage);
                 mbar_arrive_expect_tx(fb, bytes);
                 if (RAW) {
+                    // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1
+                    const int x = ks * C::kSfRow;
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                        if (mt < t.mtu)
-                            tma_load_2d(st + mt * kSfTileBytes, &gd->tmSFA, kt * (kTileK / 16), (t.mt0 + mt) * kTileM,
-                                        fb, pol);
+                        for (int bx = 0; bx < live_boxes[mt]; ++bx)
+                            tma_load_2d(st + mt * C::kSfaTile + bx * (kBoxRows * C::kSfRow), &gd->tmSFA, x,
+                                        (t.mt0 + mt) * kTileM + bx * kBoxRows, fb, pol);
                     if (wide) {
-                        tma_load_2d(st + C::kSfaBytes, &gd->tmSFBw, kt * (kTileK / 16), t.n0, fb, pol);
+                        tma_load_2d(st + C::kSfaBytes, &gd->tmSFBw, x, t.n0, fb, pol);
                     } else {
-                        for (int i = 0; i < boxes; ++i)
-                            tma_load_2d(st + C::kSfaBytes + i * 512, &gd->tmSFB32, kt * (kTileK / 16),
-                                        t.n0 + 32 * i, fb, pol);
+                        for (int i = 0; i < bboxes; ++i)
+                            tma_load_2d(st + C::kSfaBytes + i * (32 * C::kSfRow), &gd->tmSFB32, x, t.n0 + 32 * i, fb,
+                                        pol);
                     }
                 } else {
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
                         if (mt < t.mtu)
                             bulk_load(st + mt * kSfTileBytes,
-                                      gd->sfa_atoms + ((size_t)(t.mt0 + mt) * katoms + (size_t)kt * 4) * kSfAtomBytes,
+                                      gd->sfa_atoms + ((size_t)(t.mt0 + mt) * katoms + (size_t)ks * 4) * kSfAtomBytes,
                                       kSfTileBytes, fb, pol);
                     for (int b = 0; b < nblk; ++b)
                         bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
-                                  gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)kt * 4) * kSfAtomBytes,
+                                  gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
                                   kSfTileBytes, fb, pol);
                 }
                 issued_mask |= 1u << r.stage;
@@ -497,8 +552,9 @@ struct Roles {
             sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
             const int s0 = (t.n0 % 128) / 32;
             for (int kt = 0; kt < p.k_tiles; ++kt) {
+                const int sub = kt % C::kKS;  // k tile within the scale stage
                 if (!warp_wait_done(seq - NT, kSiteSfFree) ||
-                    !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull)) {
+                    (sub == 0 && !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull))) {
                     ok = false;
                     break;
                 }
@@ -507,13 +563,17 @@ struct Roles {
                 const uint8_t *sb = sa + C::kSfaBytes;
                 uint32_t va[32], vb[32];
                 if (RAW) {
-                    // raw tiles: row r's 16 bytes at 16r, word kk = the 64-k slice kk
+                    // raw rows: row r's scales at r * kSfRow, this k tile's 16 bytes
+                    // at 16 * sub; word kk = the 64-k slice kk. Rows past M_g hold
+                    // stale bytes; their accumulator rows are never stored.
+                    const uint8_t *ra = sa + 16 * sub;
+                    const uint8_t *rb = sb + 16 * sub;
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const uint4 w = (mt < t.mtu) ? *reinterpret_cast<const uint4 *>(
-                                                               sa + mt * kSfTileBytes + 16 * (32 * c + lane))
+                                                               ra + mt * C::kSfaTile + C::kSfRow * (32 * c + lane))
                                                          : make_uint4(0u, 0u, 0u, 0u);
                             va[16 * mt + 0 + c] = w.x;
                             va[16 * mt + 4 + c] = w.y;
@@ -523,8 +583,9 @@ struct Roles {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         // rows past the widest tile lie outside this stage's scale region
-                        const uint4 w = (32 * c < MAXN) ? *reinterpret_cast<const uint4 *>(sb + 16 * (32 * c + lane))
-                                                        : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 w = (32 * c < MAXN)
+                                            ? *reinterpret_cast<const uint4 *>(rb + C::kSfRow * (32 * c + lane))
+                                            : make_uint4(0u, 0u, 0u, 0u);
                         vb[0 + c] = w.x;
                         vb[8 + c] = w.y;
                         vb[16 + c] = w.z;
@@ -544,22 +605,16 @@ struct Roles {
                             va[16 * mt + 4 * kk + 2] = w.z;
                             va[16 * mt + 4 * kk + 3] = w.w;
                         }
-                    // tile column 32c + i is row n0 + 32c + i: block (s0 + c) / 4, word (s0 + c) % 4
+                    // tile column 32c + i is row n0 + 32c + i: atom group (s0 + c) / 4,
+                    // word (s0 + c) % 4 of that group's row i
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        uint4 src[3];
+                    for (int c = 0; c < 8; ++c) {
+                        const int idx = s0 + c;
+                        const bool in = (idx >> 2) < nblk;
+                        const uint8_t *src = sb + (idx >> 2) * kSfTileBytes + 16 * lane + 4 * (idx & 3);
 #pragma unroll
-                        for (int b = 0; b < 3; ++b)
-                            src[b] = (b < nblk) ? *reinterpret_cast<const uint4 *>(sb + b * kSfTileBytes +
-                                                                                     kk * kSfAtomBytes + 16 * lane)
-                                                : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int idx = s0 + c;
-                            const int blk = idx >> 2;
-                            const uint4 v = blk == 0 ? src[0] : (blk == 1 ? src[1] : src[2]);
-                            vb[8 * kk + c] = word_at(v, idx & 3);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            vb[8 * kk + c] = in ? *reinterpret_cast<const uint32_t *>(src + kk * kSfAtomBytes) : 0u;
                     }
                 }
                 const uint32_t col = (uint32_t)(C::kSfBase + rt.stage * kSfCols);
@@ -569,11 +624,12 @@ struct Roles {
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
+                const bool stage_done = (sub == C::kKS - 1) || (kt == p.k_tiles - 1);
                 if (lane == 0) {
-                    mbar_arrive(s_empty(rs.stage));
+                    if (stage_done) mbar_arrive(s_empty(rs.stage));
                     mbar_arrive(sf_ready(rt.stage));
                 }
-                rs.advance<NS>();
+                if (stage_done) rs.advance<NS>();
                 rt.advance<NT>();
             }
         }
@@ -633,7 +689,8 @@ struct Roles {
     // --------------------------------------------------------------- epilogue
     __device__ void epilogue(uint32_t tmem, int warp, int lane)
     {
-        const int q = warp & 3;  // the TMEM lane quarter this warp may read
+        const int q = warp & 3;                    // the TMEM lane quarter this warp may read
+        const int h = warp >= kWarpEpi1 ? 1 : 0;   // which half of the 32-column blocks
         RingPos racc;
         Walker wk(p);
         Unit t;
@@ -641,31 +698,34 @@ struct Roles {
             const GroupDesc *gd = p.groups + t.g;
             if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
             tc_fence_after_sync();
-            // columns [n0, n0 + 32 * nblk) hold live data; two tcgen05.ld in
-            // flight: block c + 1 is read while block c is converted and stored
+            // columns [n0, n0 + 32 * nblk) hold live data; this warp takes blocks
+            // h, h + 2, ... with two tcgen05.ld in flight: the next block is read
+            // while the current one is converted and stored
             const int nblk = (min(t.ncols, p.N - t.n0) + 31) / 32;
+            const int mine = (nblk - h + 1) / 2;
+            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (p.N % 16 == 0);
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
-                if (mt >= t.mtu || row0 >= gd->M) continue;
+                if (mt >= t.mtu || row0 >= gd->M || mine <= 0) continue;
                 const int row = row0 + lane;
                 const bool live = row < gd->M;
                 uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)p.N;
-                const uint32_t tbase =
-                    tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN);
+                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
+                                       (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(tbase, v0);
 #pragma unroll 1
-                for (int c = 0; c < nblk; c += 2) {
+                for (int j = 0; j < mine; j += 2) {
                     tmem_ld_wait();
                     pin_registers(v0);
-                    if (c + 1 < nblk) tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (c + 1)), v1);
-                    if (live) store_row_block(crow, t.n0 + 32 * c, p.N, v0);
-                    if (c + 1 < nblk) {
+                    if (j + 1 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 1)), v1);
+                    if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), p.N, v0, wide_st);
+                    if (j + 1 < mine) {
                         tmem_ld_wait();
                         pin_registers(v1);
-                        if (c + 2 < nblk) tmem_ld_32x32b_x32(tbase + (uint32_t)(32 * (c + 2)), v0);
-                        if (live) store_row_block(crow, t.n0 + 32 * (c + 1), p.N, v1);
+                        if (j + 2 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 2)), v0);
+                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j + 2), p.N, v1, wide_st);
                     }
                 }
             }
@@ -705,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         if (lane == 0) r.s_producer();
     } else if (warp == kWarpMma) {
         if (lane == 0) r.mma_issuer(tmem);
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
+    } else if ((warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) || warp >= kWarpEpi1) {
         r.epilogue(tmem, warp, lane);
     } else if (warp >= kWarpSf0 && warp < kWarpSf0 + kNumSfWarps) {
         r.sf_writer(tmem, warp, lane);
@@ -783,8 +843,8 @@ constexpr VariantEntry make_entry(bool is_default)
 
 // (MAXN, B stages, A stages, scale stages, raw scales)
 const VariantEntry kVariants[] = {
-    make_entry<256, 4, 2, 4, true>(true),  make_entry<256, 4, 2, 3, false>(true),
-    make_entry<256, 3, 3, 4, true>(false), make_entry<128, 8, 2, 4, true>(true),
+    make_entry<256, 4, 2, 2, true>(true),  make_entry<256, 4, 2, 3, false>(true),
+    make_entry<256, 3, 3, 2, true>(false), make_entry<128, 8, 2, 2, true>(true),
     make_entry<128, 8, 2, 3, false>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);

@@ -189,10 +189,12 @@ NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
  * of 128-row tiles; each pair owns ceil(N/32) consecutive 32-column chunks,
  * numbered group by group. CTA c of the persistent grid takes chunks
  * [cta_begin[c], cta_begin[c+1]). tile_n (0 = 256) and the kernel width it
- * selects cap the tiles as in nvfp4_ggemm_options_t. When every pair can be
- * covered by such tiles with at most max_ctas CTAs, each CTA gets one tile
- * inside one pair and the tiles are sized to even out the columns per CTA;
- * otherwise the chunks are cut into equal contiguous ranges. cta_begin must
+ * selects cap the tiles as in nvfp4_ggemm_options_t; the kernel cuts a range
+ * into the fewest tiles within the cap, of equal width to within one chunk.
+ * When there are no more pairs than max_ctas, every range lies inside one
+ * pair: the split uses the fewest tiles per CTA (passes over K) that fit
+ * max_ctas CTAs, and spare CTAs then shorten the longest ranges. Otherwise
+ * the chunks are cut into equal contiguous ranges. cta_begin must
  * hold max_ctas + 1 entries (max_ctas 1..1024); *grid receives the CTA
  * count (0 when every M_g is 0). This is not an operation of the pages; it
  * exposes the scheduling step for inspection and testing.

@@ -3,10 +3,10 @@
 Every group's pairs of 128-row tiles own ceil(N/32) consecutive chunks of 32
 columns; CTA c takes chunks [cta_begin[c], cta_begin[c+1]). These tests
 check the split against properties fixed by that definition: the ranges
-partition the chunks; when the grid holds one tile per CTA, each range lies
-in one pair and is no wider than that pair's cap (192 columns for two row
-tiles, tile_n for one), and no narrower cap would have fitted the grid;
-otherwise the ranges are equal to within one chunk."""
+partition the chunks; when there are no more pairs than CTAs, each range
+lies in one pair and the most tiles any CTA needs (a tile is at most 192
+columns for two row tiles, tile_n for one) is the fewest with which the
+pairs fit the grid; otherwise the ranges are equal to within one chunk."""
 import random
 
 import pytest
@@ -38,16 +38,11 @@ def caps(tile_n):
     return single, pair
 
 
-def fewest_ctas(M, N, tile_n, width=None):
+def ctas_needed(M, N, tile_n, passes):
+    """CTAs needed when each takes at most `passes` tiles inside one pair."""
     single, pair = caps(tile_n)
     n = -(-N // 32)
-    total = 0
-    for rows in pairs_of(M):
-        cap = pair if rows == 2 else single
-        if width is not None:
-            cap = min(cap, width)
-        total += -(-n // cap)
-    return total
+    return sum(-(-n // (passes * (pair if rows == 2 else single))) for rows in pairs_of(M))
 
 
 def check(M, N, tile_n, max_ctas):
@@ -64,17 +59,15 @@ def check(M, N, tile_n, max_ctas):
     assert cb[0] == 0 and cb[-1] == total
     assert all(b > a for a, b in zip(cb, cb[1:])), "every CTA gets at least one chunk"
     single, pair = caps(tile_n)
-    if fewest_ctas(M, N, tile_n) <= max_ctas:
-        widest = 0
+    if len(segs) <= max_ctas:
+        fewest = next(P for P in range(1, 10 ** 6) if ctas_needed(M, N, tile_n, P) <= max_ctas)
+        most = 0
         for a, b in zip(cb, cb[1:]):
             s = a // n
             assert (b - 1) // n == s, f"range [{a},{b}) crosses a pair boundary"
             cap = pair if segs[s] == 2 else single
-            assert b - a <= cap
-            widest = max(widest, b - a)
-        # no narrower widest tile would have fitted the grid
-        if widest > 1:
-            assert fewest_ctas(M, N, tile_n, widest - 1) > max_ctas
+            most = max(most, -(-(b - a) // cap))
+        assert most == fewest, (most, fewest)
     else:
         sizes = [b - a for a, b in zip(cb, cb[1:])]
         assert grid == min(total, max_ctas)
@@ -91,10 +84,18 @@ def test_page_shape_gets_one_tile_per_cta():
     assert max(widths) == 8  # 128 chunks over 17 CTAs per one-tile group
 
 
-def test_skinny_wide_shape_falls_back_to_equal_ranges():
+def test_skinny_wide_shape_takes_two_passes_per_cta():
     M = [40, 76, 168, 72, 164, 148, 196, 160]
     cb = check(M, 7168, 0, 152)
     assert len(cb) - 1 == 152
+    widths = [b - a for a, b in zip(cb, cb[1:])]
+    assert max(widths) <= 12  # two tiles of at most 6 chunks in the two-row-tile pairs
+
+
+def test_more_pairs_than_ctas_uses_equal_ranges():
+    M = [256] * 40
+    cb = check(M, 1024, 0, 16)
+    assert len(cb) - 1 == 16
 
 
 @pytest.mark.parametrize("tile_n", [0, 256, 224, 192, 128, 96, 32])
