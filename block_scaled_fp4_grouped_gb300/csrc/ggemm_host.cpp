@@ -169,6 +169,22 @@ int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, i
     return c;
 }
 
+void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
+                     const int32_t *m_tiles, int G)
+{
+    int g = 0;
+    for (int c = 0; c < grid; ++c) {
+        CtaRange &r = ranges[c];
+        r = CtaRange{};
+        r.begin = cta_begin[c];
+        r.end = cta_begin[c + 1];
+        while (g + 1 < G && chunk_prefix[g + 1] <= r.begin) ++g;  // ranges ascend, so g only moves forward
+        r.g = g;
+        r.g_base = chunk_prefix[g];
+        r.g_tiles = m_tiles[g];
+    }
+}
+
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
                      const void *SFB, void *C, bool sf_raw, int wide_rows)
 {
@@ -295,7 +311,8 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     int njobs = 0, items = 0;
     const int pieces = K / 256;
     for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
-    std::memcpy(tab + p->off_cta, p->cta_begin.data(), sizeof(int32_t) * p->cta_begin.size());
+    fill_cta_ranges(reinterpret_cast<CtaRange *>(tab + p->off_cta), p->cta_begin.data(), p->grid,
+                    p->chunk_prefix.data(), p->m_tiles.data(), p->G);
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
         d.M = p->M[g];
@@ -404,7 +421,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
-    gp.cta_begin = reinterpret_cast<const int32_t *>(s.d_table + p->off_cta);
+    gp.ctas = reinterpret_cast<const CtaRange *>(s.d_table + p->off_cta);
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
@@ -549,7 +566,7 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
     p->off_cta = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
-    p->off_jobs = align_up(p->off_cta + sizeof(int32_t) * (size_t)(p->grid + 1), 64);
+    p->off_jobs = align_up(p->off_cta + sizeof(CtaRange) * (size_t)std::max(p->grid, 1), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
     bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&

@@ -68,7 +68,7 @@ static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-
 struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
-    const int32_t *cta_begin;      // [grid+1]
+    const struct CtaRange *ctas;   // [grid]
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
@@ -80,6 +80,21 @@ struct GemmParams {
     int32_t wide_rows;             // rows of the wide B boxes (the kernel's widest tile)
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
 };
+
+// CTA c's chunk range and the group it starts in, so that a CTA finds its
+// first tile with one 32-byte load.
+struct alignas(32) CtaRange {
+    int32_t begin, end;   // chunks [begin, end)
+    int32_t g;            // group holding chunk `begin`
+    int32_t g_base;       // chunk_prefix[g]
+    int32_t g_tiles;      // m_tiles of group g
+    int32_t pad[3];
+};
+static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
+
+// Fills ranges[0..grid) from cta_begin[0..grid] and the group layout.
+void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
+                     const int32_t *m_tiles, int G);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {

@@ -35,6 +35,8 @@
 // records (status, site, block) in the error word, raises a CTA-wide abort
 // flag and leaves its loop; all warps then drain their own asynchronous
 // work, TMEM is released and the kernel returns normally.
+#include <cstddef>
+
 #include <cuda_fp16.h>
 
 #include "ggemm_internal.h"
@@ -112,10 +114,11 @@ struct Cfg {
 
 struct Unit {
     int g;
-    int mt0;    // first 128-row tile of the unit
-    int mtu;    // row tiles in the unit (1 or 2)
-    int n0;     // first column
-    int ncols;  // tile width: a multiple of 32
+    int mt0;     // first 128-row tile of the unit
+    int mtu;     // row tiles in the unit (1 or 2)
+    int n0;      // first column
+    int ncols;   // tile width: a multiple of 32
+    bool keep;   // the group has more pairs of row tiles, which read B again
 };
 
 // Walks this CTA's contiguous range of chunks as tiles.
@@ -123,32 +126,35 @@ struct Walker {
     int pos, end;
     // the part of the range inside the current pair: [pb, pb + plen) cut
     // into pt tiles of equal width (to within one chunk); pi = next tile
-    int pb = 0, plen = 0, pt = 0, pi = 0;
-    int g = 0, mt0 = 0, mtu = 0, ch0 = 0;
+    int plen = 0, pt = 0, pi = 0;
+    int g, g_base, g_tiles, mt0 = 0, mtu = 0, ch0 = 0;
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
-        pos = __ldg(p.cta_begin + blockIdx.x);
-        end = __ldg(p.cta_begin + blockIdx.x + 1);
+        const int4 *rec = reinterpret_cast<const int4 *>(p.ctas + blockIdx.x);
+        const int4 r0 = __ldg(rec), r1 = __ldg(rec + 1);
+        pos = r0.x;
+        end = r0.y;
+        g = r0.z;
+        g_base = r0.w;
+        g_tiles = r1.x;
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
     {
         if (pi == pt) {
             if (pos >= end) return false;
-            int lo = 0, hi = p.G;  // prefix[lo] <= pos < prefix[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (__ldg(p.chunk_prefix + mid) <= pos) lo = mid;
-                else hi = mid;
+            // groups past the one holding `pos` (only ranges that span groups get here)
+            while (pos >= g_base + ((g_tiles + 1) >> 1) * p.n_chunks) {
+                ++g;
+                g_base = __ldg(p.chunk_prefix + g);
+                g_tiles = p.groups[g].m_tiles;
             }
-            const int local = pos - __ldg(p.chunk_prefix + lo);
+            const int local = pos - g_base;
             const int mp = local / p.n_chunks;
             ch0 = local - mp * p.n_chunks;
-            g = lo;
             mt0 = mp * kRowTilesPerUnit;
-            mtu = min(kRowTilesPerUnit, p.groups[lo].m_tiles - mt0);
-            pb = pos;
+            mtu = min(kRowTilesPerUnit, g_tiles - mt0);
             plen = min(p.n_chunks - ch0, end - pos);
             const int cap = mtu == 2 ? p.cap_pair : p.cap_single;
             pt = (plen + cap - 1) / cap;
@@ -163,6 +169,7 @@ struct Walker {
         t.mtu = mtu;
         t.n0 = (ch0 + c0) * kChunkN;
         t.ncols = (c1 - c0) * kChunkN;
+        t.keep = g_tiles > kRowTilesPerUnit;
         return true;
     }
 };
@@ -303,6 +310,9 @@ __device__ __forceinline__ int row_boxes(const Unit &t, int M, int (&live)[kRowT
     return total;
 }
 
+static_assert(offsetof(GroupDesc, tmSFBw) == offsetof(GroupDesc, tmA) + 5 * sizeof(CUtensorMap),
+              "the six tensor maps are consecutive");
+
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Roles {
     using C = Cfg<MAXN, NB, NA, NS, RAW>;
@@ -382,7 +392,7 @@ struct Roles {
                 fence_tensormap_acquire(&gd->tmBw);
                 last_g = t.g;
             }
-            const uint64_t pol = gd->b_keep ? pol_keep : pol_stream;
+            const uint64_t pol = t.keep ? pol_keep : pol_stream;
             const bool wide = (t.ncols == p.wide_rows);
             const int boxes = t.ncols / 32;
             const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
@@ -748,6 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) r.init_barriers();
+    if (warp == kWarpEpi0 && lane < 6) {
+        // start fetching the tensor maps of this CTA's first group while the
+        // barriers and TMEM are set up
+        const int g = __ldg(&p.ctas[blockIdx.x].g);
+        const GroupDesc *gd = p.groups + g;
+        // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
+        if (RAW || lane < 3) prefetch_tensormap(&gd->tmA + lane);
+    }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
         tmem_relinquish();
