@@ -15,7 +15,7 @@ constexpr int kMmaK = 64;          // k per tcgen05.mma of kind::mxf4nvf4
 constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k in the atom layout
 constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
-constexpr int kMaxCtas = 1024;     // largest persistent grid the schedule describes
+constexpr int kMaxCtas = 192;      // largest persistent grid (the CTA ranges travel in the kernel parameters)
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
 constexpr int kBoxRows = 32;       // rows of the A and scale TMA boxes (partial row tiles load only live boxes)
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
@@ -34,6 +34,7 @@ enum WaitSite : uint32_t {
     kSiteLoadDrain = 10, // a producer waiting for its own loads at exit
     kSiteSEmpty = 11,    // scale producer waiting for a free scale stage
     kSiteSFull = 12,     // scale writers waiting for a scale stage
+    kSiteTileCheck = 13, // a tile larger than the CTA's ring slots (never expected)
 };
 
 // One entry of the device-resident problem table. Every tensor map
@@ -59,6 +60,19 @@ struct alignas(128) GroupDesc {
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
+// CTA c's chunk range and the group it starts in, so that a CTA finds its
+// first tile with one 32-byte load.
+struct alignas(32) CtaRange {
+    int32_t begin, end;   // chunks [begin, end)
+    int32_t g;            // group holding chunk `begin`
+    int32_t g_base;       // chunk_prefix[g]
+    int32_t g_tiles;      // m_tiles of group g
+    int32_t max_chunks;   // widest tile the CTA will walk (sizes its B ring slots)
+    int32_t max_rows;     // most row tiles in one of its tiles (sizes its A ring slots)
+    int32_t pad;
+};
+static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
+
 // Work decomposition: group g owns m_pairs_g * ceil(N/32) chunks (32 columns
 // of one pair of 128-row tiles), numbered after the chunks of groups 0..g-1
 // (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N/32) chunks.
@@ -68,7 +82,7 @@ static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-
 struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
-    const struct CtaRange *ctas;   // [grid]
+    CtaRange ctas[kMaxCtas];       // [grid]: read from the parameter bank, no memory round trip
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
@@ -81,20 +95,10 @@ struct GemmParams {
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
 };
 
-// CTA c's chunk range and the group it starts in, so that a CTA finds its
-// first tile with one 32-byte load.
-struct alignas(32) CtaRange {
-    int32_t begin, end;   // chunks [begin, end)
-    int32_t g;            // group holding chunk `begin`
-    int32_t g_base;       // chunk_prefix[g]
-    int32_t g_tiles;      // m_tiles of group g
-    int32_t pad[3];
-};
-static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
-
-// Fills ranges[0..grid) from cta_begin[0..grid] and the group layout.
+// Fills ranges[0..grid) from cta_begin[0..grid] and the group layout, walking
+// each range exactly as the kernel does to bound its tiles.
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const int32_t *m_tiles, int G);
+                     const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {

@@ -63,6 +63,7 @@ constexpr int kSfTileBytes = 4 * kSfAtomBytes;       // 2048: scales of 128 rows
 constexpr int kBRowBoxBytes = 32 * (kTileK / 2);     // 4096: one 32-row B box
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStatusTimeout = 6;  // NVFP4_ERR_TIMEOUT
+constexpr uint32_t kStatusFault = 7;    // NVFP4_ERR_DEVICE_FAULT
 constexpr int kSfCols = 32 + 32;        // TMEM scale columns per stage: SFA 2 tiles x 4 x 4, SFB 4 x 8
 
 constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
@@ -72,7 +73,10 @@ constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 // its "slot free" signal from it: the slot that stage s reuses in a ring of
 // depth D was last read by stage s - D. A ring is at most kDoneRing deep, so
 // a producer waiting for stage s - D can never see that barrier two phases on.
-constexpr int kDoneRing = 8;
+// The A and B rings are fixed byte regions; each CTA cuts them into as many
+// slots (up to kDoneRing) as its widest tile allows, so narrow tiles keep
+// more stages in flight.
+constexpr int kDoneRing = 16;
 
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Cfg {
@@ -101,12 +105,14 @@ struct Cfg {
     static constexpr int kNT0 = ((int)kTmemCols - kSfBase) / kSfCols;
     static constexpr int kNT = kNT0 > 6 ? 6 : kNT0;  // TMEM scale buffers
     static constexpr int kOffBars = kOffSRing + NS * kSStage;
-    static constexpr int kNumBars = NB + NA + 2 * NS + kNT + kDoneRing + 2 + 2 + 1;
+    static constexpr int kBRing = NB * kBStage;  // bytes
+    static constexpr int kARing = NA * kAStage;
+    static constexpr int kNumBars = kDoneRing + kDoneRing + 2 * NS + kNT + kDoneRing + 2 + 2 + 1 + 1;
     static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
     static_assert(kNT >= 2, "at least two TMEM scale buffers");
-    static_assert(NB <= kDoneRing && NA <= kDoneRing && kNT <= kDoneRing, "rings no deeper than the done ring");
+    static_assert(NB >= 2 && NA >= 2 && kNT <= kDoneRing, "ring depths");
     static_assert(kSfBase + kNT * kSfCols <= (int)kTmemCols, "TMEM budget");
     static_assert(kBStage % 1024 == 0 && kAStage % 1024 == 0, "stages keep 1024-byte swizzle alignment");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -131,13 +137,12 @@ struct Walker {
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
-        const int4 *rec = reinterpret_cast<const int4 *>(p.ctas + blockIdx.x);
-        const int4 r0 = __ldg(rec), r1 = __ldg(rec + 1);
-        pos = r0.x;
-        end = r0.y;
-        g = r0.z;
-        g_base = r0.w;
-        g_tiles = r1.x;
+        const CtaRange &r = p.ctas[blockIdx.x];
+        pos = r.begin;
+        end = r.end;
+        g = r.g;
+        g_base = r.g_base;
+        g_tiles = r.g_tiles;
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
@@ -286,6 +291,13 @@ struct RingPos {
             phase ^= 1u;
         }
     }
+    __device__ __forceinline__ void advance(int n)
+    {
+        if (++stage == n) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
 };
 
 // First and count of the 128-row scale blocks that cover columns [n0, n0+ncols) of N.
@@ -322,23 +334,48 @@ struct Roles {
     uint32_t sbase;
     volatile int *abort_flag;
     const GemmParams &p;
+    int max_chunks, max_rows;  // bound on this CTA's tiles
+    int nb, na;                // slots of the B and A rings for this CTA
+    uint32_t b_slot, a_slot;   // their sizes in bytes
 
     __device__ Roles(uint8_t *s, const GemmParams &params)
         : smem(s), sbase(smem_addr(s)), abort_flag(reinterpret_cast<volatile int *>(s + C::kOffAbort)), p(params)
     {
+        const CtaRange &r = p.ctas[blockIdx.x];
+        max_chunks = min(max(r.max_chunks, 1), MAXN / kChunkN);
+        max_rows = min(max(r.max_rows, 1), kRowTilesPerUnit);
+        b_slot = (uint32_t)max_chunks * kBRowBoxBytes;
+        a_slot = (uint32_t)max_rows * kATileBytes;
+        nb = min(kDoneRing, C::kBRing / (int)b_slot);
+        na = min(kDoneRing, C::kARing / (int)a_slot);
     }
 
-    static constexpr int kBarDone = NB + NA + 2 * NS + NT;
+    // A tile wider or taller than the slots this CTA cut its rings into
+    // (the host bounds both; this only guards the shared-memory writes).
+    __device__ __forceinline__ bool tile_fits(const Unit &t) const
+    {
+        if (t.ncols <= max_chunks * kChunkN && t.mtu <= max_rows) return true;
+        record_error(p.err, kStatusFault, kSiteTileCheck);
+        *abort_flag = 1;
+        return false;
+    }
+
+    static constexpr int kBarDone = 2 * kDoneRing + 2 * NS + NT;
     __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBars + 8 * i; }
     __device__ __forceinline__ uint32_t b_full(int s) const { return bar(s); }
-    __device__ __forceinline__ uint32_t a_full(int s) const { return bar(NB + s); }
-    __device__ __forceinline__ uint32_t s_full(int s) const { return bar(NB + NA + s); }
-    __device__ __forceinline__ uint32_t s_empty(int s) const { return bar(NB + NA + NS + s); }
-    __device__ __forceinline__ uint32_t sf_ready(int b) const { return bar(NB + NA + 2 * NS + b); }
+    __device__ __forceinline__ uint32_t a_full(int s) const { return bar(kDoneRing + s); }
+    __device__ __forceinline__ uint32_t s_full(int s) const { return bar(2 * kDoneRing + s); }
+    __device__ __forceinline__ uint32_t s_empty(int s) const { return bar(2 * kDoneRing + NS + s); }
+    __device__ __forceinline__ uint32_t sf_ready(int b) const { return bar(2 * kDoneRing + 2 * NS + b); }
     __device__ __forceinline__ uint32_t done(int d) const { return bar(kBarDone + d); }
     __device__ __forceinline__ uint32_t acc_full(int a) const { return bar(kBarDone + kDoneRing + a); }
     __device__ __forceinline__ uint32_t acc_empty(int a) const { return bar(kBarDone + kDoneRing + 2 + a); }
     __device__ __forceinline__ uint32_t drain() const { return bar(kBarDone + kDoneRing + 4); }
+    // The A and scale producers arrive once their first stage is issued (or
+    // when they have none); the B producer waits for it before its first
+    // load, so the small, scattered A and scale reads of the first stage do
+    // not queue behind every CTA's burst of B stages at kernel start.
+    __device__ __forceinline__ uint32_t first_issued() const { return bar(kBarDone + kDoneRing + 5); }
 
     // Wait until the MMAs of stage j (< 0: none) have completed.
     __device__ __forceinline__ bool wait_done(int j, uint32_t site) const
@@ -351,14 +388,16 @@ struct Roles {
         if (j < 0) return true;
         return warp_wait_phase(done(j % kDoneRing), (uint32_t)(j / kDoneRing) & 1u, abort_flag, p, site);
     }
-    __device__ __forceinline__ uint32_t b_stage(int s) const { return sbase + C::kOffBRing + s * C::kBStage; }
-    __device__ __forceinline__ uint32_t a_stage(int s) const { return sbase + C::kOffARing + s * C::kAStage; }
+    __device__ __forceinline__ uint32_t b_stage(int s) const { return sbase + C::kOffBRing + (uint32_t)s * b_slot; }
+    __device__ __forceinline__ uint32_t a_stage(int s) const { return sbase + C::kOffARing + (uint32_t)s * a_slot; }
     __device__ __forceinline__ uint32_t s_stage(int s) const { return sbase + C::kOffSRing + s * C::kSStage; }
 
     __device__ void init_barriers()
     {
-        for (int s = 0; s < NB; ++s) mbar_init(b_full(s), 1);
-        for (int s = 0; s < NA; ++s) mbar_init(a_full(s), 1);
+        for (int s = 0; s < kDoneRing; ++s) {
+            mbar_init(b_full(s), 1);
+            mbar_init(a_full(s), 1);
+        }
         for (int d = 0; d < kDoneRing; ++d) mbar_init(done(d), 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(s_full(s), 1);
@@ -370,6 +409,7 @@ struct Roles {
             mbar_init(acc_empty(a), kNumEpiWarps);
         }
         mbar_init(drain(), 1);
+        mbar_init(first_issued(), 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -382,10 +422,14 @@ struct Roles {
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = -1, loads = 0, seq = 0;
-        bool ok = true;
+        bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
+            if (!tile_fits(t)) {
+                ok = false;
+                break;
+            }
             const GroupDesc *gd = p.groups + t.g;
             if (t.g != last_g) {
                 fence_tensormap_acquire(&gd->tmB32);
@@ -397,7 +441,7 @@ struct Roles {
             const int boxes = t.ncols / 32;
             const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_done(seq - NB, kSiteBEmpty)) {
+                if (!wait_done(seq - nb, kSiteBEmpty)) {
                     ok = false;
                     break;
                 }
@@ -420,10 +464,10 @@ struct Roles {
                 } else {
                     issued_mask &= ~(1u << r.stage);  // nothing in flight for this stage
                 }
-                r.advance<NB>();
+                r.advance(nb);
             }
         }
-        for (int s = 0; s < NB; ++s)
+        for (int s = 0; s < nb; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(b_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
 
@@ -434,10 +478,15 @@ struct Roles {
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = -1, seq = 0;
+        bool signalled = false;
         bool ok = true;
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
+            if (!tile_fits(t)) {
+                ok = false;
+                break;
+            }
             const GroupDesc *gd = p.groups + t.g;
             if (t.g != last_g) {
                 fence_tensormap_acquire(&gd->tmA);
@@ -446,7 +495,7 @@ struct Roles {
             int live_boxes[kRowTilesPerUnit];
             const int boxes = row_boxes(t, gd->M, live_boxes);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_done(seq - NA, kSiteAEmpty)) {
+                if (!wait_done(seq - na, kSiteAEmpty)) {
                     ok = false;
                     break;
                 }
@@ -460,12 +509,17 @@ struct Roles {
                     for (int b = 0; b < live_boxes[mt]; ++b)
                         tma_load_2d(a_stage(r.stage) + mt * kATileBytes + b * (kBoxRows * (kTileK / 2)), &gd->tmA,
                                     kt * (kTileK / 2), (t.mt0 + mt) * kTileM + b * kBoxRows, fb, pol);
+                if (!signalled) {
+                    mbar_arrive(first_issued());
+                    signalled = true;
+                }
                 issued_mask |= 1u << r.stage;
                 issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
-                r.advance<NA>();
+                r.advance(na);
             }
         }
-        for (int s = 0; s < NA; ++s)
+        if (!signalled) mbar_arrive(first_issued());
+        for (int s = 0; s < na; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(a_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
 
@@ -476,6 +530,7 @@ struct Roles {
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = -1;
+        bool signalled = false;
         bool ok = true;
         const size_t katoms = (size_t)(p.K / 64);
         const int s_tiles = (p.k_tiles + C::kKS - 1) / C::kKS;  // scale stages per tile
@@ -533,11 +588,16 @@ struct Roles {
                                   gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
                                   kSfTileBytes, fb, pol);
                 }
+                if (!signalled) {
+                    mbar_arrive(first_issued());
+                    signalled = true;
+                }
                 issued_mask |= 1u << r.stage;
                 issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
                 r.advance<NS>();
             }
         }
+        if (!signalled) mbar_arrive(first_issued());
         for (int s = 0; s < NS; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
@@ -683,8 +743,8 @@ struct Roles {
                 // the stages and the scale buffer are free once these MMAs have read them
                 tc_commit(done(seq % kDoneRing));
                 ++seq;
-                ra.advance<NA>();
-                rb.advance<NB>();
+                ra.advance(na);
+                rb.advance(nb);
                 rt.advance<NT>();
             }
             if (!ok) break;
@@ -761,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     if (warp == kWarpEpi0 && lane < 6) {
         // start fetching the tensor maps of this CTA's first group while the
         // barriers and TMEM are set up
-        const int g = __ldg(&p.ctas[blockIdx.x].g);
+        const int g = p.ctas[blockIdx.x].g;
         const GroupDesc *gd = p.groups + g;
         // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
         if (RAW || lane < 3) prefetch_tensormap(&gd->tmA + lane);

@@ -22,16 +22,13 @@ namespace {
 constexpr int kNoAllocMaxGroups = 64;
 constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 56 KB
 constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
-constexpr size_t kCtaOffset = kPrefixOffset + 512;                              // CtaRange[grid]
-constexpr size_t kCtaBytes = 7168;
-constexpr int kNoAllocMaxCtas = (int)(kCtaBytes / sizeof(CtaRange));             // 224
-constexpr size_t kErrOffset = kCtaOffset + kCtaBytes;                           // uint32 error word
+constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
 constexpr size_t kScratchBytes = kErrOffset + 256;
 static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
-static_assert(kNoAllocMaxCtas >= 152, "CTA range area holds one range per SM of the largest part");
 static_assert(kScratchBytes <= 64 * 1024, "the array stays within 64 KB");
 
-// The scratch: problem table, chunk prefix sums, per-CTA chunk ranges, error word. In host code this
+// The scratch: problem table, chunk prefix sums, error word (the per-CTA
+// chunk ranges travel in the kernel parameters). In host code this
 // name is only a host-side stand-in; the device address comes from
 // cudaGetSymbolAddress, once per device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
@@ -136,13 +133,11 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int cap_single = kMaxTileN / kChunkN;
     const int cap_pair = pair_cap_chunks(kMaxTileN);
-    int32_t cta_begin[kNoAllocMaxCtas + 1];
+    int32_t cta_begin[kMaxCtas + 1];
     int32_t counts[kMaxCtas];
     const int grid = schedule_ctas(m_tiles, num_groups, n_chunks, cap_single, cap_pair,
-                                   std::min(g_sm_count[dev], kNoAllocMaxCtas), cta_begin, counts);
+                                   std::min(g_sm_count[dev], kMaxCtas), cta_begin, counts);
     if (grid < 1) return NVFP4_OK;
-    CtaRange ranges[kNoAllocMaxCtas];
-    fill_cta_ranges(ranges, cta_begin, grid, prefix, m_tiles, num_groups);
 
     // --- upload (pageable source: the call returns once the bytes are staged,
     //     so the stack buffer may go away), clear the error word, launch
@@ -151,8 +146,6 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     if (cudaMemcpyAsync(scratch, table, used, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(scratch + kPrefixOffset, prefix, sizeof(int32_t) * (size_t)(num_groups + 1),
                         cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(scratch + kCtaOffset, ranges, sizeof(CtaRange) * (size_t)grid, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
         cudaMemsetAsync(scratch + kErrOffset, 0, sizeof(uint32_t), s) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
@@ -160,7 +153,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
-    gp.ctas = reinterpret_cast<const CtaRange *>(scratch + kCtaOffset);
+    fill_cta_ranges(gp.ctas, cta_begin, grid, prefix, m_tiles, num_groups, n_chunks, cap_single, cap_pair);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;

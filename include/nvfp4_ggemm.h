@@ -195,7 +195,7 @@ NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
  * pair: the split uses the fewest tiles per CTA (passes over K) that fit
  * max_ctas CTAs, and spare CTAs then shorten the longest ranges. Otherwise
  * the chunks are cut into equal contiguous ranges. cta_begin must
- * hold max_ctas + 1 entries (max_ctas 1..1024); *grid receives the CTA
+ * hold max_ctas + 1 entries (max_ctas 1..192); *grid receives the CTA
  * count (0 when every M_g is 0). This is not an operation of the pages; it
  * exposes the scheduling step for inspection and testing.
  */
