@@ -170,7 +170,7 @@ int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, i
 }
 
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair)
+                     const int32_t *m_tiles, const int32_t *M, int G, int n_chunks, int cap_single, int cap_pair)
 {
     int g = 0;
     for (int c = 0; c < grid; ++c) {
@@ -182,6 +182,7 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
         r.g = g;
         r.g_base = chunk_prefix[g];
         r.g_tiles = m_tiles[g];
+        r.g_rows = M[g];
         // the kernel's walk: the part of the range in each pair is cut into
         // ceil(len / cap) tiles of equal width (to within one chunk)
         int pos = r.begin, wg = g;
@@ -251,7 +252,8 @@ struct nvfp4_ggemm_plan_s {
     int cap_single = 8, cap_pair = 6;
     int k_tiles = 0;
     std::vector<int32_t> m_tiles, m_pairs, chunk_prefix, cta_begin;
-    size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
+    std::vector<CtaRange> ctas;
+    size_t off_prefix = 0, off_cta = 0, off_jobs = 0, table_bytes = 0;
     Slot slots[kSlots];
     int cur = -1;
     uint32_t *d_err = nullptr;
@@ -329,6 +331,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     int njobs = 0, items = 0;
     const int pieces = K / 256;
     for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
+    std::memcpy(tab + p->off_cta, p->ctas.data(), sizeof(CtaRange) * p->ctas.size());
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
         d.M = p->M[g];
@@ -437,8 +440,8 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
-    fill_cta_ranges(gp.ctas, p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->m_tiles.data(), p->G,
-                    p->n_chunks, p->cap_single, p->cap_pair);
+    gp.ctas = reinterpret_cast<const CtaRange *>(s.d_table + p->off_cta);
+    for (int c = 0; c < p->grid; ++c) gp.cta_group[c] = (uint16_t)p->ctas[c].g;
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
@@ -582,7 +585,11 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     p->cta_begin.resize(p->grid + 1);
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
-    p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
+    p->ctas.assign(std::max(p->grid, 1), CtaRange{});
+    fill_cta_ranges(p->ctas.data(), p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->m_tiles.data(),
+                    p->M.data(), num_groups, p->n_chunks, p->cap_single, p->cap_pair);
+    p->off_cta = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
+    p->off_jobs = align_up(p->off_cta + sizeof(CtaRange) * p->ctas.size(), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
     bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&

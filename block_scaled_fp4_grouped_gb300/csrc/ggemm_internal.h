@@ -15,7 +15,7 @@ constexpr int kMmaK = 64;          // k per tcgen05.mma of kind::mxf4nvf4
 constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k in the atom layout
 constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
-constexpr int kMaxCtas = 192;      // largest persistent grid (the CTA ranges travel in the kernel parameters)
+constexpr int kMaxCtas = 192;      // largest persistent grid (each CTA's first group travels in the kernel parameters)
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
 constexpr int kBoxRows = 32;       // rows of the A and scale TMA boxes (partial row tiles load only live boxes)
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
@@ -61,7 +61,9 @@ struct alignas(128) GroupDesc {
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
 // CTA c's chunk range and the group it starts in, so that a CTA finds its
-// first tile with one 32-byte load.
+// first tile with one 32-byte load, issued while its barriers and TMEM are
+// set up and the tensor maps of that group (named in the kernel parameters)
+// are being prefetched.
 struct alignas(32) CtaRange {
     int32_t begin, end;   // chunks [begin, end)
     int32_t g;            // group holding chunk `begin`
@@ -69,7 +71,7 @@ struct alignas(32) CtaRange {
     int32_t g_tiles;      // m_tiles of group g
     int32_t max_chunks;   // widest tile the CTA will walk (sizes its B ring slots)
     int32_t max_rows;     // most row tiles in one of its tiles (sizes its A ring slots)
-    int32_t pad;
+    int32_t g_rows;       // M of group g
 };
 static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 
@@ -82,7 +84,8 @@ static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
-    CtaRange ctas[kMaxCtas];       // [grid]: read from the parameter bank, no memory round trip
+    const CtaRange *ctas;          // [grid]
+    uint16_t cta_group[kMaxCtas];  // ctas[c].g, in the parameter bank
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
@@ -98,7 +101,7 @@ struct GemmParams {
 // Fills ranges[0..grid) from cta_begin[0..grid] and the group layout, walking
 // each range exactly as the kernel does to bound its tiles.
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair);
+                     const int32_t *m_tiles, const int32_t *M, int G, int n_chunks, int cap_single, int cap_pair);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {

@@ -108,7 +108,8 @@ struct Cfg {
     static constexpr int kBRing = NB * kBStage;  // bytes
     static constexpr int kARing = NA * kAStage;
     static constexpr int kNumBars = kDoneRing + kDoneRing + 2 * NS + kNT + kDoneRing + 2 + 2 + 1 + 1;
-    static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
+    static constexpr int kOffRecord = (kOffBars + 8 * kNumBars + 31) / 32 * 32;
+    static constexpr int kOffTmemSlot = kOffRecord + (int)sizeof(CtaRange);
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
     static_assert(kNT >= 2, "at least two TMEM scale buffers");
@@ -125,6 +126,7 @@ struct Unit {
     int n0;      // first column
     int ncols;   // tile width: a multiple of 32
     bool keep;   // the group has more pairs of row tiles, which read B again
+    int M;       // rows of the group
 };
 
 // Walks this CTA's contiguous range of chunks as tiles.
@@ -133,16 +135,16 @@ struct Walker {
     // the part of the range inside the current pair: [pb, pb + plen) cut
     // into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
-    int g, g_base, g_tiles, mt0 = 0, mtu = 0, ch0 = 0;
+    int g, g_base, g_tiles, g_rows, mt0 = 0, mtu = 0, ch0 = 0;
 
-    __device__ __forceinline__ explicit Walker(const GemmParams &p)
+    __device__ __forceinline__ explicit Walker(const CtaRange &r)
     {
-        const CtaRange &r = p.ctas[blockIdx.x];
         pos = r.begin;
         end = r.end;
         g = r.g;
         g_base = r.g_base;
         g_tiles = r.g_tiles;
+        g_rows = r.g_rows;
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
@@ -154,6 +156,7 @@ struct Walker {
                 ++g;
                 g_base = __ldg(p.chunk_prefix + g);
                 g_tiles = p.groups[g].m_tiles;
+                g_rows = p.groups[g].M;
             }
             const int local = pos - g_base;
             const int mp = local / p.n_chunks;
@@ -175,6 +178,7 @@ struct Walker {
         t.n0 = (ch0 + c0) * kChunkN;
         t.ncols = (c1 - c0) * kChunkN;
         t.keep = g_tiles > kRowTilesPerUnit;
+        t.M = g_rows;
         return true;
     }
 };
@@ -341,7 +345,18 @@ struct Roles {
     __device__ Roles(uint8_t *s, const GemmParams &params)
         : smem(s), sbase(smem_addr(s)), abort_flag(reinterpret_cast<volatile int *>(s + C::kOffAbort)), p(params)
     {
-        const CtaRange &r = p.ctas[blockIdx.x];
+    }
+
+    // This CTA's range record, copied to shared memory at kernel start.
+    __device__ __forceinline__ const CtaRange &rec() const
+    {
+        return *reinterpret_cast<const CtaRange *>(smem + C::kOffRecord);
+    }
+
+    // After the record has landed in shared memory: size the ring slots.
+    __device__ void size_rings()
+    {
+        const CtaRange &r = rec();
         max_chunks = min(max(r.max_chunks, 1), MAXN / kChunkN);
         max_rows = min(max(r.max_rows, 1), kRowTilesPerUnit);
         b_slot = (uint32_t)max_chunks * kBRowBoxBytes;
@@ -423,7 +438,7 @@ struct Roles {
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = -1, loads = 0, seq = 0;
         bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!tile_fits(t)) {
@@ -480,7 +495,7 @@ struct Roles {
         int last_g = -1, seq = 0;
         bool signalled = false;
         bool ok = true;
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!tile_fits(t)) {
@@ -493,7 +508,7 @@ struct Roles {
                 last_g = t.g;
             }
             int live_boxes[kRowTilesPerUnit];
-            const int boxes = row_boxes(t, gd->M, live_boxes);
+            const int boxes = row_boxes(t, t.M, live_boxes);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!wait_done(seq - na, kSiteAEmpty)) {
                     ok = false;
@@ -534,7 +549,7 @@ struct Roles {
         bool ok = true;
         const size_t katoms = (size_t)(p.K / 64);
         const int s_tiles = (p.k_tiles + C::kKS - 1) / C::kKS;  // scale stages per tile
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (ok && wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
@@ -549,7 +564,7 @@ struct Roles {
             int b0 = 0, nblk = 0;
             sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
             int live_boxes[kRowTilesPerUnit];
-            const int aboxes = row_boxes(t, gd->M, live_boxes);
+            const int aboxes = row_boxes(t, t.M, live_boxes);
             const uint32_t bytes =
                 RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
                     : (uint32_t)t.mtu * kSfTileBytes + (uint32_t)nblk * kSfTileBytes;
@@ -615,7 +630,7 @@ struct Roles {
         RingPos rs, rt;
         int seq = 0;
         bool ok = true;
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (ok && wk.next(p, t)) {
             int b0 = 0, nblk = 0;
@@ -712,7 +727,7 @@ struct Roles {
         RingPos ra, rb, rt, racc;
         int seq = 0;
         bool ok = true;
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!wait_phase(acc_empty(racc.stage), racc.phase ^ 1u, abort_flag, p, kSiteAccEmpty)) break;
@@ -762,7 +777,7 @@ struct Roles {
         const int q = warp & 3;                    // the TMEM lane quarter this warp may read
         const int h = warp >= kWarpEpi1 ? 1 : 0;   // which half of the 32-column blocks
         RingPos racc;
-        Walker wk(p);
+        Walker wk(rec());
         Unit t;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
@@ -777,9 +792,9 @@ struct Roles {
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
-                if (mt >= t.mtu || row0 >= gd->M || mine <= 0) continue;
+                if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
                 const int row = row0 + lane;
-                const bool live = row < gd->M;
+                const bool live = row < t.M;
                 uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)p.N;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN + 32 * h);
@@ -821,10 +836,15 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     if (warp == kWarpEpi0 && lane < 6) {
         // start fetching the tensor maps of this CTA's first group while the
         // barriers and TMEM are set up
-        const int g = p.ctas[blockIdx.x].g;
+        const int g = p.cta_group[blockIdx.x];
         const GroupDesc *gd = p.groups + g;
         // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
         if (RAW || lane < 3) prefetch_tensormap(&gd->tmA + lane);
+    }
+    if (warp == kWarpEpi0 + 1 && lane < (int)(sizeof(CtaRange) / 4)) {
+        // this CTA's range record, for every role after the barrier below
+        reinterpret_cast<int32_t *>(smem + C::kOffRecord)[lane] =
+            __ldg(reinterpret_cast<const int32_t *>(p.ctas + blockIdx.x) + lane);
     }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
@@ -834,6 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
+    r.size_rings();
 
     if (warp == kWarpBProducer) {
         if (lane == 0) r.b_producer();
@@ -921,8 +942,8 @@ constexpr VariantEntry make_entry(bool is_default)
 
 // (MAXN, B stages, A stages, scale stages, raw scales)
 const VariantEntry kVariants[] = {
-    make_entry<256, 4, 2, 2, true>(true),  make_entry<256, 4, 2, 3, false>(true),
-    make_entry<256, 3, 3, 2, true>(false), make_entry<128, 8, 2, 2, true>(true),
+    make_entry<256, 3, 3, 2, true>(true),  make_entry<256, 3, 3, 3, false>(true),
+    make_entry<256, 4, 2, 2, true>(false), make_entry<128, 8, 2, 2, true>(true),
     make_entry<128, 8, 2, 3, false>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);

@@ -102,9 +102,12 @@ typedef struct {
                                  timeout (exercises the error path) */
     int32_t b_stages;         /* shared-memory stages of the B ring; 0 (with a_stages 0) = the
                                  default for the tile width and scale path. Kernels exist for
-                                 (tile width, b_stages, a_stages) = (256,4,2) (default),
-                                 (256,3,3) and (128,8,2) (default) with raw scales, and the
-                                 defaults (256,4,2), (128,8,2) with atom-layout scales */
+                                 (tile width, b_stages, a_stages) = (256,3,3) (default),
+                                 (256,4,2) and (128,8,2) (default) with raw scales, and the
+                                 defaults (256,3,3), (128,8,2) with atom-layout scales. The
+                                 stage counts size the A and B regions for the widest tile;
+                                 each CTA cuts them into more slots when its tiles are
+                                 narrower or have one row tile */
     int32_t a_stages;         /* shared-memory stages of the A ring (see b_stages) */
     int32_t reserved[3];
 } nvfp4_ggemm_options_t;
