@@ -204,6 +204,19 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
     }
 }
 
+void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks)
+{
+    for (int c = 0; c < grid; ++c) {
+        const CtaRange &r = ranges[c];
+        out[c].begin = r.begin;
+        out[c].g_base = r.g_base;
+        out[c].g_rows = r.g_rows;
+        out[c].packed = (uint32_t)(r.g & 0xFFFF) | ((uint32_t)(r.max_chunks & 0xFF) << 16) |
+                        ((uint32_t)(r.max_rows & 0xFF) << 24);
+    }
+    out[grid] = CtaStart{total_chunks, 0, 0, 0};
+}
+
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
                      const void *SFB, void *C, bool sf_raw, int wide_rows)
 {
@@ -253,7 +266,7 @@ struct nvfp4_ggemm_plan_s {
     int k_tiles = 0;
     std::vector<int32_t> m_tiles, m_pairs, chunk_prefix, cta_begin;
     std::vector<CtaRange> ctas;
-    size_t off_prefix = 0, off_cta = 0, off_jobs = 0, table_bytes = 0;
+    size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
     Slot slots[kSlots];
     int cur = -1;
     uint32_t *d_err = nullptr;
@@ -331,7 +344,6 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     int njobs = 0, items = 0;
     const int pieces = K / 256;
     for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
-    std::memcpy(tab + p->off_cta, p->ctas.data(), sizeof(CtaRange) * p->ctas.size());
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
         d.M = p->M[g];
@@ -440,8 +452,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
-    gp.ctas = reinterpret_cast<const CtaRange *>(s.d_table + p->off_cta);
-    for (int c = 0; c < p->grid; ++c) gp.cta_group[c] = (uint16_t)p->ctas[c].g;
+    pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks);
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
@@ -588,8 +599,7 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     p->ctas.assign(std::max(p->grid, 1), CtaRange{});
     fill_cta_ranges(p->ctas.data(), p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->m_tiles.data(),
                     p->M.data(), num_groups, p->n_chunks, p->cap_single, p->cap_pair);
-    p->off_cta = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
-    p->off_jobs = align_up(p->off_cta + sizeof(CtaRange) * p->ctas.size(), 64);
+    p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
     bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&

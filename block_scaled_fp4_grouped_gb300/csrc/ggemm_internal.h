@@ -15,7 +15,7 @@ constexpr int kMmaK = 64;          // k per tcgen05.mma of kind::mxf4nvf4
 constexpr int kSfAtomBytes = 512;  // scales of 128 rows x 64 k in the atom layout
 constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
-constexpr int kMaxCtas = 192;      // largest persistent grid (each CTA's first group travels in the kernel parameters)
+constexpr int kMaxCtas = 192;      // largest persistent grid (the CTA start records travel in the kernel parameters)
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
 constexpr int kBoxRows = 32;       // rows of the A and scale TMA boxes (partial row tiles load only live boxes)
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
@@ -60,10 +60,7 @@ struct alignas(128) GroupDesc {
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
-// CTA c's chunk range and the group it starts in, so that a CTA finds its
-// first tile with one 32-byte load, issued while its barriers and TMEM are
-// set up and the tensor maps of that group (named in the kernel parameters)
-// are being prefetched.
+// CTA c's chunk range and the group it starts in (host side).
 struct alignas(32) CtaRange {
     int32_t begin, end;   // chunks [begin, end)
     int32_t g;            // group holding chunk `begin`
@@ -75,6 +72,17 @@ struct alignas(32) CtaRange {
 };
 static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 
+// What a CTA needs to start, packed into 16 bytes of the kernel parameters
+// so that no role reads memory before its first load. CTA c's range ends
+// where CTA c + 1's begins (a sentinel follows the last CTA).
+struct CtaStart {
+    int32_t begin;    // first chunk
+    int32_t g_base;   // chunk_prefix[g]
+    int32_t g_rows;   // M of group g
+    uint32_t packed;  // g (bits 0-15) | widest tile in chunks (16-23) | most row tiles (24-31)
+};
+static_assert(sizeof(CtaStart) == 16, "packed start record");
+
 // Work decomposition: group g owns m_pairs_g * ceil(N/32) chunks (32 columns
 // of one pair of 128-row tiles), numbered after the chunks of groups 0..g-1
 // (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N/32) chunks.
@@ -84,8 +92,7 @@ static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
-    const CtaRange *ctas;          // [grid]
-    uint16_t cta_group[kMaxCtas];  // ctas[c].g, in the parameter bank
+    CtaStart cta[kMaxCtas + 1];    // [grid + 1]
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G, N, K;
@@ -99,9 +106,11 @@ struct GemmParams {
 };
 
 // Fills ranges[0..grid) from cta_begin[0..grid] and the group layout, walking
-// each range exactly as the kernel does to bound its tiles.
+// each range exactly as the kernel does to bound its tiles; pack_cta_starts
+// turns them into the kernel's start records (grid + 1 entries).
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
                      const int32_t *m_tiles, const int32_t *M, int G, int n_chunks, int cap_single, int cap_pair);
+void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {

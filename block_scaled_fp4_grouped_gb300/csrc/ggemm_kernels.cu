@@ -108,8 +108,7 @@ struct Cfg {
     static constexpr int kBRing = NB * kBStage;  // bytes
     static constexpr int kARing = NA * kAStage;
     static constexpr int kNumBars = kDoneRing + kDoneRing + 2 * NS + kNT + kDoneRing + 2 + 2 + 1 + 1;
-    static constexpr int kOffRecord = (kOffBars + 8 * kNumBars + 31) / 32 * 32;
-    static constexpr int kOffTmemSlot = kOffRecord + (int)sizeof(CtaRange);
+    static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
     static_assert(kNT >= 2, "at least two TMEM scale buffers");
@@ -137,14 +136,15 @@ struct Walker {
     int plen = 0, pt = 0, pi = 0;
     int g, g_base, g_tiles, g_rows, mt0 = 0, mtu = 0, ch0 = 0;
 
-    __device__ __forceinline__ explicit Walker(const CtaRange &r)
+    __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
+        const CtaStart &r = p.cta[blockIdx.x];
         pos = r.begin;
-        end = r.end;
-        g = r.g;
+        end = p.cta[blockIdx.x + 1].begin;
+        g = (int)(r.packed & 0xFFFFu);
         g_base = r.g_base;
-        g_tiles = r.g_tiles;
         g_rows = r.g_rows;
+        g_tiles = (g_rows + kTileM - 1) / kTileM;
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Unit &t)
@@ -345,20 +345,15 @@ struct Roles {
     __device__ Roles(uint8_t *s, const GemmParams &params)
         : smem(s), sbase(smem_addr(s)), abort_flag(reinterpret_cast<volatile int *>(s + C::kOffAbort)), p(params)
     {
+        size_rings();
     }
 
-    // This CTA's range record, copied to shared memory at kernel start.
-    __device__ __forceinline__ const CtaRange &rec() const
-    {
-        return *reinterpret_cast<const CtaRange *>(smem + C::kOffRecord);
-    }
-
-    // After the record has landed in shared memory: size the ring slots.
+    // Size the ring slots from this CTA's widest tile and most row tiles.
     __device__ void size_rings()
     {
-        const CtaRange &r = rec();
-        max_chunks = min(max(r.max_chunks, 1), MAXN / kChunkN);
-        max_rows = min(max(r.max_rows, 1), kRowTilesPerUnit);
+        const uint32_t packed = p.cta[blockIdx.x].packed;
+        max_chunks = min(max((int)((packed >> 16) & 0xFFu), 1), MAXN / kChunkN);
+        max_rows = min(max((int)(packed >> 24), 1), kRowTilesPerUnit);
         b_slot = (uint32_t)max_chunks * kBRowBoxBytes;
         a_slot = (uint32_t)max_rows * kATileBytes;
         nb = min(kDoneRing, C::kBRing / (int)b_slot);
@@ -438,7 +433,7 @@ struct Roles {
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = -1, loads = 0, seq = 0;
         bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!tile_fits(t)) {
@@ -495,7 +490,7 @@ struct Roles {
         int last_g = -1, seq = 0;
         bool signalled = false;
         bool ok = true;
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!tile_fits(t)) {
@@ -549,7 +544,7 @@ struct Roles {
         bool ok = true;
         const size_t katoms = (size_t)(p.K / 64);
         const int s_tiles = (p.k_tiles + C::kKS - 1) / C::kKS;  // scale stages per tile
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
@@ -630,7 +625,7 @@ struct Roles {
         RingPos rs, rt;
         int seq = 0;
         bool ok = true;
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
             int b0 = 0, nblk = 0;
@@ -727,7 +722,7 @@ struct Roles {
         RingPos ra, rb, rt, racc;
         int seq = 0;
         bool ok = true;
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
             if (!wait_phase(acc_empty(racc.stage), racc.phase ^ 1u, abort_flag, p, kSiteAccEmpty)) break;
@@ -777,7 +772,7 @@ struct Roles {
         const int q = warp & 3;                    // the TMEM lane quarter this warp may read
         const int h = warp >= kWarpEpi1 ? 1 : 0;   // which half of the 32-column blocks
         RingPos racc;
-        Walker wk(rec());
+        Walker wk(p);
         Unit t;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
@@ -836,15 +831,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     if (warp == kWarpEpi0 && lane < 6) {
         // start fetching the tensor maps of this CTA's first group while the
         // barriers and TMEM are set up
-        const int g = p.cta_group[blockIdx.x];
+        const int g = (int)(p.cta[blockIdx.x].packed & 0xFFFFu);
         const GroupDesc *gd = p.groups + g;
         // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
         if (RAW || lane < 3) prefetch_tensormap(&gd->tmA + lane);
-    }
-    if (warp == kWarpEpi0 + 1 && lane < (int)(sizeof(CtaRange) / 4)) {
-        // this CTA's range record, for every role after the barrier below
-        reinterpret_cast<int32_t *>(smem + C::kOffRecord)[lane] =
-            __ldg(reinterpret_cast<const int32_t *>(p.ctas + blockIdx.x) + lane);
     }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
@@ -854,7 +844,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
-    r.size_rings();
 
     if (warp == kWarpBProducer) {
         if (lane == 0) r.b_producer();

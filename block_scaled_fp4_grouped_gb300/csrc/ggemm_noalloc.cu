@@ -22,13 +22,13 @@ namespace {
 constexpr int kNoAllocMaxGroups = 64;
 constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 56 KB
 constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
-constexpr size_t kCtaOffset = kPrefixOffset + 512;                              // CtaRange[grid]
-constexpr size_t kErrOffset = kCtaOffset + sizeof(CtaRange) * kMaxCtas;         // uint32 error word
+constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
 constexpr size_t kScratchBytes = kErrOffset + 256;
 static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
 static_assert(kScratchBytes <= 64 * 1024, "the array stays within 64 KB");
 
-// The scratch: problem table, chunk prefix sums, per-CTA chunk ranges, error word. In host code this
+// The scratch: problem table, chunk prefix sums, error word (the CTA start
+// records travel in the kernel parameters). In host code this
 // name is only a host-side stand-in; the device address comes from
 // cudaGetSymbolAddress, once per device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
@@ -148,8 +148,6 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     if (cudaMemcpyAsync(scratch, table, used, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(scratch + kPrefixOffset, prefix, sizeof(int32_t) * (size_t)(num_groups + 1),
                         cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(scratch + kCtaOffset, ranges, sizeof(CtaRange) * (size_t)grid, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
         cudaMemsetAsync(scratch + kErrOffset, 0, sizeof(uint32_t), s) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
@@ -157,8 +155,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
-    gp.ctas = reinterpret_cast<const CtaRange *>(scratch + kCtaOffset);
-    for (int c = 0; c < grid; ++c) gp.cta_group[c] = (uint16_t)ranges[c].g;
+    pack_cta_starts(gp.cta, ranges, grid, (int)total);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
