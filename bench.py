@@ -253,26 +253,45 @@ def time_e2e(prob, kw, steps, warmup, torch, nb):
 
 def oracle_sample_time(prob, budget_s: float):
     """Time the oracle (as it stands) on a bounded sample of `prob`: whole
-    groups while they fit the budget, else a row subset of one group.
-    Returns (µs per full call extrapolated by flops, threads, sample text)."""
+    groups while they fit the budget, else a row subset of the largest
+    group. Returns (µs per full call extrapolated by flops, threads, sample
+    text)."""
     import oracle as oracle_pkg
     O = oracle_pkg.get()
     threads = os.cpu_count() or 1
     total_flops = synth.algorithmic_flops(prob.M, prob.N, prob.K)
-    g = int(np.argmax(prob.M))
-    rows = prob.M[g]
-    # probe with 8 rows to size the sample
+    g0 = int(np.argmax(prob.M))
+    # size the sample from 4 rows per thread of the largest group (after a warm-up call)
+    probe = max(1, min(prob.M[g0], 4 * threads))
+    O.group_gemm(prob.A[g0][:4], prob.B[g0], prob.SFA[g0][:4], prob.SFB[g0], prob.K, nthreads=threads)
     t0 = time.perf_counter()
-    O.group_gemm(prob.A[g][:8], prob.B[g], prob.SFA[g][:8], prob.SFB[g], prob.K, nthreads=threads)
-    probe = time.perf_counter() - t0
-    per_row = max(probe / 8, 1e-6)
-    take = int(max(8, min(rows, budget_s / per_row)))
-    t0 = time.perf_counter()
-    O.group_gemm(prob.A[g][:take], prob.B[g], prob.SFA[g][:take], prob.SFB[g], prob.K, nthreads=threads)
-    dt = time.perf_counter() - t0
-    sample_flops = 2 * take * prob.N * prob.K
+    O.group_gemm(prob.A[g0][:probe], prob.B[g0], prob.SFA[g0][:probe], prob.SFB[g0], prob.K, nthreads=threads)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
+    groups, est = [], 0.0
+    for g, m in enumerate(prob.M):
+        if m > 0 and est + m * per_row <= budget_s:
+            groups.append(g)
+            est += m * per_row
+    if groups:
+        t0 = time.perf_counter()
+        for g in groups:
+            O.group_gemm(prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], prob.K, nthreads=threads)
+        dt = time.perf_counter() - t0
+        rows = sum(prob.M[g] for g in groups)
+        sample_flops = 2 * rows * prob.N * prob.K
+        what = (f"{len(groups)} of {sum(1 for m in prob.M if m > 0)} groups ({rows} of {sum(prob.M)} rows) "
+                f"x N={prob.N} x K={prob.K} ({dt:.2f} s)")
+    else:
+        take = int(max(8, min(prob.M[g0], budget_s / per_row)))
+        t0 = time.perf_counter()
+        O.group_gemm(prob.A[g0][:take], prob.B[g0], prob.SFA[g0][:take], prob.SFB[g0], prob.K, nthreads=threads)
+        dt = time.perf_counter() - t0
+        sample_flops = 2 * take * prob.N * prob.K
+        what = f"group {g0}: {take} of {prob.M[g0]} rows x N={prob.N} x K={prob.K} ({dt:.2f} s)"
     us_full = dt * 1e6 * total_flops / sample_flops
-    return us_full, threads, f"group {g}: {take} of {rows} rows x N={prob.N} x K={prob.K} ({dt:.2f} s), scaled by flops"
+    if sample_flops < total_flops:
+        what += ", scaled by flops"
+    return us_full, threads, what
 
 
 def run_reference(args, world, rank):

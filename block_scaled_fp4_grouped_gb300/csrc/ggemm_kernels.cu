@@ -260,8 +260,11 @@ __device__ __forceinline__ void pin_registers(uint32_t (&v)[32])
 // RN to fp16 and stores of 32 accumulator columns of one C row, starting at
 // column col0 (a multiple of 32); columns >= N are not written. wide: the row
 // is 32-byte aligned and N % 16 == 0, so two 32-byte stores cover the block;
-// otherwise four 16-byte stores (N % 8 == 0).
-__device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N, const uint32_t (&v)[32], bool wide)
+// otherwise four 16-byte stores (N % 8 == 0). The stores carry an L2
+// evict-first policy: C is written once and never read here, so its lines
+// should be the first to leave L2 rather than lines other work still holds.
+__device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N, const uint32_t (&v)[32], bool wide,
+                                                uint64_t pol)
 {
     uint32_t h[16];
 #pragma unroll
@@ -270,16 +273,18 @@ __device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N,
 #pragma unroll
         for (int j = 0; j < 2; ++j)
             if (col0 + 16 * j < N)
-                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(crow + col0 + 16 * j),
+                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(
+                                 crow + col0 + 16 * j),
                              "r"(h[8 * j + 0]), "r"(h[8 * j + 1]), "r"(h[8 * j + 2]), "r"(h[8 * j + 3]),
-                             "r"(h[8 * j + 4]), "r"(h[8 * j + 5]), "r"(h[8 * j + 6]), "r"(h[8 * j + 7])
+                             "r"(h[8 * j + 4]), "r"(h[8 * j + 5]), "r"(h[8 * j + 6]), "r"(h[8 * j + 7]), "l"(pol)
                              : "memory");
     } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (col0 + 8 * j < N)
-                *reinterpret_cast<uint4 *>(crow + col0 + 8 * j) =
-                    make_uint4(h[4 * j + 0], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(crow + col0 + 8 * j),
+                             "r"(h[4 * j + 0]), "r"(h[4 * j + 1]), "r"(h[4 * j + 2]), "r"(h[4 * j + 3]), "l"(pol)
+                             : "memory");
     }
 }
 
@@ -771,6 +776,7 @@ struct Roles {
     {
         const int q = warp & 3;                    // the TMEM lane quarter this warp may read
         const int h = warp >= kWarpEpi1 ? 1 : 0;   // which half of the 32-column blocks
+        const uint64_t pol_c = policy_evict_first();
         RingPos racc;
         Walker wk(p);
         Unit t;
@@ -800,12 +806,12 @@ struct Roles {
                     tmem_ld_wait();
                     pin_registers(v0);
                     if (j + 1 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 1)), v1);
-                    if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), p.N, v0, wide_st);
+                    if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), p.N, v0, wide_st, pol_c);
                     if (j + 1 < mine) {
                         tmem_ld_wait();
                         pin_registers(v1);
                         if (j + 2 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 2)), v0);
-                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j + 2), p.N, v1, wide_st);
+                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j + 2), p.N, v1, wide_st, pol_c);
                     }
                 }
             }
