@@ -48,6 +48,7 @@ EXPORTED = (
     "nvfp4_ggemm_version",
     "nvfp4_ggemm_run_noalloc",
     "nvfp4_ggemm_schedule",
+    "nvfp4_ggemm_plan_shapes",
 )
 
 
@@ -136,9 +137,13 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_int32, _VPP, _VPP, _VPP, _VPP, _VPP, _VP,
                                           ctypes.POINTER(ctypes.c_uint32)]
     L.nvfp4_ggemm_schedule.restype = ctypes.c_int
-    L.nvfp4_ggemm_schedule.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
-                                       ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
-                                       ctypes.POINTER(ctypes.c_int32)]
+    L.nvfp4_ggemm_schedule.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    L.nvfp4_ggemm_plan_shapes.restype = ctypes.c_int
+    L.nvfp4_ggemm_plan_shapes.argtypes = [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]
     _lib = L
     return L
 
@@ -191,12 +196,24 @@ def nvfp4_ggemm_default_options() -> nvfp4_ggemm_options_t:
     return opt
 
 
-def nvfp4_ggemm_plan(device: int, M: Sequence[int], N: int, K: int,
+def _i32_array(vals: Sequence[int]):
+    return (ctypes.c_int32 * max(1, len(vals)))(*[int(v) for v in vals])
+
+
+def nvfp4_ggemm_plan(device: int, M: Sequence[int], N, K,
                      opt: Optional[nvfp4_ggemm_options_t] = None) -> Tuple[int, Optional[int]]:
+    """N and K: one value for every group (nvfp4_ggemm_plan) or one per group
+    (nvfp4_ggemm_plan_shapes)."""
     handle = _VP()
-    m = (ctypes.c_int32 * max(1, len(M)))(*[int(v) for v in M])
-    st = lib().nvfp4_ggemm_plan(ctypes.byref(handle), int(device), len(M), m, int(N), int(K),
-                                ctypes.byref(opt) if opt is not None else None)
+    m = _i32_array(M)
+    o = ctypes.byref(opt) if opt is not None else None
+    if isinstance(N, (list, tuple)) or isinstance(K, (list, tuple)):
+        Ns = list(N) if isinstance(N, (list, tuple)) else [int(N)] * len(M)
+        Ks = list(K) if isinstance(K, (list, tuple)) else [int(K)] * len(M)
+        st = lib().nvfp4_ggemm_plan_shapes(ctypes.byref(handle), int(device), len(M), m, _i32_array(Ns),
+                                           _i32_array(Ks), o)
+    else:
+        st = lib().nvfp4_ggemm_plan(ctypes.byref(handle), int(device), len(M), m, int(N), int(K), o)
     return st, (handle.value if st == NVFP4_OK else None)
 
 
@@ -264,13 +281,15 @@ def nvfp4_ggemm_run_noalloc(M: Sequence[int], N: int, K: int, A, B, SFA, SFB, C,
     return st, int(word.value)
 
 
-def nvfp4_ggemm_schedule(M: Sequence[int], N: int, tile_n: int = 0, max_ctas: int = 148) -> Tuple[int, List[int]]:
-    """Per-CTA chunk ranges a plan would use (host only). Returns
-    (status, cta_begin[0..grid])."""
-    m = (ctypes.c_int32 * max(1, len(M)))(*[int(v) for v in M])
+def nvfp4_ggemm_schedule(M: Sequence[int], N, tile_n: int = 0, max_ctas: int = 148, K=256) -> Tuple[int, List[int]]:
+    """Per-CTA chunk ranges a plan would use (host only). N and K: one value
+    for every group or one per group. Returns (status, cta_begin[0..grid])."""
+    Ns = list(N) if isinstance(N, (list, tuple)) else [int(N)] * len(M)
+    Ks = list(K) if isinstance(K, (list, tuple)) else [int(K)] * len(M)
     out = (ctypes.c_int32 * (max(1, int(max_ctas)) + 1))()
     grid = ctypes.c_int32(0)
-    st = lib().nvfp4_ggemm_schedule(len(M), m, int(N), int(tile_n), int(max_ctas), out, ctypes.byref(grid))
+    st = lib().nvfp4_ggemm_schedule(len(M), _i32_array(M), _i32_array(Ns), _i32_array(Ks), int(tile_n),
+                                    int(max_ctas), out, ctypes.byref(grid))
     if st != NVFP4_OK:
         return st, []
     return st, [int(out[i]) for i in range(grid.value + 1)] if grid.value > 0 else [0]
@@ -302,7 +321,10 @@ class GroupedGemm:
     codes (raw [rows, K/16] or atom layout), C[g] float16 [M_g, N]."""
 
     def __init__(self, M: Sequence[int], N: int, K: int, device: int = 0, **options):
-        self.M, self.N, self.K = [int(m) for m in M], int(N), int(K)
+        self.M = [int(m) for m in M]
+        # N and K: one value for every group, or one per group
+        self.N = [int(n) for n in N] if isinstance(N, (list, tuple)) else int(N)
+        self.K = [int(k) for k in K] if isinstance(K, (list, tuple)) else int(K)
         self.opt = make_options(**options)
         st, handle = nvfp4_ggemm_plan(device, self.M, self.N, self.K, self.opt)
         if st != NVFP4_OK:

@@ -62,6 +62,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Per-group N and K limits: 16-byte C rows, whole 256-k pipeline stages.
+inline bool shape_ok(int32_t N, int32_t K)
+{
+    return N >= 8 && N <= kMaxN && N % 8 == 0 && K >= 256 && K <= kMaxK && K % 256 == 0;
+}
+
 uint64_t atom_bytes(int64_t rows, int64_t K)
 {
     return (uint64_t)((rows + 127) / 128) * (uint64_t)(K / 64) * (uint64_t)kSfAtomBytes;
@@ -103,57 +109,71 @@ TensorMapEncodeFn tensor_map_encoder()
 
 int pair_cap_chunks(int max_n) { return (max_n >= 192 ? 192 : max_n) / kChunkN; }
 
-int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair, int max_ctas,
-                  int32_t *cta_begin, int32_t *counts)
+int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int32_t *cta_begin,
+                  int32_t *counts)
 {
     max_ctas = std::max(1, std::min(max_ctas, kMaxCtas));
     // segments: pairs of row tiles; the last pair of a group with an odd tile count has one
-    long seg1 = 0, seg2 = 0;
+    long nseg = 0, total = 0;
     for (int g = 0; g < G; ++g) {
-        seg2 += m_tiles[g] / 2;
-        seg1 += m_tiles[g] % 2;
+        const long pairs = (shapes[g].m_tiles + 1) / 2;
+        nseg += pairs;
+        total += pairs * shapes[g].n_chunks;
     }
-    const long nseg = seg1 + seg2;
-    const long total = nseg * (long)n_chunks;
     if (total == 0) {
         cta_begin[0] = 0;
         return 0;
     }
-    // CTAs a segment needs when a CTA may take `passes` tiles of at most cap chunks
-    auto ctas_for = [&](int cap, long passes) { return (n_chunks + passes * cap - 1) / (passes * cap); };
-    auto need = [&](long passes) { return seg1 * ctas_for(cap_single, passes) + seg2 * ctas_for(cap_pair, passes); };
-    // the fewest passes per CTA with every CTA's range inside one segment
-    long P = 1;
-    if (nseg <= max_ctas)
-        while (need(P) > max_ctas) ++P;  // ends by P = n_chunks, where need(P) = nseg
     if (nseg > max_ctas) {
         // more segments than CTAs: equal contiguous chunk ranges
         const int grid = (int)std::min<long>(total, max_ctas);
         for (int c = 0; c <= grid; ++c) cta_begin[c] = (int32_t)((long)c * total / grid);
         return grid;
     }
+    auto seg_cap = [&](int g, int t) { return (shapes[g].m_tiles - t) >= 2 ? cap_pair : cap_single; };
+    // CTAs a segment needs when a CTA may spend `budget` k-stages on it (at least one pass)
+    auto ctas_for = [&](int g, int t, long budget) {
+        const long passes = std::max<long>(1, budget / shapes[g].k_tiles);
+        const long per_cta = passes * seg_cap(g, t);
+        return (shapes[g].n_chunks + per_cta - 1) / per_cta;
+    };
+    auto need = [&](long budget) {
+        long n = 0;
+        for (int g = 0; g < G; ++g)
+            for (int t = 0; t < shapes[g].m_tiles; t += 2) n += ctas_for(g, t, budget);
+        return n;
+    };
+    // the smallest budget that fits (need() does not grow with the budget; a
+    // budget of max(k) * max(n) gives one CTA per segment)
+    long hi = 1;
+    for (int g = 0; g < G; ++g) hi = std::max<long>(hi, (long)shapes[g].k_tiles * shapes[g].n_chunks);
+    long lo = 1;
+    while (lo < hi) {
+        const long mid = lo + (hi - lo) / 2;
+        if (need(mid) <= max_ctas) hi = mid;
+        else lo = mid + 1;
+    }
     int grid = 0;
     {
         long s = 0;
         for (int g = 0; g < G; ++g)
-            for (int t = 0; t < m_tiles[g]; t += 2, ++s)
-                counts[s] = (int32_t)ctas_for((m_tiles[g] - t) >= 2 ? cap_pair : cap_single, P);
+            for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) counts[s] = (int32_t)ctas_for(g, t, lo);
         for (long i = 0; i < nseg; ++i) grid += counts[i];
     }
-    // spare CTAs shorten the longest ranges, measured in passes, then in chunks
+    // spare CTAs shorten the longest ranges, measured in k-stages, then in chunks
     for (; grid < max_ctas; ++grid) {
-        long best = -1;
-        long best_pass = 0, best_len = 0;
+        long best = -1, best_stages = 0, best_len = 0;
         long s = 0;
         for (int g = 0; g < G; ++g)
-            for (int t = 0; t < m_tiles[g]; t += 2, ++s) {
-                if (counts[s] >= n_chunks) continue;
-                const int cap = (m_tiles[g] - t) >= 2 ? cap_pair : cap_single;
-                const long len = (n_chunks + counts[s] - 1) / counts[s];  // longest range of this segment
-                const long pass = (len + cap - 1) / cap;
-                if (best < 0 || pass > best_pass || (pass == best_pass && len > best_len)) {
+            for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) {
+                const int n = shapes[g].n_chunks;
+                if (counts[s] >= n) continue;
+                const long len = (n + counts[s] - 1) / counts[s];  // longest range of this segment
+                const long cap = seg_cap(g, t);
+                const long stages = (len + cap - 1) / cap * shapes[g].k_tiles;
+                if (best < 0 || stages > best_stages || (stages == best_stages && len > best_len)) {
                     best = s;
-                    best_pass = pass;
+                    best_stages = stages;
                     best_len = len;
                 }
             }
@@ -161,16 +181,19 @@ int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, i
         ++counts[best];
     }
     int c = 0;
-    for (long i = 0; i < nseg; ++i) {
-        const long base = i * (long)n_chunks;
-        for (int j = 0; j < counts[i]; ++j) cta_begin[c++] = (int32_t)(base + (long)j * n_chunks / counts[i]);
-    }
+    long s = 0, base = 0;
+    for (int g = 0; g < G; ++g)
+        for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) {
+            const long n = shapes[g].n_chunks;
+            for (int j = 0; j < counts[s]; ++j) cta_begin[c++] = (int32_t)(base + (long)j * n / counts[s]);
+            base += n;
+        }
     cta_begin[c] = (int32_t)total;
     return c;
 }
 
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const int32_t *m_tiles, const int32_t *M, int G, int n_chunks, int cap_single, int cap_pair)
+                     const GroupShape *shapes, int G, int cap_single, int cap_pair)
 {
     int g = 0;
     for (int c = 0; c < grid; ++c) {
@@ -181,20 +204,21 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
         while (g + 1 < G && chunk_prefix[g + 1] <= r.begin) ++g;  // ranges ascend, so g only moves forward
         r.g = g;
         r.g_base = chunk_prefix[g];
-        r.g_tiles = m_tiles[g];
-        r.g_rows = M[g];
+        r.g_tiles = shapes[g].m_tiles;
+        r.g_rows = shapes[g].M;
         // the kernel's walk: the part of the range in each pair is cut into
         // ceil(len / cap) tiles of equal width (to within one chunk)
         int pos = r.begin, wg = g;
         r.max_chunks = 1;
         r.max_rows = 1;
         while (pos < r.end) {
-            while (pos >= chunk_prefix[wg] + ((m_tiles[wg] + 1) / 2) * n_chunks) ++wg;
+            while (pos >= chunk_prefix[wg] + ((shapes[wg].m_tiles + 1) / 2) * shapes[wg].n_chunks) ++wg;
+            const int n = shapes[wg].n_chunks;
             const int local = pos - chunk_prefix[wg];
-            const int mp = local / n_chunks;
-            const int ch0 = local - mp * n_chunks;
-            const int mtu = std::min(kRowTilesPerUnit, m_tiles[wg] - mp * kRowTilesPerUnit);
-            const int plen = std::min(n_chunks - ch0, r.end - pos);
+            const int mp = local / n;
+            const int ch0 = local - mp * n;
+            const int mtu = std::min(kRowTilesPerUnit, shapes[wg].m_tiles - mp * kRowTilesPerUnit);
+            const int plen = std::min(n - ch0, r.end - pos);
             const int cap = mtu == 2 ? cap_pair : cap_single;
             const int pt = ceil_div(plen, cap);
             r.max_chunks = std::max(r.max_chunks, ceil_div(plen, pt));
@@ -204,15 +228,15 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
     }
 }
 
-void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks)
+void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes)
 {
     for (int c = 0; c < grid; ++c) {
         const CtaRange &r = ranges[c];
+        const GroupShape &sh = shapes[r.g];
         out[c].begin = r.begin;
         out[c].g_base = r.g_base;
-        out[c].g_rows = r.g_rows;
-        out[c].packed = (uint32_t)(r.g & 0xFFFF) | ((uint32_t)(r.max_chunks & 0xFF) << 16) |
-                        ((uint32_t)(r.max_rows & 0xFF) << 24);
+        out[c].rows = cta_pack_rows(sh.M, sh.k_tiles);
+        out[c].packed = cta_pack(r.g, r.max_chunks, r.max_rows, sh.n_chunks);
     }
     out[grid] = CtaStart{total_chunks, 0, 0, 0};
 }
@@ -226,6 +250,9 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
     d.m_tiles = ceil_div(M, kTileM);
     d.m_pairs = ceil_div(d.m_tiles, kRowTilesPerUnit);
     d.b_keep = d.m_pairs > 1 ? 1 : 0;
+    d.N = N;
+    d.k_tiles = K / kTileK;
+    d.n_chunks = ceil_div(N, kChunkN);
     d.C = static_cast<uint16_t *>(C);
     bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kBoxRows,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -254,17 +281,16 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
 struct nvfp4_ggemm_plan_s {
     int device = 0;
     int sm_count = 0;
-    int G = 0, N = 0, K = 0;
-    std::vector<int32_t> M;
+    int G = 0;
+    std::vector<int32_t> M, N, K;  // per group
     nvfp4_ggemm_options_t opt{};
     int variant = -1;
     GemmVariant var{};
     int grid = 0;
     int total_chunks = 0;
-    int n_chunks = 0;
     int cap_single = 8, cap_pair = 6;
-    int k_tiles = 0;
     std::vector<int32_t> m_tiles, m_pairs, chunk_prefix, cta_begin;
+    std::vector<GroupShape> shapes;
     std::vector<CtaRange> ctas;
     size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
     Slot slots[kSlots];
@@ -340,9 +366,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     auto *groups = reinterpret_cast<GroupDesc *>(tab);
     auto *prefix = reinterpret_cast<int32_t *>(tab + p->off_prefix);
     auto *jobs = reinterpret_cast<RelayoutJob *>(tab + p->off_jobs);
-    const int K = p->K, N = p->N;
     int njobs = 0, items = 0;
-    const int pieces = K / 256;
     for (int g = 0; g <= p->G; ++g) prefix[g] = p->chunk_prefix[g];
     for (int g = 0; g < p->G; ++g) {
         GroupDesc &d = groups[g];
@@ -351,12 +375,13 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         d.m_pairs = p->m_pairs[g];
         d.chunk_begin = p->chunk_prefix[g];
         if (p->M[g] == 0) continue;
+        const int N = p->N[g], K = p->K[g], pieces = K / 256;
         const void *sfa = SFA[g];
         const void *sfb = SFB ? SFB[g] : nullptr;
         if (p->relayout()) {
             sfa = p->d_ws + p->ws_sfa[g];
             sfb = p->d_ws + p->ws_sfb[g];
-            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFA[g]), p->d_ws + p->ws_sfa[g], p->M[g], items};
+            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFA[g]), p->d_ws + p->ws_sfa[g], p->M[g], K, items, 0};
             items += ceil_div(p->M[g], 128) * pieces;
             ++njobs;
         }
@@ -366,8 +391,9 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     if (p->relayout() && (force_sfb || !p->opt.cache_b_scales)) {
         for (int g = 0; g < p->G; ++g) {
             if (p->M[g] == 0) continue;
-            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], N, items};
-            items += ceil_div(N, 128) * pieces;
+            const int N = p->N[g], K = p->K[g];
+            jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], N, K, items, 0};
+            items += ceil_div(N, 128) * (K / 256);
             ++njobs;
         }
     }
@@ -378,12 +404,12 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
 
 int relayout_items(nvfp4_ggemm_plan_s *p, bool with_sfb)
 {
-    const int pieces = p->K / 256;
     int items = 0;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
+        const int pieces = p->K[g] / 256;
         items += ceil_div(p->M[g], 128) * pieces;
-        if (with_sfb) items += ceil_div(p->N, 128) * pieces;
+        if (with_sfb) items += ceil_div(p->N[g], 128) * pieces;
     }
     return items;
 }
@@ -444,7 +470,6 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         int nj = 0;
         for (int g = 0; g < p->G; ++g) nj += p->M[g] > 0 ? 1 : 0;
         rp.njobs = sfb_cached ? nj : 2 * nj;
-        rp.K = p->K;
         rp.total_items = relayout_items(p, !sfb_cached);
         if (relayout_launch(rp, p->sm_count, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     }
@@ -452,15 +477,10 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
-    pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks);
+    pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks, p->shapes.data());
     gp.err = p->d_err;
     gp.timeout_ns = p->opt.wait_timeout_ns;
     gp.G = p->G;
-    gp.N = p->N;
-    gp.K = p->K;
-    gp.k_tiles = p->k_tiles;
-    gp.n_chunks = p->n_chunks;
-    gp.total_chunks = p->total_chunks;
     gp.cap_single = p->cap_single;
     gp.cap_pair = p->cap_pair;
     gp.wide_rows = p->var.max_n;
@@ -491,27 +511,27 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->a_stages = 0;
 }
 
-nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, int32_t N, int32_t tile_n, int32_t max_ctas,
-                                    int32_t *cta_begin, int32_t *grid)
+nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,
+                                    int32_t tile_n, int32_t max_ctas, int32_t *cta_begin, int32_t *grid)
 {
-    if (!M || !cta_begin || !grid || num_groups < 1 || num_groups > kMaxGroups) return NVFP4_ERR_INVALID_ARG;
+    if (!M || !N || !K || !cta_begin || !grid || num_groups < 1 || num_groups > kMaxGroups)
+        return NVFP4_ERR_INVALID_ARG;
     if (max_ctas < 1 || max_ctas > kMaxCtas) return NVFP4_ERR_INVALID_ARG;
-    if (N < 8 || N > kMaxN || N % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (tile_n == 0) tile_n = kDefaultTileN;
     if (tile_n < kChunkN || tile_n > kMaxTileN || tile_n % kChunkN != 0) return NVFP4_ERR_INVALID_ARG;
-    std::vector<int32_t> m_tiles(num_groups), counts(kMaxCtas, 0);
+    std::vector<GroupShape> shapes(num_groups);
+    std::vector<int32_t> counts(kMaxCtas, 0);
     long total = 0;
-    const int n_chunks = ceil_div(N, kChunkN);
     for (int g = 0; g < num_groups; ++g) {
         if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
-        m_tiles[g] = ceil_div(M[g], kTileM);
-        total += (long)ceil_div(m_tiles[g], kRowTilesPerUnit) * n_chunks;
+        if (!shape_ok(N[g], K[g])) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        shapes[g] = GroupShape{ceil_div(M[g], kTileM), ceil_div(N[g], kChunkN), K[g] / kTileK, M[g]};
+        total += (long)ceil_div(shapes[g].m_tiles, kRowTilesPerUnit) * shapes[g].n_chunks;
     }
     if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int cap_single = tile_n / kChunkN;
     const int cap_pair = std::min(cap_single, pair_cap_chunks(variant_width(tile_n)));
-    *grid = schedule_ctas(m_tiles.data(), num_groups, n_chunks, cap_single, cap_pair, max_ctas, cta_begin,
-                          counts.data());
+    *grid = schedule_ctas(shapes.data(), num_groups, cap_single, cap_pair, max_ctas, cta_begin, counts.data());
     return NVFP4_OK;
 }
 
@@ -520,11 +540,22 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
 {
     if (!out) return NVFP4_ERR_INVALID_ARG;
     *out = nullptr;
-    if (num_groups < 1 || num_groups > kMaxGroups || !M || device < 0) return NVFP4_ERR_INVALID_ARG;
+    if (num_groups < 1 || num_groups > kMaxGroups || !M) return NVFP4_ERR_INVALID_ARG;
+    if (!shape_ok(N, K)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    std::vector<int32_t> Ns(num_groups, N), Ks(num_groups, K);
+    return nvfp4_ggemm_plan_shapes(out, device, num_groups, M, Ns.data(), Ks.data(), opt_in);
+}
+
+nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int num_groups, const int32_t *M,
+                                       const int32_t *N, const int32_t *K, const nvfp4_ggemm_options_t *opt_in)
+{
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_groups < 1 || num_groups > kMaxGroups || !M || !N || !K || device < 0) return NVFP4_ERR_INVALID_ARG;
     for (int g = 0; g < num_groups; ++g)
         if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
-    if (N < 8 || N > kMaxN || K < 256 || K > kMaxK) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (N % 8 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    for (int g = 0; g < num_groups; ++g)
+        if (!shape_ok(N[g], K[g])) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     nvfp4_ggemm_options_t opt;
     nvfp4_status_t st = validate_options(opt_in, &opt);
     if (st != NVFP4_OK) return st;
@@ -549,11 +580,10 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     p->device = device;
     p->sm_count = sms;
     p->G = num_groups;
-    p->N = N;
-    p->K = K;
     p->M.assign(M, M + num_groups);
+    p->N.assign(N, N + num_groups);
+    p->K.assign(K, K + num_groups);
     p->opt = opt;
-    p->k_tiles = K / kTileK;
 
     p->variant = ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused());
     if (p->variant < 0) {
@@ -566,19 +596,20 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
         return NVFP4_ERR_CUDA;
     }
 
-    // Work decomposition: m_pairs_g x ceil(N/32) chunks per group, prefix-summed.
+    // Work decomposition: m_pairs_g x ceil(N_g/32) chunks per group, prefix-summed.
     p->cap_single = opt.tile_n / kChunkN;
     p->cap_pair = std::min(p->cap_single, pair_cap_chunks(p->var.max_n));
-    p->n_chunks = ceil_div(N, kChunkN);
     p->chunk_prefix.assign(num_groups + 1, 0);
     p->m_tiles.assign(num_groups, 0);
     p->m_pairs.assign(num_groups, 0);
+    p->shapes.assign(num_groups, GroupShape{});
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         p->m_tiles[g] = ceil_div(M[g], kTileM);
         p->m_pairs[g] = ceil_div(p->m_tiles[g], kRowTilesPerUnit);
+        p->shapes[g] = GroupShape{p->m_tiles[g], ceil_div(N[g], kChunkN), K[g] / kTileK, M[g]};
         p->chunk_prefix[g] = (int32_t)total;
-        total += (long)p->m_pairs[g] * p->n_chunks;
+        total += (long)p->m_pairs[g] * p->shapes[g].n_chunks;
     }
     if (total > 0x7FFFFFFF) {
         release(p);
@@ -590,15 +621,15 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
     p->cta_begin.assign(cap + 1, 0);
     {
         std::vector<int32_t> counts(kMaxCtas, 0);
-        p->grid = schedule_ctas(p->m_tiles.data(), num_groups, p->n_chunks, p->cap_single, p->cap_pair, cap,
-                                p->cta_begin.data(), counts.data());
+        p->grid = schedule_ctas(p->shapes.data(), num_groups, p->cap_single, p->cap_pair, cap, p->cta_begin.data(),
+                                counts.data());
     }
     p->cta_begin.resize(p->grid + 1);
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
     p->ctas.assign(std::max(p->grid, 1), CtaRange{});
-    fill_cta_ranges(p->ctas.data(), p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->m_tiles.data(),
-                    p->M.data(), num_groups, p->n_chunks, p->cap_single, p->cap_pair);
+    fill_cta_ranges(p->ctas.data(), p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->shapes.data(),
+                    num_groups, p->cap_single, p->cap_pair);
     p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
@@ -615,11 +646,11 @@ nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_gro
         p->ws_sfb.assign(num_groups, 0);
         for (int g = 0; g < num_groups; ++g) {
             p->ws_sfa[g] = off;
-            off = align_up(off + atom_bytes(M[g], K), 256);
+            off = align_up(off + atom_bytes(M[g], K[g]), 256);
         }
         for (int g = 0; g < num_groups; ++g) {
             p->ws_sfb[g] = off;
-            off = align_up(off + atom_bytes(N, K), 256);
+            off = align_up(off + atom_bytes(N[g], K[g]), 256);
         }
         ok = cudaMalloc(&p->d_ws, std::max<size_t>(off, 256)) == cudaSuccess &&
              cudaMalloc(&p->d_prep_jobs, sizeof(RelayoutJob) * (size_t)num_groups) == cudaSuccess &&
@@ -657,8 +688,9 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
     DeviceGuard guard(p->device);
     if (!guard.ok) return NVFP4_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t K = (size_t)p->K, N = (size_t)p->N;
-    auto sf_bytes = [&](size_t rows) -> size_t { return p->raw() ? rows * K / 16 : (size_t)atom_bytes(rows, K); };
+    auto sf_bytes = [&](size_t rows, size_t K) -> size_t {
+        return p->raw() ? rows * K / 16 : (size_t)atom_bytes((int64_t)rows, (int64_t)K);
+    };
     if (!p->d_io) {
         size_t off = 0;
         p->io_a.assign(p->G, 0);
@@ -667,11 +699,11 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
         p->io_sfb.assign(p->G, 0);
         p->io_c.assign(p->G, 0);
         for (int g = 0; g < p->G; ++g) {
-            const size_t m = (size_t)p->M[g];
+            const size_t m = (size_t)p->M[g], N = (size_t)p->N[g], K = (size_t)p->K[g];
             p->io_a[g] = off, off = align_up(off + m * K / 2, 256);
             p->io_b[g] = off, off = align_up(off + N * K / 2, 256);
-            p->io_sfa[g] = off, off = align_up(off + sf_bytes(m), 256);
-            p->io_sfb[g] = off, off = align_up(off + sf_bytes(N), 256);
+            p->io_sfa[g] = off, off = align_up(off + sf_bytes(m, K), 256);
+            p->io_sfb[g] = off, off = align_up(off + sf_bytes(N, K), 256);
             p->io_c[g] = off, off = align_up(off + m * N * 2, 256);
         }
         p->io_bytes = std::max<size_t>(off, 256);
@@ -684,7 +716,7 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
     std::vector<const void *> dA(p->G), dB(p->G), dSFA(p->G), dSFB(p->G);
     std::vector<void *> dC(p->G);
     for (int g = 0; g < p->G; ++g) {
-        const size_t m = (size_t)p->M[g];
+        const size_t m = (size_t)p->M[g], N = (size_t)p->N[g], K = (size_t)p->K[g];
         dA[g] = p->d_io + p->io_a[g];
         dB[g] = p->d_io + p->io_b[g];
         dSFA[g] = p->d_io + p->io_sfa[g];
@@ -693,9 +725,9 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
         if (m == 0) continue;
         if (cudaMemcpyAsync(const_cast<void *>(dA[g]), A[g], m * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(const_cast<void *>(dB[g]), B[g], N * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(const_cast<void *>(dSFA[g]), SFA[g], sf_bytes(m), cudaMemcpyHostToDevice, s) !=
+            cudaMemcpyAsync(const_cast<void *>(dSFA[g]), SFA[g], sf_bytes(m, K), cudaMemcpyHostToDevice, s) !=
                 cudaSuccess ||
-            cudaMemcpyAsync(const_cast<void *>(dSFB[g]), SFB[g], sf_bytes(N), cudaMemcpyHostToDevice, s) !=
+            cudaMemcpyAsync(const_cast<void *>(dSFB[g]), SFB[g], sf_bytes(N, K), cudaMemcpyHostToDevice, s) !=
                 cudaSuccess) {
             cudaGetLastError();
             return NVFP4_ERR_CUDA;
@@ -707,7 +739,7 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
         return st;
     }
     for (int g = 0; g < p->G; ++g) {
-        const size_t m = (size_t)p->M[g];
+        const size_t m = (size_t)p->M[g], N = (size_t)p->N[g];
         if (m == 0) continue;
         if (cudaMemcpyAsync(C[g], dC[g], m * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
             cudaGetLastError();
@@ -735,12 +767,12 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
     if (!guard.ok) return NVFP4_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->prep_used && cudaEventSynchronize(p->ev_prep) != cudaSuccess) return NVFP4_ERR_CUDA;
-    const int pieces = p->K / 256;
     int nj = 0, items = 0;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
-        p->h_prep_jobs[nj++] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N, items};
-        items += ceil_div(p->N, 128) * pieces;
+        p->h_prep_jobs[nj++] =
+            RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N[g], p->K[g], items, 0};
+        items += ceil_div(p->N[g], 128) * (p->K[g] / 256);
     }
     if (nj > 0) {
         if (cudaMemcpyAsync(p->d_prep_jobs, p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)nj, cudaMemcpyHostToDevice,
@@ -749,7 +781,6 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
         RelayoutParams rp{};
         rp.jobs = p->d_prep_jobs;
         rp.njobs = nj;
-        rp.K = p->K;
         rp.total_items = items;
         if (relayout_launch(rp, p->sm_count, s) != cudaSuccess) {
             cudaGetLastError();
@@ -808,9 +839,8 @@ nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_
     }
     RelayoutParams rp{};
     rp.jobs = nullptr;
-    rp.single = RelayoutJob{static_cast<const uint8_t *>(in), static_cast<uint8_t *>(out), rows, 0};
+    rp.single = RelayoutJob{static_cast<const uint8_t *>(in), static_cast<uint8_t *>(out), rows, K, 0, 0};
     rp.njobs = 1;
-    rp.K = K;
     rp.total_items = ceil_div(rows, 128) * (K / 256);
     if (relayout_launch(rp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();

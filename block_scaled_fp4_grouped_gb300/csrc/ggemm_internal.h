@@ -39,24 +39,26 @@ enum WaitSite : uint32_t {
 
 // One entry of the device-resident problem table. Every tensor map
 // describes one group's buffer exactly, so the TMA zero-fills rows past
-// M_g / N. Two B maps: boxes as wide as the kernel's widest tile for
+// M_g / N_g. Two B maps: boxes as wide as the kernel's widest tile for
 // full-width tiles, 32-row boxes for the rest.
 struct alignas(128) GroupDesc {
-    CUtensorMap tmA;       // A_g bytes [M_g][K/2];   box 128 B x 32 rows;  128-byte swizzle
-    CUtensorMap tmB32;     // B_g bytes [N][K/2];     box 128 B x 32 rows;  128-byte swizzle
-    CUtensorMap tmBw;      // B_g bytes [N][K/2];     box 128 B x wide rows; 128-byte swizzle
-    CUtensorMap tmSFA;     // raw SFA_g [M_g][K/16];  box 32 B x 32 rows    (raw-scale path)
-    CUtensorMap tmSFB32;   // raw SFB_g [N][K/16];    box 32 B x 32 rows    (raw-scale path)
-    CUtensorMap tmSFBw;    // raw SFB_g [N][K/16];    box 32 B x wide rows  (raw-scale path)
+    CUtensorMap tmA;       // A_g bytes [M_g][K_g/2];   box 128 B x 32 rows;  128-byte swizzle
+    CUtensorMap tmB32;     // B_g bytes [N_g][K_g/2];   box 128 B x 32 rows;  128-byte swizzle
+    CUtensorMap tmBw;      // B_g bytes [N_g][K_g/2];   box 128 B x wide rows; 128-byte swizzle
+    CUtensorMap tmSFA;     // raw SFA_g [M_g][K_g/16];  box 32 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFB32;   // raw SFB_g [N_g][K_g/16];  box 32 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFBw;    // raw SFB_g [N_g][K_g/16];  box 32 B x wide rows  (raw-scale path)
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
     const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
-    uint16_t *C;               // C_g fp16 [M_g][N]
+    uint16_t *C;               // C_g fp16 [M_g][N_g]
     int32_t M;
     int32_t m_tiles;      // ceil(M / 128)
     int32_t m_pairs;      // ceil(m_tiles / 2): passes over B
     int32_t chunk_begin;  // first scheduling chunk of this group (prefix sum)
     int32_t b_keep;       // 1: B is read by more than one pair of row tiles (keep it in L2)
-    int32_t pad[3];
+    int32_t N;            // N_g
+    int32_t k_tiles;      // K_g / 256
+    int32_t n_chunks;     // ceil(N_g / 32)
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
@@ -72,20 +74,49 @@ struct alignas(32) CtaRange {
 };
 static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 
+// Per-group shape for the host scheduling helpers.
+struct GroupShape {
+    int32_t m_tiles;   // ceil(M_g / 128)
+    int32_t n_chunks;  // ceil(N_g / 32)
+    int32_t k_tiles;   // K_g / 256
+    int32_t M;
+};
+
 // What a CTA needs to start, packed into 16 bytes of the kernel parameters
 // so that no role reads memory before its first load. CTA c's range ends
 // where CTA c + 1's begins (a sentinel follows the last CTA).
 struct CtaStart {
     int32_t begin;    // first chunk
     int32_t g_base;   // chunk_prefix[g]
-    int32_t g_rows;   // M of group g
-    uint32_t packed;  // g (bits 0-15) | widest tile in chunks (16-23) | most row tiles (24-31)
+    uint32_t rows;    // group g: M (bits 0-20) | K / 256 (bits 21-31)
+    uint32_t packed;  // g (bits 0-9) | widest tile in chunks (10-13) | most row tiles (14-15) |
+                      // group g's ceil(N / 32) (16-31)
 };
 static_assert(sizeof(CtaStart) == 16, "packed start record");
 
-// Work decomposition: group g owns m_pairs_g * ceil(N/32) chunks (32 columns
-// of one pair of 128-row tiles), numbered after the chunks of groups 0..g-1
-// (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N/32) chunks.
+// The one packing of CtaStart's fields, used by the host and the kernel.
+#if defined(__CUDACC__)
+#define NVFP4_HD __host__ __device__ __forceinline__
+#else
+#define NVFP4_HD inline
+#endif
+NVFP4_HD uint32_t cta_pack_rows(int M, int k_tiles) { return (uint32_t)(M & 0x1FFFFF) | ((uint32_t)(k_tiles & 0x7FF) << 21); }
+NVFP4_HD uint32_t cta_pack(int g, int max_chunks, int max_rows, int n_chunks)
+{
+    return (uint32_t)(g & 0x3FF) | ((uint32_t)(max_chunks & 0xF) << 10) | ((uint32_t)(max_rows & 0x3) << 14) |
+           ((uint32_t)(n_chunks & 0xFFFF) << 16);
+}
+NVFP4_HD int cta_rows_m(uint32_t rows) { return (int)(rows & 0x1FFFFFu); }
+NVFP4_HD int cta_rows_ktiles(uint32_t rows) { return (int)(rows >> 21); }
+NVFP4_HD int cta_group(uint32_t packed) { return (int)(packed & 0x3FFu); }
+NVFP4_HD int cta_max_chunks(uint32_t packed) { return (int)((packed >> 10) & 0xFu); }
+NVFP4_HD int cta_max_rows(uint32_t packed) { return (int)((packed >> 14) & 0x3u); }
+NVFP4_HD int cta_n_chunks(uint32_t packed) { return (int)(packed >> 16); }
+
+// Work decomposition: group g owns m_pairs_g * ceil(N_g/32) chunks (32
+// columns of one pair of 128-row tiles), numbered after the chunks of groups
+// 0..g-1 (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N_g/32)
+// chunks.
 // CTA c takes the chunk range [cta_begin[c], cta_begin[c+1]) and walks it as
 // tiles inside one segment of up to cap_pair chunks (segments with two row
 // tiles, whose accumulators share TMEM) or cap_single chunks (one row tile).
@@ -95,10 +126,7 @@ struct GemmParams {
     CtaStart cta[kMaxCtas + 1];    // [grid + 1]
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
-    int32_t G, N, K;
-    int32_t k_tiles;               // K / 256
-    int32_t n_chunks;              // ceil(N / 32)
-    int32_t total_chunks;
+    int32_t G;
     int32_t cap_single;            // chunks per tile, one row tile (1..MAXN/32)
     int32_t cap_pair;              // chunks per tile, two row tiles
     int32_t wide_rows;             // rows of the wide B boxes (the kernel's widest tile)
@@ -109,22 +137,23 @@ struct GemmParams {
 // each range exactly as the kernel does to bound its tiles; pack_cta_starts
 // turns them into the kernel's start records (grid + 1 entries).
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const int32_t *m_tiles, const int32_t *M, int G, int n_chunks, int cap_single, int cap_pair);
-void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks);
+                     const GroupShape *shapes, int G, int cap_single, int cap_pair);
+void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {
     const uint8_t *src;  // raw [rows][K/16]
     uint8_t *dst;        // atoms
     int32_t rows;
+    int32_t K;
     int32_t item_begin;  // prefix over jobs of ceil(rows/128) * (K/256)
+    int32_t pad;
 };
 
 struct RelayoutParams {
     const RelayoutJob *jobs;  // device array, or nullptr to use `single`
     RelayoutJob single;
     int32_t njobs;
-    int32_t K;
     int32_t total_items;
 };
 
@@ -153,15 +182,15 @@ cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t 
 // widest tile is max_n columns (their accumulators share TMEM).
 int pair_cap_chunks(int max_n);
 
-// Splits the chunks of all segments into per-CTA ranges, written to
-// cta_begin[0..grid], and returns grid (<= max_ctas <= kMaxCtas). When every
-// segment can be covered by tiles of at most its cap with no more than
-// max_ctas CTAs in total, each CTA gets one tile inside one segment, and the
-// tiles are sized to balance the columns (B bytes) per CTA; otherwise the
-// chunks are split into equal contiguous ranges. m_tiles[g] = ceil(M_g/128);
-// counts is scratch for kMaxCtas ints.
-int schedule_ctas(const int32_t *m_tiles, int G, int n_chunks, int cap_single, int cap_pair, int max_ctas,
-                  int32_t *cta_begin, int32_t *counts);
+// Splits the chunks of all segments (pairs of row tiles, group by group)
+// into per-CTA ranges, written to cta_begin[0..grid], and returns grid
+// (<= max_ctas <= kMaxCtas). With no more segments than max_ctas, every range
+// lies inside one segment: the split takes the smallest per-CTA budget of
+// k-stages (passes over K_g times K_g / 256) that fits max_ctas CTAs, and
+// spare CTAs then shorten the longest ranges; otherwise the chunks are split
+// into equal contiguous ranges. counts is scratch for kMaxCtas ints.
+int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int32_t *cta_begin,
+                  int32_t *counts);
 using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                        const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                        CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,

@@ -126,6 +126,8 @@ struct Unit {
     int ncols;   // tile width: a multiple of 32
     bool keep;   // the group has more pairs of row tiles, which read B again
     int M;       // rows of the group
+    int N;       // columns of the group
+    int k_tiles; // K of the group / 256
 };
 
 // Walks this CTA's contiguous range of chunks as tiles.
@@ -134,16 +136,18 @@ struct Walker {
     // the part of the range inside the current pair: [pb, pb + plen) cut
     // into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
-    int g, g_base, g_tiles, g_rows, mt0 = 0, mtu = 0, ch0 = 0;
+    int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
         const CtaStart &r = p.cta[blockIdx.x];
         pos = r.begin;
         end = p.cta[blockIdx.x + 1].begin;
-        g = (int)(r.packed & 0xFFFFu);
+        g = cta_group(r.packed);
         g_base = r.g_base;
-        g_rows = r.g_rows;
+        g_rows = cta_rows_m(r.rows);
+        g_ktiles = cta_rows_ktiles(r.rows);
+        g_chunks = cta_n_chunks(r.packed);
         g_tiles = (g_rows + kTileM - 1) / kTileM;
     }
 
@@ -152,18 +156,22 @@ struct Walker {
         if (pi == pt) {
             if (pos >= end) return false;
             // groups past the one holding `pos` (only ranges that span groups get here)
-            while (pos >= g_base + ((g_tiles + 1) >> 1) * p.n_chunks) {
+            while (pos >= g_base + ((g_tiles + 1) >> 1) * g_chunks) {
                 ++g;
+                const GroupDesc &gd = p.groups[g];
                 g_base = __ldg(p.chunk_prefix + g);
-                g_tiles = p.groups[g].m_tiles;
-                g_rows = p.groups[g].M;
+                g_rows = gd.M;
+                g_tiles = gd.m_tiles;
+                g_chunks = gd.n_chunks;
+                g_ktiles = gd.k_tiles;
+                g_cols = gd.N;
             }
             const int local = pos - g_base;
-            const int mp = local / p.n_chunks;
-            ch0 = local - mp * p.n_chunks;
+            const int mp = local / g_chunks;
+            ch0 = local - mp * g_chunks;
             mt0 = mp * kRowTilesPerUnit;
             mtu = min(kRowTilesPerUnit, g_tiles - mt0);
-            plen = min(p.n_chunks - ch0, end - pos);
+            plen = min(g_chunks - ch0, end - pos);
             const int cap = mtu == 2 ? p.cap_pair : p.cap_single;
             pt = (plen + cap - 1) / cap;
             pi = 0;
@@ -179,6 +187,10 @@ struct Walker {
         t.ncols = (c1 - c0) * kChunkN;
         t.keep = g_tiles > kRowTilesPerUnit;
         t.M = g_rows;
+        t.k_tiles = g_ktiles;
+        // N itself is only in the table; a bound that never cuts a live column
+        // (the chunks cover N) serves until a role reads it
+        t.N = g_cols >= 0 ? g_cols : g_chunks * kChunkN;
         return true;
     }
 };
@@ -357,8 +369,8 @@ struct Roles {
     __device__ void size_rings()
     {
         const uint32_t packed = p.cta[blockIdx.x].packed;
-        max_chunks = min(max((int)((packed >> 16) & 0xFFu), 1), MAXN / kChunkN);
-        max_rows = min(max((int)(packed >> 24), 1), kRowTilesPerUnit);
+        max_chunks = min(max(cta_max_chunks(packed), 1), MAXN / kChunkN);
+        max_rows = min(max(cta_max_rows(packed), 1), kRowTilesPerUnit);
         b_slot = (uint32_t)max_chunks * kBRowBoxBytes;
         a_slot = (uint32_t)max_rows * kATileBytes;
         nb = min(kDoneRing, C::kBRing / (int)b_slot);
@@ -455,7 +467,7 @@ struct Roles {
             const bool wide = (t.ncols == p.wide_rows);
             const int boxes = t.ncols / 32;
             const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_done(seq - nb, kSiteBEmpty)) {
                     ok = false;
                     break;
@@ -509,7 +521,7 @@ struct Roles {
             }
             int live_boxes[kRowTilesPerUnit];
             const int boxes = row_boxes(t, t.M, live_boxes);
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_done(seq - na, kSiteAEmpty)) {
                     ok = false;
                     break;
@@ -547,8 +559,7 @@ struct Roles {
         int last_g = -1;
         bool signalled = false;
         bool ok = true;
-        const size_t katoms = (size_t)(p.K / 64);
-        const int s_tiles = (p.k_tiles + C::kKS - 1) / C::kKS;  // scale stages per tile
+
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
@@ -562,9 +573,11 @@ struct Roles {
             const bool wide = (t.ncols == p.wide_rows);
             const int bboxes = t.ncols / 32;
             int b0 = 0, nblk = 0;
-            sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
+            sfb_blocks(t.n0, t.ncols, t.N, b0, nblk);
             int live_boxes[kRowTilesPerUnit];
             const int aboxes = row_boxes(t, t.M, live_boxes);
+            const size_t katoms = (size_t)t.k_tiles * 4;                 // 64-k atoms per 128-row block
+            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;  // scale stages of this tile
             const uint32_t bytes =
                 RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
                     : (uint32_t)t.mtu * kSfTileBytes + (uint32_t)nblk * kSfTileBytes;
@@ -634,9 +647,9 @@ struct Roles {
         Unit t;
         while (ok && wk.next(p, t)) {
             int b0 = 0, nblk = 0;
-            sfb_blocks(t.n0, t.ncols, p.N, b0, nblk);
+            sfb_blocks(t.n0, t.ncols, t.N, b0, nblk);
             const int s0 = (t.n0 % 128) / 32;
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            for (int kt = 0; kt < t.k_tiles; ++kt) {
                 const int sub = kt % C::kKS;  // k tile within the scale stage
                 if (!warp_wait_done(seq - NT, kSiteSfFree) ||
                     (sub == 0 && !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull))) {
@@ -709,7 +722,7 @@ struct Roles {
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                const bool stage_done = (sub == C::kKS - 1) || (kt == p.k_tiles - 1);
+                const bool stage_done = (sub == C::kKS - 1) || (kt == t.k_tiles - 1);
                 if (lane == 0) {
                     if (stage_done) mbar_arrive(s_empty(rs.stage));
                     mbar_arrive(sf_ready(rt.stage));
@@ -734,7 +747,7 @@ struct Roles {
             tc_fence_after_sync();
             const uint32_t d = tmem + (uint32_t)(racc.stage * C::kAccCols);
             const uint32_t idesc = idesc_mxf4nvf4_m128((uint32_t)t.ncols);
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_phase(b_full(rb.stage), rb.phase, abort_flag, p, kSiteBFull) ||
                     !wait_phase(a_full(ra.stage), ra.phase, abort_flag, p, kSiteAFull) ||
                     !wait_phase(sf_ready(rt.stage), rt.phase, abort_flag, p, kSiteSfReady)) {
@@ -782,21 +795,22 @@ struct Roles {
         Unit t;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
+            const int N = gd->N;
             if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
             tc_fence_after_sync();
             // columns [n0, n0 + 32 * nblk) hold live data; this warp takes blocks
             // h, h + 2, ... with two tcgen05.ld in flight: the next block is read
             // while the current one is converted and stored
-            const int nblk = (min(t.ncols, p.N - t.n0) + 31) / 32;
+            const int nblk = (min(t.ncols, N - t.n0) + 31) / 32;
             const int mine = (nblk - h + 1) / 2;
-            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (p.N % 16 == 0);
+            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (N % 16 == 0);
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
                 if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
                 const int row = row0 + lane;
                 const bool live = row < t.M;
-                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)p.N;
+                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)N;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
@@ -806,12 +820,12 @@ struct Roles {
                     tmem_ld_wait();
                     pin_registers(v0);
                     if (j + 1 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 1)), v1);
-                    if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), p.N, v0, wide_st, pol_c);
+                    if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), N, v0, wide_st, pol_c);
                     if (j + 1 < mine) {
                         tmem_ld_wait();
                         pin_registers(v1);
                         if (j + 2 < mine) tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * (j + 2)), v0);
-                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j + 2), p.N, v1, wide_st, pol_c);
+                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j + 2), N, v1, wide_st, pol_c);
                     }
                 }
             }
@@ -837,10 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     if (warp == kWarpEpi0 && lane < 6) {
         // start fetching the tensor maps of this CTA's first group while the
         // barriers and TMEM are set up
-        const int g = (int)(p.cta[blockIdx.x].packed & 0xFFFFu);
+        const int g = cta_group(p.cta[blockIdx.x].packed);
         const GroupDesc *gd = p.groups + g;
         // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
-        if (RAW || lane < 3) prefetch_tensormap(&gd->tmA + lane);
+        if (g < p.G && (RAW || lane < 3)) prefetch_tensormap(&gd->tmA + lane);
     }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
@@ -883,9 +897,6 @@ __global__ void __launch_bounds__(256) sf_relayout_kernel(const __grid_constant_
 {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
-    const int pieces = p.K / 256;
-    const int katoms = p.K / 64;
-    const size_t row_bytes = (size_t)(p.K / 16);
     for (int item = blockIdx.x * wpb + (threadIdx.x >> 5); item < p.total_items; item += gridDim.x * wpb) {
         RelayoutJob job;
         if (p.jobs == nullptr) {
@@ -899,6 +910,9 @@ __global__ void __launch_bounds__(256) sf_relayout_kernel(const __grid_constant_
             }
             job = p.jobs[lo];
         }
+        const int pieces = job.K / 256;
+        const int katoms = job.K / 64;
+        const size_t row_bytes = (size_t)(job.K / 16);
         const int l = item - job.item_begin;
         const int rb = l / pieces;
         const int pc = l % pieces;

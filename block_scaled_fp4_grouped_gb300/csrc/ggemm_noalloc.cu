@@ -112,14 +112,14 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     auto *groups = reinterpret_cast<GroupDesc *>(table);
     auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
     const int n_chunks = ceil_div_i(N, kChunkN);
-    int32_t m_tiles[kNoAllocMaxGroups];
+    GroupShape shapes[kNoAllocMaxGroups];
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         GroupDesc &d = groups[g];
         d.M = M[g];
         d.m_tiles = ceil_div_i(M[g], kTileM);
         d.m_pairs = ceil_div_i(d.m_tiles, kRowTilesPerUnit);
-        m_tiles[g] = d.m_tiles;
+        shapes[g] = GroupShape{d.m_tiles, n_chunks, K / kTileK, M[g]};
         d.chunk_begin = (int32_t)total;
         prefix[g] = (int32_t)total;
         total += (long)d.m_pairs * n_chunks;
@@ -135,11 +135,11 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     const int cap_pair = pair_cap_chunks(kMaxTileN);
     int32_t cta_begin[kMaxCtas + 1];
     int32_t counts[kMaxCtas];
-    const int grid = schedule_ctas(m_tiles, num_groups, n_chunks, cap_single, cap_pair,
-                                   std::min(g_sm_count[dev], kMaxCtas), cta_begin, counts);
+    const int grid = schedule_ctas(shapes, num_groups, cap_single, cap_pair, std::min(g_sm_count[dev], kMaxCtas),
+                                   cta_begin, counts);
     if (grid < 1) return NVFP4_OK;
     CtaRange ranges[kMaxCtas];
-    fill_cta_ranges(ranges, cta_begin, grid, prefix, m_tiles, M, num_groups, n_chunks, cap_single, cap_pair);
+    fill_cta_ranges(ranges, cta_begin, grid, prefix, shapes, num_groups, cap_single, cap_pair);
 
     // --- upload (pageable source: the call returns once the bytes are staged,
     //     so the stack buffer may go away), clear the error word, launch
@@ -155,15 +155,10 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     GemmParams gp{};
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
-    pack_cta_starts(gp.cta, ranges, grid, (int)total);
+    pack_cta_starts(gp.cta, ranges, grid, (int)total, shapes);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
-    gp.N = N;
-    gp.K = K;
-    gp.k_tiles = K / kTileK;
-    gp.n_chunks = n_chunks;
-    gp.total_chunks = (int32_t)total;
     gp.cap_single = cap_single;
     gp.cap_pair = cap_pair;
     gp.wide_rows = kMaxTileN;

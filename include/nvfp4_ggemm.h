@@ -129,6 +129,19 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, i
                                 const nvfp4_ggemm_options_t *opt);
 
 /*
+ * The same with per-group N_g and K_g (host arrays N[0..G-1], K[0..G-1]):
+ * group g computes C_g[M_g, N_g] = sum over K_g of the block-scaled products
+ * of A_g[M_g, K_g] and B_g[N_g, K_g], every size meeting the per-group rules
+ * above (N_g % 8 == 0, K_g % 256 == 0). The pages' own interface takes one
+ * (m, n, k) per group; nvfp4_ggemm_plan is this call with N_g = N and
+ * K_g = K. Everything else (layouts per group, run, run_host, prepare,
+ * status) is as for nvfp4_ggemm_plan.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int num_groups,
+                                       const int32_t *M, const int32_t *N, const int32_t *K,
+                                       const nvfp4_ggemm_options_t *opt);
+
+/*
  * Grouped GEMM on device buffers. A, B, SFA, SFB, C are host arrays of G
  * device pointers (layouts above; scales in the plan's sf_layout). `stream`
  * is a cudaStream_t (NULL = legacy default stream). Encodes the per-group
@@ -188,22 +201,25 @@ NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
 
 /*
  * The work split a plan would use, computed on the host alone (no device,
- * no allocation). Every group with M_g > 0 has ceil(ceil(M_g/128)/2) pairs
- * of 128-row tiles; each pair owns ceil(N/32) consecutive 32-column chunks,
- * numbered group by group. CTA c of the persistent grid takes chunks
- * [cta_begin[c], cta_begin[c+1]). tile_n (0 = 256) and the kernel width it
- * selects cap the tiles as in nvfp4_ggemm_options_t; the kernel cuts a range
- * into the fewest tiles within the cap, of equal width to within one chunk.
- * When there are no more pairs than max_ctas, every range lies inside one
- * pair: the split uses the fewest tiles per CTA (passes over K) that fit
+ * no allocation). M, N and K are host arrays of the G per-group sizes (the
+ * limits of nvfp4_ggemm_plan_shapes). Every group with M_g > 0 has
+ * ceil(ceil(M_g/128)/2) pairs of 128-row tiles; each pair owns ceil(N_g/32)
+ * consecutive 32-column chunks, numbered group by group. CTA c of the
+ * persistent grid takes chunks [cta_begin[c], cta_begin[c+1]). tile_n (0 =
+ * 256) and the kernel width it selects cap the tiles as in
+ * nvfp4_ggemm_options_t; the kernel cuts a range into the fewest tiles within
+ * the cap, of equal width to within one chunk. When there are no more pairs
+ * than max_ctas, every range lies inside one pair: the split uses the
+ * smallest budget of k-stages per CTA (tiles times K_g/256) that fits
  * max_ctas CTAs, and spare CTAs then shorten the longest ranges. Otherwise
- * the chunks are cut into equal contiguous ranges. cta_begin must
- * hold max_ctas + 1 entries (max_ctas 1..192); *grid receives the CTA
- * count (0 when every M_g is 0). This is not an operation of the pages; it
- * exposes the scheduling step for inspection and testing.
+ * the chunks are cut into equal contiguous ranges. cta_begin must hold
+ * max_ctas + 1 entries (max_ctas 1..192); *grid receives the CTA count (0
+ * when every M_g is 0). This is not an operation of the pages; it exposes
+ * the scheduling step for inspection and testing.
  */
-NVFP4_API nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, int32_t N, int32_t tile_n,
-                                    int32_t max_ctas, int32_t *cta_begin, int32_t *grid);
+NVFP4_API nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N,
+                                    const int32_t *K, int32_t tile_n, int32_t max_ctas,
+                                    int32_t *cta_begin, int32_t *grid);
 
 /* Plan introspection (for tests and benchmarks). */
 typedef struct {

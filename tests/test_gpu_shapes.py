@@ -1,0 +1,117 @@
+"""Per-group N_g and K_g (nvfp4_ggemm_plan_shapes) on the GPU against the oracle.
+
+Group g computes C_g[M_g, N_g] from A_g[M_g, K_g] and B_g[N_g, K_g] with their
+own scales; the oracle computes each group on its own (it is a per-group
+definition), so the comparison is element by element within the stated
+tolerance |gpu - ref| <= 1e-2 + 1e-2 |ref|. The shapes mix N_g that are and
+are not multiples of 32 and 256, K_g of one to many 256-k stages, groups of
+one and two 128-row tiles, an empty group and a partial last row tile."""
+import numpy as np
+import pytest
+
+import oracle
+from block_scaled_fp4_grouped_gb300 import synth
+from gpu_util import assert_close, atom_copy, to_device
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [  # (M_g, N_g, K_g)
+    (200, 328, 768),
+    (64, 4096, 256),
+    (0, 512, 512),
+    (130, 72, 2048),
+    (256, 1000, 1536),
+    (17, 8, 256),
+    (384, 2056, 1024),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_scaled_fp4_grouped_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def O():
+    return oracle.get()
+
+
+def _groups(seed):
+    parts = [synth.make_problem("custom", seed=seed + g, M=[m], N=n, K=k) for g, (m, n, k) in enumerate(SHAPES)]
+    return parts
+
+
+def _run(parts, sf_layout="raw", sf_path="fused", use_host=False, cache_b_scales=False):
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    M = [p.M[0] for p in parts]
+    N = [p.N for p in parts]
+    K = [p.K for p in parts]
+    if use_host:
+        A = [np.ascontiguousarray(p.A[0]) for p in parts]
+        B = [np.ascontiguousarray(p.B[0]) for p in parts]
+        SFA = [np.ascontiguousarray(p.SFA[0]) for p in parts]
+        SFB = [np.ascontiguousarray(p.SFB[0]) for p in parts]
+        C = [np.zeros((m, n), np.float16) for m, n in zip(M, N)]
+        with nb.GroupedGemm(M, N, K) as gg:
+            gg.run_host(A, B, SFA, SFB, C)
+            st, word = gg.sync_status()
+            assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+        return C
+    A = to_device([p.A[0] for p in parts])
+    B = to_device([p.B[0] for p in parts])
+    SFA = to_device([p.SFA[0] for p in parts])
+    SFB = to_device([p.SFB[0] for p in parts])
+    if sf_layout == "atom":
+        SFA = [atom_copy(s, m, k) for s, m, k in zip(SFA, M, K)]
+        SFB = [atom_copy(s, n, k) for s, n, k in zip(SFB, N, K)]
+    C = [torch.full((m, n), float("nan"), dtype=torch.float16, device="cuda") for m, n in zip(M, N)]
+    with nb.GroupedGemm(M, N, K, sf_layout=sf_layout, sf_path=sf_path, cache_b_scales=cache_b_scales) as gg:
+        if cache_b_scales:
+            gg.prepare_b_scales(SFB)
+            gg.run(A, B, SFA, [None] * len(SFB), C)
+        else:
+            gg.run(A, B, SFA, SFB, C)
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+    torch.cuda.synchronize()
+    return [c.cpu().numpy() for c in C]
+
+
+@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "relayout", False),
+                                                ("raw", "relayout", True), ("atom", "fused", False)])
+def test_per_group_shapes_match_the_oracle(O, layout, path, cached):
+    parts = _groups(seed=500)
+    got = _run(parts, sf_layout=layout, sf_path=path, cache_b_scales=cached)
+    for g, p in enumerate(parts):
+        assert got[g].shape == (p.M[0], p.N)
+        if p.M[0] == 0:
+            continue
+        ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
+        assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
+        assert_close(got[g], ref, f"group {g} (M={p.M[0]}, N={p.N}, K={p.K})")
+
+
+def test_per_group_shapes_through_host_buffers(O):
+    parts = _groups(seed=600)
+    got = _run(parts, use_host=True)
+    for g, p in enumerate(parts):
+        if p.M[0] == 0:
+            continue
+        ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
+        assert_close(got[g], ref, f"group {g}")
+
+
+def test_uniform_call_equals_per_group_call_bitwise():
+    prob = synth.make_problem("custom", seed=700, M=[150, 0, 300], N=384, K=1024)
+    parts = []
+    for g, m in enumerate(prob.M):
+        q = synth.Problem("part", prob.N, prob.K, [m], seed=700)
+        q.A, q.B, q.SFA, q.SFB = [prob.A[g]], [prob.B[g]], [prob.SFA[g]], [prob.SFB[g]]
+        parts.append(q)
+    per_group = _run(parts)
+    from gpu_util import run_gpu
+    uniform = run_gpu(prob)
+    for g in range(prob.G):
+        assert np.array_equal(per_group[g].view(np.uint16), uniform[g].view(np.uint16))

@@ -121,3 +121,58 @@ def test_bad_arguments(kw):
     args.update(kw)
     st, _ = nb.nvfp4_ggemm_schedule(args["M"], args["N"], args["tile_n"], args["max_ctas"])
     assert st in (nb.NVFP4_ERR_INVALID_ARG, nb.NVFP4_ERR_UNSUPPORTED_SHAPE)
+
+
+def _check_shapes(M, N, K, tile_n, max_ctas):
+    """Per-group N_g and K_g: the ranges partition the chunks (pairs of group g
+    own ceil(N_g/32) chunks each); with no more pairs than CTAs every range
+    lies in one pair and the most k-stages any CTA needs (tiles x K_g/256) is
+    the smallest budget with which the pairs fit the grid."""
+    st, cb = nb.nvfp4_ggemm_schedule(M, N, tile_n, max_ctas, K=K)
+    assert st == nb.NVFP4_OK
+    single, pair = caps(tile_n)
+    segs = []  # (first chunk, chunks, cap, k tiles)
+    base = 0
+    for m, n, k in zip(M, N, K):
+        tiles = -(-m // 128)
+        for t in range(0, tiles, 2):
+            c = -(-n // 32)
+            segs.append((base, c, pair if tiles - t >= 2 else single, k // 256))
+            base += c
+    total = base
+    grid = len(cb) - 1
+    if total == 0:
+        assert grid == 0
+        return
+    assert cb[0] == 0 and cb[-1] == total and all(b > a for a, b in zip(cb, cb[1:]))
+    if len(segs) > max_ctas:
+        return
+    def seg_of(x):
+        return next(i for i, s in enumerate(segs) if s[0] <= x < s[0] + s[1])
+    def need(budget):
+        return sum(-(-c // (max(1, budget // kt) * cap)) for _, c, cap, kt in segs)
+    fewest = next(B for B in range(1, 10 ** 7) if need(B) <= max_ctas)
+    for a, b in zip(cb, cb[1:]):
+        i = seg_of(a)
+        assert seg_of(b - 1) == i, f"range [{a},{b}) crosses a pair boundary"
+        _, c, cap, kt = segs[i]
+        stages = -(-(b - a) // cap) * kt
+        # within the smallest fitting budget, or one pass where a pass alone exceeds it
+        assert stages <= max(fewest, kt), (stages, fewest, kt)
+
+
+@pytest.mark.parametrize("tile_n", [0, 192, 128])
+def test_random_per_group_shapes(tile_n):
+    rng = random.Random(77 + tile_n)
+    for _ in range(150):
+        G = rng.randint(1, 10)
+        M = [rng.choice([0, rng.randint(1, 600)]) for _ in range(G)]
+        N = [8 * rng.randint(1, 700) for _ in range(G)]
+        K = [256 * rng.randint(1, 24) for _ in range(G)]
+        _check_shapes(M, N, K, tile_n, rng.choice([1, 7, 64, 152]))
+
+
+def test_per_group_bad_shapes():
+    for N, K in (([256, 12], [256, 256]), ([256, 256], [256, 300])):
+        st, _ = nb.nvfp4_ggemm_schedule([64, 64], N, 0, 152, K=K)
+        assert st == nb.NVFP4_ERR_UNSUPPORTED_SHAPE
