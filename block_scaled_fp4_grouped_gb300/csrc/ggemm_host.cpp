@@ -1,7 +1,7 @@
 // Host side of the C ABI: argument validation, the work decomposition
-// (prefix sums of column chunks), per-group TMA tensor maps in a
-// device-resident problem table, workspace for re-laid-out scales, kernel
-// launches and the device error word.
+// (prefix sums of column chunks, per-CTA ranges), per-group TMA tensor maps
+// in a device-resident problem table, workspace for re-laid-out scales,
+// kernel launches and the device error word.
 #include <algorithm>
 #include <cstring>
 #include <mutex>

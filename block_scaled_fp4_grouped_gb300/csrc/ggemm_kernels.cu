@@ -1,35 +1,40 @@
 // Device code: the persistent warp-specialised NVFP4 grouped GEMM and the
 // scale re-layout kernel, for sm_103a.
 //
-// GEMM structure (one CTA per SM, persistent, 12 warps):
+// GEMM structure (one CTA per SM, persistent, 16 warps):
 //   warp 0      B producer: per 256-k stage, TMA loads of the tile's B rows
-//               (128-byte swizzle) into a ring of NB stages. B is the operand
-//               streamed from HBM; its stages hold nothing else, so a stage
-//               is refilled as soon as its MMAs have read it.
-//   warp 6      A producer: the unit's one or two 128-row A tiles into a ring
-//               of NA stages (A is small and re-read from L2).
+//               (128-byte swizzle) into the B ring. B is the operand streamed
+//               from HBM; a slot holds nothing else, so it is refilled as
+//               soon as its MMAs have read it.
+//   warp 6      A producer: the tile's one or two 128-row A tiles (only the
+//               32-row boxes that hold rows < M_g) into the A ring; A is
+//               small and re-read from L2.
 //   warp 7      scale producer: the stage's A and B scales into a ring of NS
 //               small stages, running ahead of the operands.
 //   warps 8-11  scale writers: each turns a scale stage into the TMEM layout
 //               the block-scaled MMA reads (32 lanes x 4 columns per 128
 //               rows, the same in every lane quarter) and writes its quarter
-//               with tcgen05.st into one of NT TMEM scale buffers. Raw
+//               with tcgen05.st into one of two TMEM scale buffers. Raw
 //               row-major and atom-layout scales are both handled here, off
 //               the tensor pipe and ahead of the MMAs.
 //   warp 1      allocates TMEM; one lane issues kind::mxf4nvf4 block16 MMAs
 //               (M = 128 per row tile, N = tile width up to MAXN) into fp32
 //               accumulators, then commits one stage-completion barrier that
 //               frees the stage's A and B slots and its TMEM scale buffer.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulators (one lane quarter
-//               each), RN to fp16, 16-byte stores of each row straight to C.
-// Work: group g owns m_pairs_g x ceil(N/32) chunks (32 columns of one pair
+//   warps 2-5,  epilogue: tcgen05.ld of the accumulators (lane quarter
+//   12-15       warp % 4; the two warps of a quarter split the 32-column
+//               blocks), RN to fp16, 32- or 16-byte stores of each row
+//               straight to C.
+// Work: group g owns m_pairs_g x ceil(N_g/32) chunks (32 columns of one pair
 // of 128-row tiles); the chunks of all groups are numbered through prefix
-// sums, and the host gives every CTA a contiguous chunk range (cta_begin).
-// A CTA walks its range as tiles inside one pair: up to 192 columns when the
-// pair has two row tiles (their accumulators share TMEM) and up to MAXN when
-// it has one. Both row tiles of a pair share every B stage, so each B strip
-// is read from HBM once, by one SM. Where the grid allows, the host makes
-// each range a single tile, so a CTA streams its B strip in one pass over K.
+// sums, and the host gives every CTA a contiguous chunk range (its start
+// record travels in the kernel parameters). A CTA walks its range as tiles
+// inside one pair: up to 192 columns when the pair has two row tiles (their
+// accumulators share TMEM) and up to MAXN when it has one. Both row tiles of
+// a pair share every B stage, so each B strip is read from HBM once, by one
+// SM. The host keeps every range inside one pair when it can and picks the
+// smallest per-CTA budget of k-stages that fits the grid, so a CTA streams
+// its B strip in as few passes over K as possible.
 //
 // Every mbarrier wait is bounded by the plan's timeout: on expiry the waiter
 // records (status, site, block) in the error word, raises a CTA-wide abort
@@ -133,8 +138,8 @@ struct Unit {
 // Walks this CTA's contiguous range of chunks as tiles.
 struct Walker {
     int pos, end;
-    // the part of the range inside the current pair: [pb, pb + plen) cut
-    // into pt tiles of equal width (to within one chunk); pi = next tile
+    // the part of the range inside the current pair (plen chunks from ch0)
+    // is cut into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
     int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
 

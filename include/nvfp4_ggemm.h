@@ -10,7 +10,9 @@
  *                                * e2m1(B_g[n,k]) * e4m3(SFB_g[n, k/16]) )
  *
  * for m < M_g, n < N. Products accumulate in fp32 on the tensor cores and
- * the result is rounded to fp16 (round to nearest even) once.
+ * the result is rounded to fp16 (round to nearest even) once. N and K are
+ * shared by the groups here; nvfp4_ggemm_plan_shapes takes N_g and K_g per
+ * group, and everything below then holds with N_g, K_g in place of N, K.
  *
  * Layouts (all dense, row-major, K-major for the inputs; device memory):
  *   A[g]    M_g x K/2 bytes. Two E2M1 codes per byte, the even k in the low
