@@ -49,6 +49,7 @@ EXPORTED = (
     "nvfp4_ggemm_run_noalloc",
     "nvfp4_ggemm_schedule",
     "nvfp4_ggemm_plan_shapes",
+    "nvfp4_ggemm_run_strided",
 )
 
 
@@ -140,6 +141,8 @@ def lib() -> ctypes.CDLL:
     L.nvfp4_ggemm_schedule.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    L.nvfp4_ggemm_run_strided.restype = ctypes.c_int
+    L.nvfp4_ggemm_run_strided.argtypes = [_VP, _VPP, _VPP, _VPP, _VPP, _VPP, ctypes.POINTER(ctypes.c_int32), _VP]
     L.nvfp4_ggemm_plan_shapes.restype = ctypes.c_int
     L.nvfp4_ggemm_plan_shapes.argtypes = [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
@@ -220,6 +223,12 @@ def nvfp4_ggemm_plan(device: int, M: Sequence[int], N, K,
 def nvfp4_ggemm_run(plan: int, A, B, SFA, SFB, C, stream=None) -> int:
     return lib().nvfp4_ggemm_run(plan, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB),
                                  _ptr_array(C), _stream(stream))
+
+
+def nvfp4_ggemm_run_strided(plan: int, A, B, SFA, SFB, C, ldc: Sequence[int], stream=None) -> int:
+    """nvfp4_ggemm_run with a row stride (fp16 elements) for every C[g]."""
+    return lib().nvfp4_ggemm_run_strided(plan, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB),
+                                         _ptr_array(C), _i32_array(ldc), _stream(stream))
 
 
 def nvfp4_ggemm_run_host(plan: int, A, B, SFA, SFB, C, stream=None) -> int:
@@ -338,6 +347,11 @@ class GroupedGemm:
         st = nvfp4_ggemm_run(self.handle, A, B, SFA, SFB, C, stream)
         if st != NVFP4_OK:
             raise Nvfp4Error(st, "nvfp4_ggemm_run")
+
+    def run_strided(self, A, B, SFA, SFB, C, ldc, stream=None) -> None:
+        st = nvfp4_ggemm_run_strided(self.handle, A, B, SFA, SFB, C, ldc, stream)
+        if st != NVFP4_OK:
+            raise Nvfp4Error(st, "nvfp4_ggemm_run_strided")
 
     def run_host(self, A, B, SFA, SFB, C, stream=None) -> None:
         st = nvfp4_ggemm_run_host(self.handle, A, B, SFA, SFB, C, stream)

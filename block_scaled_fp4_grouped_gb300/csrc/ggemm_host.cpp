@@ -253,6 +253,7 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
     d.N = N;
     d.k_tiles = K / kTileK;
     d.n_chunks = ceil_div(N, kChunkN);
+    d.ldc = N;
     d.C = static_cast<uint16_t *>(C);
     bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kBoxRows,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -360,7 +361,8 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
 }
 
 bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *const *A, const void *const *B,
-                const void *const *SFA, const void *const *SFB, void *const *C, bool force_sfb, int *njobs_out)
+                const void *const *SFA, const void *const *SFB, void *const *C, const int32_t *ldc, bool force_sfb,
+                int *njobs_out)
 {
     std::memset(tab, 0, p->table_bytes);
     auto *groups = reinterpret_cast<GroupDesc *>(tab);
@@ -387,6 +389,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         }
         if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->var.max_n)) return false;
         d.chunk_begin = p->chunk_prefix[g];
+        if (ldc) d.ldc = ldc[g];
     }
     if (p->relayout() && (force_sfb || !p->opt.cache_b_scales)) {
         for (int g = 0; g < p->G; ++g) {
@@ -429,13 +432,17 @@ nvfp4_status_t check_group_ptrs(nvfp4_ggemm_plan_s *p, const void *const *A, con
 }
 
 nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const void *const *B,
-                          const void *const *SFA, const void *const *SFB, void *const *C, cudaStream_t stream,
-                          bool force_sfb)
+                          const void *const *SFA, const void *const *SFB, void *const *C, const int32_t *ldc,
+                          cudaStream_t stream, bool force_sfb)
 {
     const bool sfb_cached = p->relayout() && p->opt.cache_b_scales && !force_sfb;
     if (sfb_cached && !p->b_prepared) return NVFP4_ERR_NOT_PREPARED;
     nvfp4_status_t st = check_group_ptrs(p, A, B, SFA, SFB, C, !sfb_cached);
     if (st != NVFP4_OK) return st;
+    if (ldc) {
+        for (int g = 0; g < p->G; ++g)
+            if (p->M[g] > 0 && (ldc[g] < p->N[g] || ldc[g] % 8 != 0)) return NVFP4_ERR_INVALID_ARG;
+    }
     if (p->total_chunks == 0) return NVFP4_OK;
 
     std::vector<const void *> key;
@@ -447,6 +454,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         key.push_back(on ? SFA[g] : nullptr);
         key.push_back(on && !sfb_cached ? SFB[g] : nullptr);
         key.push_back(on ? C[g] : nullptr);
+        key.push_back(reinterpret_cast<const void *>(static_cast<uintptr_t>(on && ldc ? ldc[g] : 0)));
     }
     key.push_back(reinterpret_cast<const void *>(static_cast<uintptr_t>(force_sfb ? 1 : 0)));
 
@@ -456,7 +464,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         Slot &s = p->slots[slot];
         if (s.used && cudaEventSynchronize(s.ev) != cudaSuccess) return NVFP4_ERR_CUDA;
         int njobs = 0;
-        if (!fill_table(p, s.h_table, s.d_table, A, B, SFA, SFB, C, force_sfb, &njobs)) return NVFP4_ERR_CUDA;
+        if (!fill_table(p, s.h_table, s.d_table, A, B, SFA, SFB, C, ldc, force_sfb, &njobs)) return NVFP4_ERR_CUDA;
         if (cudaMemcpyAsync(s.d_table, s.h_table, p->table_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         s.key = key;
@@ -672,7 +680,19 @@ nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *const *A, co
     if (!plan) return NVFP4_ERR_INVALID_ARG;
     DeviceGuard guard(plan->device);
     if (!guard.ok) return NVFP4_ERR_CUDA;
-    nvfp4_status_t st = run_device(plan, A, B, SFA, SFB, C, static_cast<cudaStream_t>(stream), false);
+    nvfp4_status_t st = run_device(plan, A, B, SFA, SFB, C, nullptr, static_cast<cudaStream_t>(stream), false);
+    if (st == NVFP4_ERR_CUDA) cudaGetLastError();
+    return st;
+}
+
+nvfp4_status_t nvfp4_ggemm_run_strided(nvfp4_ggemm_plan_t plan, const void *const *A, const void *const *B,
+                                       const void *const *SFA, const void *const *SFB, void *const *C,
+                                       const int32_t *ldc, void *stream)
+{
+    if (!plan || !ldc) return NVFP4_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    nvfp4_status_t st = run_device(plan, A, B, SFA, SFB, C, ldc, static_cast<cudaStream_t>(stream), false);
     if (st == NVFP4_ERR_CUDA) cudaGetLastError();
     return st;
 }
@@ -733,7 +753,7 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
             return NVFP4_ERR_CUDA;
         }
     }
-    nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), s, true);
+    nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true);
     if (st != NVFP4_OK) {
         cudaGetLastError();
         return st;

@@ -50,7 +50,7 @@ struct alignas(128) GroupDesc {
     CUtensorMap tmSFBw;    // raw SFB_g [N_g][K_g/16];  box 32 B x wide rows  (raw-scale path)
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
     const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
-    uint16_t *C;               // C_g fp16 [M_g][N_g]
+    uint16_t *C;               // C_g fp16 [M_g][ldc], columns [0, N_g) written
     int32_t M;
     int32_t m_tiles;      // ceil(M / 128)
     int32_t m_pairs;      // ceil(m_tiles / 2): passes over B
@@ -59,6 +59,8 @@ struct alignas(128) GroupDesc {
     int32_t N;            // N_g
     int32_t k_tiles;      // K_g / 256
     int32_t n_chunks;     // ceil(N_g / 32)
+    int32_t ldc;          // row stride of C_g in elements (>= N_g, a multiple of 8)
+    int32_t pad[3];
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 

@@ -801,6 +801,7 @@ struct Roles {
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
             const int N = gd->N;
+            const int ldc = gd->ldc;
             if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
             tc_fence_after_sync();
             // columns [n0, n0 + 32 * nblk) hold live data; this warp takes blocks
@@ -808,14 +809,14 @@ struct Roles {
             // while the current one is converted and stored
             const int nblk = (min(t.ncols, N - t.n0) + 31) / 32;
             const int mine = (nblk - h + 1) / 2;
-            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (N % 16 == 0);
+            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (N % 16 == 0) && (ldc % 16 == 0);
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
                 if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
                 const int row = row0 + lane;
                 const bool live = row < t.M;
-                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)N;
+                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)ldc;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];

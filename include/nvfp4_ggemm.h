@@ -155,6 +155,19 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *co
                                void *stream);
 
 /*
+ * nvfp4_ggemm_run with a row stride for every C_g: ldc is a host array of G
+ * strides in fp16 elements, each >= N_g and a multiple of 8 (16-byte rows);
+ * row m of C_g starts at C[g] + m * ldc[g], and columns N_g .. ldc[g]-1 are
+ * not written. This covers output buffers that are column slices of a wider
+ * matrix (the strided C of submission 498317). Returns NVFP4_ERR_INVALID_ARG
+ * for a bad stride before anything is enqueued; otherwise as nvfp4_ggemm_run.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_run_strided(nvfp4_ggemm_plan_t plan, const void *const *A,
+                                       const void *const *B, const void *const *SFA,
+                                       const void *const *SFB, void *const *C, const int32_t *ldc,
+                                       void *stream);
+
+/*
  * The same operation on HOST buffers: copies every input to plan-owned
  * device buffers (allocated on the first call), runs, and copies C back,
  * all on `stream`; returns after the stream has drained. Host buffers should

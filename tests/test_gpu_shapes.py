@@ -115,3 +115,31 @@ def test_uniform_call_equals_per_group_call_bitwise():
     uniform = run_gpu(prob)
     for g in range(prob.G):
         assert np.array_equal(per_group[g].view(np.uint16), uniform[g].view(np.uint16))
+
+
+def test_strided_c_writes_only_its_columns():
+    """nvfp4_ggemm_run_strided: each C_g is a column slice of a wider fp16
+    matrix (row stride ldc_g > N_g). The slice must equal the dense result
+    bit for bit, and the columns around it must keep their sentinel."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import run_gpu
+    prob = synth.make_problem("custom", seed=800, M=[150, 0, 300, 40], N=328, K=1024)
+    dense = run_gpu(prob)
+    A, B, SFA, SFB = to_device(prob.A), to_device(prob.B), to_device(prob.SFA), to_device(prob.SFB)
+    pads = [(16, 40), (8, 8), (0, 24), (64, 0)]  # columns before / after each slice
+    wide = [torch.full((m, lo + prob.N + hi), -7.0, dtype=torch.float16, device="cuda")
+            for m, (lo, hi) in zip(prob.M, pads)]
+    C = [w[:, lo:lo + prob.N] for w, (lo, _) in zip(wide, pads)]
+    ldc = [w.shape[1] for w in wide]
+    with nb.GroupedGemm(prob.M, prob.N, prob.K) as gg:
+        gg.run_strided(A, B, SFA, SFB, C, ldc)
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+        with pytest.raises(nb.Nvfp4Error):
+            gg.run_strided(A, B, SFA, SFB, C, [prob.N - 8] + ldc[1:])  # stride below N
+    torch.cuda.synchronize()
+    for g, (m, (lo, hi)) in enumerate(zip(prob.M, pads)):
+        w = wide[g].cpu().numpy()
+        assert np.array_equal(w[:, lo:lo + prob.N].view(np.uint16), dense[g].view(np.uint16))
+        assert (w[:, :lo] == -7.0).all() and (w[:, lo + prob.N:] == -7.0).all()
