@@ -79,6 +79,7 @@ class nvfp4_ggemm_plan_info_t(ctypes.Structure):
         ("sm_count", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
         ("kernels_per_run", ctypes.c_int32),
+        ("sf_path", ctypes.c_int32),
     ]
 
 
@@ -353,6 +354,11 @@ class GroupedGemm:
         if st != NVFP4_OK:
             raise Nvfp4Error(st, "nvfp4_ggemm_run_strided")
 
+    def bind(self, A, B, SFA, SFB, C, ldc: Optional[Sequence[int]] = None) -> "BoundCall":
+        """Marshal one set of per-group buffers once, for repeated calls on
+        them (the per-call cost is then one C call)."""
+        return BoundCall(self, A, B, SFA, SFB, C, ldc)
+
     def run_host(self, A, B, SFA, SFB, C, stream=None) -> None:
         st = nvfp4_ggemm_run_host(self.handle, A, B, SFA, SFB, C, stream)
         if st != NVFP4_OK:
@@ -382,3 +388,26 @@ class GroupedGemm:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class BoundCall:
+    """nvfp4_ggemm_run (or _run_strided) on one fixed set of device buffers:
+    the pointer arrays are built once and the tensors are kept alive for as
+    long as this object is."""
+
+    def __init__(self, gemm: GroupedGemm, A, B, SFA, SFB, C, ldc=None):
+        self.gemm = gemm
+        self._keep = (A, B, SFA, SFB, C)
+        self._args = (_ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C))
+        self._ldc = _i32_array(ldc) if ldc is not None else None
+
+    def __call__(self, stream=None) -> None:
+        L = lib()
+        if self._ldc is None:
+            st = L.nvfp4_ggemm_run(self.gemm.handle, *self._args, _stream(stream))
+            name = "nvfp4_ggemm_run"
+        else:
+            st = L.nvfp4_ggemm_run_strided(self.gemm.handle, *self._args, self._ldc, _stream(stream))
+            name = "nvfp4_ggemm_run_strided"
+        if st != NVFP4_OK:
+            raise Nvfp4Error(st, name)

@@ -62,11 +62,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Per-group N and K limits: 16-byte C rows, whole 256-k pipeline stages.
+// Per-group N and K limits: 16-byte C rows; whole 64-k MMA slices (a last
+// 256-k stage may be partial). Raw scale rows are 16-byte TMA rows only when
+// K % 256 == 0; plans with other K re-lay the scales out first.
 inline bool shape_ok(int32_t N, int32_t K)
 {
-    return N >= 8 && N <= kMaxN && N % 8 == 0 && K >= 256 && K <= kMaxK && K % 256 == 0;
+    return N >= 8 && N <= kMaxN && N % 8 == 0 && K >= 64 && K <= kMaxK && K % 64 == 0;
 }
+
+inline bool raw_tma_ok(int32_t K) { return K % 256 == 0; }
 
 uint64_t atom_bytes(int64_t rows, int64_t K)
 {
@@ -236,7 +240,7 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
         out[c].begin = r.begin;
         out[c].g_base = r.g_base;
         out[c].rows = cta_pack_rows(sh.M, sh.k_tiles);
-        out[c].packed = cta_pack(r.g, r.max_chunks, r.max_rows, sh.n_chunks);
+        out[c].packed = cta_pack(r.g, std::max(r.max_chunks, 1), std::max(r.max_rows, 1), sh.k_last, sh.n_chunks);
     }
     out[grid] = CtaStart{total_chunks, 0, 0, 0};
 }
@@ -251,7 +255,8 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
     d.m_pairs = ceil_div(d.m_tiles, kRowTilesPerUnit);
     d.b_keep = d.m_pairs > 1 ? 1 : 0;
     d.N = N;
-    d.k_tiles = K / kTileK;
+    d.k_tiles = k_tiles_of(K);
+    d.k_last = k_last_of(K);
     d.n_chunks = ceil_div(N, kChunkN);
     d.ldc = N;
     d.C = static_cast<uint16_t *>(C);
@@ -377,7 +382,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         d.m_pairs = p->m_pairs[g];
         d.chunk_begin = p->chunk_prefix[g];
         if (p->M[g] == 0) continue;
-        const int N = p->N[g], K = p->K[g], pieces = K / 256;
+        const int N = p->N[g], K = p->K[g], pieces = k_tiles_of(K);
         const void *sfa = SFA[g];
         const void *sfb = SFB ? SFB[g] : nullptr;
         if (p->relayout()) {
@@ -396,7 +401,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
             if (p->M[g] == 0) continue;
             const int N = p->N[g], K = p->K[g];
             jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], N, K, items, 0};
-            items += ceil_div(N, 128) * (K / 256);
+            items += ceil_div(N, 128) * k_tiles_of(K);
             ++njobs;
         }
     }
@@ -410,7 +415,7 @@ int relayout_items(nvfp4_ggemm_plan_s *p, bool with_sfb)
     int items = 0;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
-        const int pieces = p->K[g] / 256;
+        const int pieces = k_tiles_of(p->K[g]);
         items += ceil_div(p->M[g], 128) * pieces;
         if (with_sfb) items += ceil_div(p->N[g], 128) * pieces;
     }
@@ -533,7 +538,7 @@ nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int3
     for (int g = 0; g < num_groups; ++g) {
         if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
         if (!shape_ok(N[g], K[g])) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-        shapes[g] = GroupShape{ceil_div(M[g], kTileM), ceil_div(N[g], kChunkN), K[g] / kTileK, M[g]};
+        shapes[g] = group_shape(M[g], N[g], K[g]);
         total += (long)ceil_div(shapes[g].m_tiles, kRowTilesPerUnit) * shapes[g].n_chunks;
     }
     if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -567,6 +572,19 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     nvfp4_ggemm_options_t opt;
     nvfp4_status_t st = validate_options(opt_in, &opt);
     if (st != NVFP4_OK) return st;
+    // Raw scale rows of K_g / 16 bytes are TMA rows only when K_g % 256 == 0;
+    // otherwise the plan re-lays the scales out (its own kernel) and runs the
+    // atom-layout GEMM. Explicit ring depths without an atom-layout kernel
+    // fall back to that kernel's defaults.
+    if (opt.sf_layout == NVFP4_SF_RAW && opt.sf_path == NVFP4_SF_FUSED) {
+        for (int g = 0; g < num_groups; ++g) {
+            if (raw_tma_ok(K[g])) continue;
+            opt.sf_path = NVFP4_SF_RELAYOUT;
+            if (ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, false) < 0)
+                opt.b_stages = opt.a_stages = 0;
+            break;
+        }
+    }
 
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
@@ -615,7 +633,7 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     for (int g = 0; g < num_groups; ++g) {
         p->m_tiles[g] = ceil_div(M[g], kTileM);
         p->m_pairs[g] = ceil_div(p->m_tiles[g], kRowTilesPerUnit);
-        p->shapes[g] = GroupShape{p->m_tiles[g], ceil_div(N[g], kChunkN), K[g] / kTileK, M[g]};
+        p->shapes[g] = group_shape(M[g], N[g], K[g]);
         p->chunk_prefix[g] = (int32_t)total;
         total += (long)p->m_pairs[g] * p->shapes[g].n_chunks;
     }
@@ -792,7 +810,7 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
         if (p->M[g] == 0) continue;
         p->h_prep_jobs[nj++] =
             RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N[g], p->K[g], items, 0};
-        items += ceil_div(p->N[g], 128) * (p->K[g] / 256);
+        items += ceil_div(p->N[g], 128) * k_tiles_of(p->K[g]);
     }
     if (nj > 0) {
         if (cudaMemcpyAsync(p->d_prep_jobs, p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)nj, cudaMemcpyHostToDevice,
@@ -849,7 +867,7 @@ nvfp4_status_t nvfp4_ggemm_destroy(nvfp4_ggemm_plan_t plan)
 nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_t K, void *stream)
 {
     if (!in || !out || rows < 1 || rows > (1 << 24)) return NVFP4_ERR_INVALID_ARG;
-    if (K < 256 || K > kMaxK || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (K < 64 || K > kMaxK || K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(in) || !aligned16(out)) return NVFP4_ERR_ALIGNMENT;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -861,7 +879,7 @@ nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_
     rp.jobs = nullptr;
     rp.single = RelayoutJob{static_cast<const uint8_t *>(in), static_cast<uint8_t *>(out), rows, K, 0, 0};
     rp.njobs = 1;
-    rp.total_items = ceil_div(rows, 128) * (K / 256);
+    rp.total_items = ceil_div(rows, 128) * k_tiles_of(K);
     if (relayout_launch(rp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
@@ -886,6 +904,7 @@ nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_i
     info->sm_count = plan->sm_count;
     info->smem_bytes = ggemm_smem_bytes(plan->variant);
     info->kernels_per_run = plan->total_chunks == 0 ? 0 : (plan->relayout() ? 2 : 1);
+    info->sf_path = plan->relayout() ? NVFP4_SF_RELAYOUT : NVFP4_SF_FUSED;
     return NVFP4_OK;
 }
 

@@ -57,10 +57,11 @@ struct alignas(128) GroupDesc {
     int32_t chunk_begin;  // first scheduling chunk of this group (prefix sum)
     int32_t b_keep;       // 1: B is read by more than one pair of row tiles (keep it in L2)
     int32_t N;            // N_g
-    int32_t k_tiles;      // K_g / 256
+    int32_t k_tiles;      // ceil(K_g / 256)
     int32_t n_chunks;     // ceil(N_g / 32)
     int32_t ldc;          // row stride of C_g in elements (>= N_g, a multiple of 8)
-    int32_t pad[3];
+    int32_t k_last;       // 64-k slices in the last k tile (1..4; 4 when K_g % 256 == 0)
+    int32_t pad[2];
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
@@ -80,9 +81,18 @@ static_assert(sizeof(CtaRange) == 32, "one sector per CTA");
 struct GroupShape {
     int32_t m_tiles;   // ceil(M_g / 128)
     int32_t n_chunks;  // ceil(N_g / 32)
-    int32_t k_tiles;   // K_g / 256
+    int32_t k_tiles;   // ceil(K_g / 256)
     int32_t M;
+    int32_t k_last;    // 64-k slices in the last k tile (1..4)
 };
+
+// k tiles of 256 and 64-k slices in the last one, for K a multiple of 64.
+inline int k_tiles_of(int K) { return (K + 255) / 256; }
+inline int k_last_of(int K) { return (K / 64 - 1) % 4 + 1; }
+inline GroupShape group_shape(int M, int N, int K)
+{
+    return GroupShape{(M + 127) / 128, (N + 31) / 32, k_tiles_of(K), M, k_last_of(K)};
+}
 
 // What a CTA needs to start, packed into 16 bytes of the kernel parameters
 // so that no role reads memory before its first load. CTA c's range ends
@@ -90,9 +100,9 @@ struct GroupShape {
 struct CtaStart {
     int32_t begin;    // first chunk
     int32_t g_base;   // chunk_prefix[g]
-    uint32_t rows;    // group g: M (bits 0-20) | K / 256 (bits 21-31)
-    uint32_t packed;  // g (bits 0-9) | widest tile in chunks (10-13) | most row tiles (14-15) |
-                      // group g's ceil(N / 32) (16-31)
+    uint32_t rows;    // group g: M (bits 0-20) | ceil(K / 256) (bits 21-31)
+    uint32_t packed;  // g (bits 0-9) | widest tile in chunks - 1 (10-12) | most row tiles - 1 (13) |
+                      // group g's 64-k slices in its last k tile - 1 (14-15) | group g's ceil(N / 32) (16-31)
 };
 static_assert(sizeof(CtaStart) == 16, "packed start record");
 
@@ -103,16 +113,19 @@ static_assert(sizeof(CtaStart) == 16, "packed start record");
 #define NVFP4_HD inline
 #endif
 NVFP4_HD uint32_t cta_pack_rows(int M, int k_tiles) { return (uint32_t)(M & 0x1FFFFF) | ((uint32_t)(k_tiles & 0x7FF) << 21); }
-NVFP4_HD uint32_t cta_pack(int g, int max_chunks, int max_rows, int n_chunks)
+// max_chunks 1..8, max_rows 1..2, k_last 1..4 (a CTA with no tile packs 1s)
+NVFP4_HD uint32_t cta_pack(int g, int max_chunks, int max_rows, int k_last, int n_chunks)
 {
-    return (uint32_t)(g & 0x3FF) | ((uint32_t)(max_chunks & 0xF) << 10) | ((uint32_t)(max_rows & 0x3) << 14) |
+    return (uint32_t)(g & 0x3FF) | ((uint32_t)((max_chunks - 1) & 0x7) << 10) |
+           ((uint32_t)((max_rows - 1) & 0x1) << 13) | ((uint32_t)((k_last - 1) & 0x3) << 14) |
            ((uint32_t)(n_chunks & 0xFFFF) << 16);
 }
 NVFP4_HD int cta_rows_m(uint32_t rows) { return (int)(rows & 0x1FFFFFu); }
 NVFP4_HD int cta_rows_ktiles(uint32_t rows) { return (int)(rows >> 21); }
 NVFP4_HD int cta_group(uint32_t packed) { return (int)(packed & 0x3FFu); }
-NVFP4_HD int cta_max_chunks(uint32_t packed) { return (int)((packed >> 10) & 0xFu); }
-NVFP4_HD int cta_max_rows(uint32_t packed) { return (int)((packed >> 14) & 0x3u); }
+NVFP4_HD int cta_max_chunks(uint32_t packed) { return (int)((packed >> 10) & 0x7u) + 1; }
+NVFP4_HD int cta_max_rows(uint32_t packed) { return (int)((packed >> 13) & 0x1u) + 1; }
+NVFP4_HD int cta_k_last(uint32_t packed) { return (int)((packed >> 14) & 0x3u) + 1; }
 NVFP4_HD int cta_n_chunks(uint32_t packed) { return (int)(packed >> 16); }
 
 // Work decomposition: group g owns m_pairs_g * ceil(N_g/32) chunks (32
@@ -147,8 +160,8 @@ struct RelayoutJob {
     const uint8_t *src;  // raw [rows][K/16]
     uint8_t *dst;        // atoms
     int32_t rows;
-    int32_t K;
-    int32_t item_begin;  // prefix over jobs of ceil(rows/128) * (K/256)
+    int32_t K;           // a multiple of 64
+    int32_t item_begin;  // prefix over jobs of ceil(rows/128) * ceil(K/256)
     int32_t pad;
 };
 

@@ -132,7 +132,8 @@ struct Unit {
     bool keep;   // the group has more pairs of row tiles, which read B again
     int M;       // rows of the group
     int N;       // columns of the group
-    int k_tiles; // K of the group / 256
+    int k_tiles; // ceil(K of the group / 256)
+    int k_last;  // 64-k slices in the last k tile (1..4)
 };
 
 // Walks this CTA's contiguous range of chunks as tiles.
@@ -141,7 +142,7 @@ struct Walker {
     // the part of the range inside the current pair (plen chunks from ch0)
     // is cut into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
-    int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
+    int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_klast, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
@@ -153,6 +154,7 @@ struct Walker {
         g_rows = cta_rows_m(r.rows);
         g_ktiles = cta_rows_ktiles(r.rows);
         g_chunks = cta_n_chunks(r.packed);
+        g_klast = cta_k_last(r.packed);
         g_tiles = (g_rows + kTileM - 1) / kTileM;
     }
 
@@ -169,6 +171,7 @@ struct Walker {
                 g_tiles = gd.m_tiles;
                 g_chunks = gd.n_chunks;
                 g_ktiles = gd.k_tiles;
+                g_klast = gd.k_last;
                 g_cols = gd.N;
             }
             const int local = pos - g_base;
@@ -193,6 +196,7 @@ struct Walker {
         t.keep = g_tiles > kRowTilesPerUnit;
         t.M = g_rows;
         t.k_tiles = g_ktiles;
+        t.k_last = g_klast;
         // N itself is only in the table; a bound that never cuts a live column
         // (the chunks cover N) serves until a role reads it
         t.N = g_cols >= 0 ? g_cols : g_chunks * kChunkN;
@@ -408,6 +412,12 @@ struct Roles {
     // load, so the small, scattered A and scale reads of the first stage do
     // not queue behind every CTA's burst of B stages at kernel start.
     __device__ __forceinline__ uint32_t first_issued() const { return bar(kBarDone + kDoneRing + 5); }
+    // The group whose tensor maps the kernel prologue has fenced (-1: none).
+    __device__ __forceinline__ int first_group() const
+    {
+        const int g = cta_group(p.cta[blockIdx.x].packed);
+        return g < p.G ? g : -1;
+    }
 
     // Wait until the MMAs of stage j (< 0: none) have completed.
     __device__ __forceinline__ bool wait_done(int j, uint32_t site) const
@@ -453,7 +463,7 @@ struct Roles {
         const uint64_t pol_keep = policy_evict_normal();    // read again by the group's other row tiles
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1, loads = 0, seq = 0;
+        int last_g = first_group(), loads = 0, seq = 0;
         bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
         Walker wk(p);
         Unit t;
@@ -509,7 +519,7 @@ struct Roles {
         const uint64_t pol = policy_evict_last();  // A tiles are re-read by every column tile
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1, seq = 0;
+        int last_g = first_group(), seq = 0;
         bool signalled = false;
         bool ok = true;
         Walker wk(p);
@@ -561,7 +571,7 @@ struct Roles {
         const uint64_t pol = policy_evict_normal();
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = -1;
+        int last_g = first_group();
         bool signalled = false;
         bool ok = true;
 
@@ -581,12 +591,13 @@ struct Roles {
             sfb_blocks(t.n0, t.ncols, t.N, b0, nblk);
             int live_boxes[kRowTilesPerUnit];
             const int aboxes = row_boxes(t, t.M, live_boxes);
-            const size_t katoms = (size_t)t.k_tiles * 4;                 // 64-k atoms per 128-row block
-            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;  // scale stages of this tile
-            const uint32_t bytes =
-                RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
-                    : (uint32_t)t.mtu * kSfTileBytes + (uint32_t)nblk * kSfTileBytes;
+            const size_t katoms = (size_t)(t.k_tiles - 1) * 4 + t.k_last;  // 64-k atoms per 128-row block
+            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;          // scale stages of this tile
             for (int ks = 0; ks < s_tiles; ++ks) {
+                // atom layout: the atoms of k tile ks (fewer in a partial last one)
+                const uint32_t piece = ks + 1 == s_tiles ? (uint32_t)t.k_last * kSfAtomBytes : kSfTileBytes;
+                const uint32_t bytes = RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
+                                           : (uint32_t)(t.mtu + nblk) * piece;
                 if (!wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
                     ok = false;
                     break;
@@ -615,11 +626,11 @@ struct Roles {
                         if (mt < t.mtu)
                             bulk_load(st + mt * kSfTileBytes,
                                       gd->sfa_atoms + ((size_t)(t.mt0 + mt) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                      kSfTileBytes, fb, pol);
+                                      piece, fb, pol);
                     for (int b = 0; b < nblk; ++b)
                         bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
                                   gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                  kSfTileBytes, fb, pol);
+                                  piece, fb, pol);
                 }
                 if (!signalled) {
                     mbar_arrive(first_issued());
@@ -763,12 +774,14 @@ struct Roles {
                 const uint32_t sa = a_stage(ra.stage);
                 const uint32_t sb = b_stage(rb.stage);
                 const uint32_t sf = tmem + (uint32_t)(C::kSfBase + rt.stage * kSfCols);
+                // a last k tile of K % 256 != 0 holds fewer live 64-k slices
+                const int slices = kt + 1 == t.k_tiles ? t.k_last : 4;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                        if (mt < t.mtu)
+                        if (mt < t.mtu && kk < slices)
                             tc_mma_nvf4(d + (uint32_t)(mt * C::kPairN), desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32),
                                         bdesc, idesc, sf + mt * 16 + kk * 4, sf + 32 + kk * 8,
                                         (kt | kk) != 0 ? 1u : 0u);
@@ -855,12 +868,19 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
 
     if (threadIdx.x == 0) r.init_barriers();
     if (warp == kWarpEpi0 && lane < 6) {
-        // start fetching the tensor maps of this CTA's first group while the
-        // barriers and TMEM are set up
+        // The tensor maps of this CTA's first group: one lane per map takes
+        // the tensormap-proxy acquire fence (a round trip to memory each, so
+        // they run side by side here, under the barrier and TMEM set-up, not
+        // one after another in the producers) and starts fetching the map.
+        // The __syncthreads below orders these fences before every
+        // producer's first TMA; the producers fence later groups themselves.
         const int g = cta_group(p.cta[blockIdx.x].packed);
         const GroupDesc *gd = p.groups + g;
         // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
-        if (g < p.G && (RAW || lane < 3)) prefetch_tensormap(&gd->tmA + lane);
+        if (g < p.G && (RAW || lane < 3)) {
+            fence_tensormap_acquire(&gd->tmA + lane);
+            prefetch_tensormap(&gd->tmA + lane);
+        }
     }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
@@ -916,24 +936,37 @@ __global__ void __launch_bounds__(256) sf_relayout_kernel(const __grid_constant_
             }
             job = p.jobs[lo];
         }
-        const int pieces = job.K / 256;
-        const int katoms = job.K / 64;
+        const int pieces = (job.K + 255) / 256;
+        const int katoms = job.K / 64;  // K is a multiple of 64
         const size_t row_bytes = (size_t)(job.K / 16);
         const int l = item - job.item_begin;
         const int rb = l / pieces;
         const int pc = l % pieces;
+        const int live = min(4, katoms - 4 * pc);  // atoms (4-byte words of a row) in this piece
         uint4 w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int r = rb * 128 + 32 * j + lane;
-            w[j] = (r < job.rows) ? __ldg(reinterpret_cast<const uint4 *>(job.src + (size_t)r * row_bytes + pc * 16))
-                                  : make_uint4(0u, 0u, 0u, 0u);
+            const uint8_t *src = job.src + (size_t)r * row_bytes + pc * 16;
+            if (r >= job.rows) {
+                w[j] = make_uint4(0u, 0u, 0u, 0u);
+            } else if (row_bytes % 16 == 0) {
+                w[j] = __ldg(reinterpret_cast<const uint4 *>(src));
+            } else {
+                // rows of K/16 bytes, a multiple of 4: 4-byte aligned words only
+                const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+                w[j].x = __ldg(s32);
+                w[j].y = live > 1 ? __ldg(s32 + 1) : 0u;
+                w[j].z = live > 2 ? __ldg(s32 + 2) : 0u;
+                w[j].w = live > 3 ? __ldg(s32 + 3) : 0u;
+            }
         }
         uint8_t *dst = job.dst + ((size_t)rb * katoms + (size_t)pc * 4) * kSfAtomBytes + 16 * lane;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4 *>(dst + c * kSfAtomBytes) =
-                make_uint4(word_at(w[0], c), word_at(w[1], c), word_at(w[2], c), word_at(w[3], c));
+            if (c < live)
+                *reinterpret_cast<uint4 *>(dst + c * kSfAtomBytes) =
+                    make_uint4(word_at(w[0], c), word_at(w[1], c), word_at(w[2], c), word_at(w[3], c));
     }
 }
 

@@ -119,7 +119,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
         d.M = M[g];
         d.m_tiles = ceil_div_i(M[g], kTileM);
         d.m_pairs = ceil_div_i(d.m_tiles, kRowTilesPerUnit);
-        shapes[g] = GroupShape{d.m_tiles, n_chunks, K / kTileK, M[g]};
+        shapes[g] = group_shape(M[g], N, K);
         d.chunk_begin = (int32_t)total;
         prefix[g] = (int32_t)total;
         total += (long)d.m_pairs * n_chunks;

@@ -27,11 +27,16 @@
  *   C[g]    M_g x N fp16, row-major (row stride N elements).
  *
  * Requirements (checked before anything is enqueued): 1 <= G <= 1024,
- * 0 <= M_g <= 2^20, 8 <= N <= 2^20 with N % 8 == 0 (16-byte C rows), 256 <= K
- * <= 2^18 with K % 256 == 0 (the kernel's k tile; the K % 256 rule is the one
- * the TMA helper of submission 498317 enforces), every pointer of a group
- * with M_g > 0 non-null and 16-byte aligned (the TMA rule). A group with
- * M_g == 0 is skipped and its pointers are not read.
+ * 0 <= M_g <= 2^20, 8 <= N <= 2^20 with N % 8 == 0 (16-byte C rows), 64 <= K
+ * <= 2^18 with K % 64 == 0 (one 64-k MMA slice; the kernel's k tile is 256
+ * and a last partial tile is read with the TMA's zero fill, as the kernel of
+ * submission 503584 counts its k tiles by a ceil-div of k), every pointer of
+ * a group with M_g > 0 non-null and 16-byte aligned (the TMA rule). A group
+ * with M_g == 0 is skipped and its pointers are not read. Raw scale rows (K/16 bytes) are rows
+ * the TMA can load only when K % 256 == 0 (the rule the TMA helper of
+ * submission 498317 enforces on K); a raw-scale plan with some K_g % 256 != 0
+ * therefore runs the NVFP4_SF_RELAYOUT path whatever sf_path asks
+ * (nvfp4_ggemm_plan_info reports it).
  *
  * Ownership: the caller owns every tensor and the host arrays of pointers;
  * the arrays are read during the call only. A plan owns its device problem
@@ -66,7 +71,7 @@ typedef enum {
     NVFP4_OK = 0,
     NVFP4_ERR_INVALID_ARG = 1,       /* null, negative or out-of-range argument */
     NVFP4_ERR_ALIGNMENT = 2,         /* a tensor pointer is not 16-byte aligned */
-    NVFP4_ERR_UNSUPPORTED_SHAPE = 3, /* K % 256 != 0, N % 8 != 0, size limits */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 3, /* K % 64 != 0, N % 8 != 0, size limits */
     NVFP4_ERR_UNSUPPORTED_DEVICE = 4,/* no device, or not compute capability 10.3 */
     NVFP4_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
     NVFP4_ERR_TIMEOUT = 6,           /* a device pipeline wait exceeded the timeout */
@@ -88,7 +93,8 @@ enum {
 typedef struct {
     uint32_t struct_size;     /* sizeof(nvfp4_ggemm_options_t) */
     int32_t sf_layout;        /* NVFP4_SF_RAW (default) or NVFP4_SF_ATOM */
-    int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only */
+    int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only
+                                 (FUSED needs every K_g % 256 == 0, else RELAYOUT is used) */
     int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
                                  nvfp4_ggemm_prepare_b_scales and run skips it */
     uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
@@ -134,7 +140,7 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, i
  * The same with per-group N_g and K_g (host arrays N[0..G-1], K[0..G-1]):
  * group g computes C_g[M_g, N_g] = sum over K_g of the block-scaled products
  * of A_g[M_g, K_g] and B_g[N_g, K_g], every size meeting the per-group rules
- * above (N_g % 8 == 0, K_g % 256 == 0). The pages' own interface takes one
+ * above (N_g % 8 == 0, K_g % 64 == 0). The pages' own interface takes one
  * (m, n, k) per group; nvfp4_ggemm_plan is this call with N_g = N and
  * K_g = K. Everything else (layouts per group, run, run_host, prepare,
  * status) is as for nvfp4_ggemm_plan.
@@ -207,7 +213,8 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_destroy(nvfp4_ggemm_plan_t plan);
  * sits at byte (r%32)*16 + ((r%128)/32)*4 + j%4 (the scale-factor atom of
  * the CuTe kernel of submission 402102, tiled as in the TMA issue code of
  * submission 498317). Rows past `rows` are written as zero. in and out are
- * device pointers, 16-byte aligned; K % 256 == 0; rows >= 1. Asynchronous.
+ * device pointers, 16-byte aligned; K % 64 == 0 (64 <= K <= 2^18); rows >= 1.
+ * Asynchronous.
  */
 NVFP4_API nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_t K, void *stream);
 
@@ -246,6 +253,8 @@ typedef struct {
     int32_t sm_count;
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t kernels_per_run; /* kernel launches enqueued by one run */
+    int32_t sf_path;       /* the scale path runs take: NVFP4_SF_FUSED, or NVFP4_SF_RELAYOUT (asked for,
+                              or forced by a raw-scale plan with some K_g % 256 != 0) */
 } nvfp4_ggemm_plan_info_t;
 
 NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info);

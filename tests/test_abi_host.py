@@ -59,8 +59,8 @@ def test_default_options(L):
     ([(1 << 20) + 1], 256, 256, nb.NVFP4_ERR_INVALID_ARG),       # M too large
     ([64], 260, 256, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),            # N % 8
     ([64], 0, 256, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),              # N too small
-    ([64], 256, 320, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),            # K % 256
-    ([64], 256, 128, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),            # K too small
+    ([64], 256, 352, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),            # K % 64
+    ([64], 256, 32, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),             # K too small
     ([64], 256, 1 << 19, nb.NVFP4_ERR_UNSUPPORTED_SHAPE),        # K too large
 ])
 def test_plan_rejects_bad_shapes(L, M, N, K, want):
@@ -95,7 +95,8 @@ def test_null_plan_calls(L):
 def test_relayout_argument_checks(L):
     assert nb.nvfp4_sf_relayout(0, 0, 128, 256) == nb.NVFP4_ERR_INVALID_ARG
     assert nb.nvfp4_sf_relayout(16, 32, 0, 256) == nb.NVFP4_ERR_INVALID_ARG
-    assert nb.nvfp4_sf_relayout(16, 32, 128, 320) == nb.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert nb.nvfp4_sf_relayout(16, 32, 128, 352) == nb.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert nb.nvfp4_sf_relayout(16, 32, 128, 0) == nb.NVFP4_ERR_UNSUPPORTED_SHAPE
     assert nb.nvfp4_sf_relayout(17, 32, 128, 256) == nb.NVFP4_ERR_ALIGNMENT
     assert nb.nvfp4_sf_relayout(16, 40, 128, 256) == nb.NVFP4_ERR_ALIGNMENT
 
@@ -106,6 +107,9 @@ def test_atom_bytes(L):
     assert nb.nvfp4_sf_atom_bytes(129, 7168) == 2 * 112 * 512
     assert nb.nvfp4_sf_atom_bytes(4096, 7168) == 32 * 112 * 512
     assert nb.nvfp4_sf_atom_bytes(5, 100) == 0
+    # K % 256 != 0: the atoms of the pages' layout, K/64 per 128-row block, unpadded
+    assert nb.nvfp4_sf_atom_bytes(130, 320) == 2 * 5 * 512
+    assert nb.nvfp4_sf_atom_bytes(1, 64) == 512
 
 
 def _has_gpu():

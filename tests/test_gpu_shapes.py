@@ -143,3 +143,86 @@ def test_strided_c_writes_only_its_columns():
         w = wide[g].cpu().numpy()
         assert np.array_equal(w[:, lo:lo + prob.N].view(np.uint16), dense[g].view(np.uint16))
         assert (w[:, :lo] == -7.0).all() and (w[:, lo + prob.N:] == -7.0).all()
+
+
+def test_bound_call_equals_run_bitwise():
+    """GroupedGemm.bind: pointer arrays built once, then repeated calls. Two
+    bound buffer sets on one plan (one dense, one strided) must each equal
+    the plain call bit for bit, called in alternation."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import run_gpu
+    prob = synth.make_problem("custom", seed=900, M=[96, 260, 0, 33], N=264, K=768)
+    dense = run_gpu(prob)
+    A, B, SFA, SFB = to_device(prob.A), to_device(prob.B), to_device(prob.SFA), to_device(prob.SFB)
+    C1 = [torch.full((m, prob.N), 3.0, dtype=torch.float16, device="cuda") for m in prob.M]
+    wide = [torch.full((m, prob.N + 24), -5.0, dtype=torch.float16, device="cuda") for m in prob.M]
+    C2 = [w[:, 8:8 + prob.N] for w in wide]
+    with nb.GroupedGemm(prob.M, prob.N, prob.K) as gg:
+        call1 = gg.bind(A, B, SFA, SFB, C1)
+        call2 = gg.bind(A, B, SFA, SFB, C2, ldc=[prob.N + 24] * prob.G)
+        for _ in range(3):
+            call1()
+            call2()
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+    torch.cuda.synchronize()
+    for g in range(prob.G):
+        assert np.array_equal(C1[g].cpu().numpy().view(np.uint16), dense[g].view(np.uint16))
+        w = wide[g].cpu().numpy()
+        assert np.array_equal(w[:, 8:8 + prob.N].view(np.uint16), dense[g].view(np.uint16))
+        assert (w[:, :8] == -5.0).all() and (w[:, 8 + prob.N:] == -5.0).all()
+
+
+SHAPES_K64 = [  # (M_g, N_g, K_g): most K_g are not multiples of 256
+    (200, 328, 320),
+    (64, 256, 64),
+    (130, 72, 832),
+    (0, 512, 192),
+    (257, 1000, 1088),
+    (17, 8, 128),
+    (96, 520, 256),
+    (33, 4096, 448),
+]
+
+
+@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "relayout", True),
+                                                ("atom", "fused", False)])
+def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
+    """K_g % 64 == 0 with a partial last 256-k tile: A and B past K_g come
+    from the TMA's zero fill, the last tile issues only its live 64-k MMA
+    slices and loads only its live scale atoms. A raw-scale plan runs the
+    re-layout path (raw scale rows are not 16-byte TMA rows) and says so."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    parts = [synth.make_problem("custom", seed=1000 + g, M=[m], N=n, K=k)
+             for g, (m, n, k) in enumerate(SHAPES_K64)]
+    with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts],
+                        sf_layout=layout, sf_path=path) as gg:
+        info = gg.info()
+        assert info.sf_path == (nb.NVFP4_SF_RELAYOUT if layout == "raw" else nb.NVFP4_SF_FUSED)
+        assert info.kernels_per_run == (2 if layout == "raw" else 1)
+    got = _run(parts, sf_layout=layout, sf_path=path, cache_b_scales=cached)
+    for g, p in enumerate(parts):
+        assert got[g].shape == (p.M[0], p.N)
+        if p.M[0] == 0:
+            continue
+        ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
+        assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
+        assert_close(got[g], ref, f"group {g} (M={p.M[0]}, N={p.N}, K={p.K})")
+
+
+def test_k_multiple_of_64_uniform_and_exact(O):
+    """One K for every group (nvfp4_ggemm_plan), K = 704 = 2 x 256 + 192,
+    with power-of-two scales of span 4 so that every fp32 partial sum is
+    exact: the GPU must equal the oracle bit for bit."""
+    from gpu_util import run_gpu
+    prob = synth.make_problem("custom", seed=1100, M=[140, 64, 0, 300], N=392, K=704)
+    rng = np.random.default_rng(1100)
+    for g in range(prob.G):
+        # E4M3 codes of 2^e, e in [-2, 1]: (e + 7) << 3
+        prob.SFA[g] = (((rng.integers(-2, 2, prob.SFA[g].shape) + 7) << 3)).astype(np.uint8)
+        prob.SFB[g] = (((rng.integers(-2, 2, prob.SFB[g].shape) + 7) << 3)).astype(np.uint8)
+    ref, _ = O.grouped(prob)
+    got = run_gpu(prob)
+    for g in range(prob.G):
+        assert np.array_equal(got[g].view(np.uint16), ref[g].view(np.uint16)), f"group {g}"

@@ -126,7 +126,7 @@ def test_bad_arguments(kw):
 def _check_shapes(M, N, K, tile_n, max_ctas):
     """Per-group N_g and K_g: the ranges partition the chunks (pairs of group g
     own ceil(N_g/32) chunks each); with no more pairs than CTAs every range
-    lies in one pair and the most k-stages any CTA needs (tiles x K_g/256) is
+    lies in one pair and the most k-stages any CTA needs (tiles x ceil(K_g/256)) is
     the smallest budget with which the pairs fit the grid."""
     st, cb = nb.nvfp4_ggemm_schedule(M, N, tile_n, max_ctas, K=K)
     assert st == nb.NVFP4_OK
@@ -137,7 +137,7 @@ def _check_shapes(M, N, K, tile_n, max_ctas):
         tiles = -(-m // 128)
         for t in range(0, tiles, 2):
             c = -(-n // 32)
-            segs.append((base, c, pair if tiles - t >= 2 else single, k // 256))
+            segs.append((base, c, pair if tiles - t >= 2 else single, -(-k // 256)))
             base += c
     total = base
     grid = len(cb) - 1
@@ -168,7 +168,7 @@ def test_random_per_group_shapes(tile_n):
         G = rng.randint(1, 10)
         M = [rng.choice([0, rng.randint(1, 600)]) for _ in range(G)]
         N = [8 * rng.randint(1, 700) for _ in range(G)]
-        K = [256 * rng.randint(1, 24) for _ in range(G)]
+        K = [rng.choice([256 * rng.randint(1, 24), 64 * rng.randint(1, 96)]) for _ in range(G)]
         _check_shapes(M, N, K, tile_n, rng.choice([1, 7, 64, 152]))
 
 
