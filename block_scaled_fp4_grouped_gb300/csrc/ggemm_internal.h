@@ -17,7 +17,8 @@ constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
 constexpr int kMaxCtas = 192;      // largest persistent grid (the CTA start records travel in the kernel parameters)
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
-constexpr int kBoxRows = 32;       // rows of the A and scale TMA boxes (partial row tiles load only live boxes)
+constexpr int kBoxRows = 128;      // rows of the A and raw SFA TMA boxes: one box per row tile; rows past
+                                   // M_g are the TMA's zero fill (the maps end at M_g), no memory traffic
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
 
 // Wait sites recorded in the error word (bits 8-15).
@@ -42,10 +43,10 @@ enum WaitSite : uint32_t {
 // M_g / N_g. Two B maps: boxes as wide as the kernel's widest tile for
 // full-width tiles, 32-row boxes for the rest.
 struct alignas(128) GroupDesc {
-    CUtensorMap tmA;       // A_g bytes [M_g][K_g/2];   box 128 B x 32 rows;  128-byte swizzle
+    CUtensorMap tmA;       // A_g bytes [M_g][K_g/2];   box 128 B x 128 rows; 128-byte swizzle
     CUtensorMap tmB32;     // B_g bytes [N_g][K_g/2];   box 128 B x 32 rows;  128-byte swizzle
     CUtensorMap tmBw;      // B_g bytes [N_g][K_g/2];   box 128 B x wide rows; 128-byte swizzle
-    CUtensorMap tmSFA;     // raw SFA_g [M_g][K_g/16];  box 32 B x 32 rows    (raw-scale path)
+    CUtensorMap tmSFA;     // raw SFA_g [M_g][K_g/16];  box 32 B x 128 rows   (raw-scale path)
     CUtensorMap tmSFB32;   // raw SFB_g [N_g][K_g/16];  box 32 B x 32 rows    (raw-scale path)
     CUtensorMap tmSFBw;    // raw SFB_g [N_g][K_g/16];  box 32 B x wide rows  (raw-scale path)
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)

@@ -6,9 +6,9 @@
 //               (128-byte swizzle) into the B ring. B is the operand streamed
 //               from HBM; a slot holds nothing else, so it is refilled as
 //               soon as its MMAs have read it.
-//   warp 6      A producer: the tile's one or two 128-row A tiles (only the
-//               32-row boxes that hold rows < M_g) into the A ring; A is
-//               small and re-read from L2.
+//   warp 6      A producer: the tile's one or two 128-row A tiles (one box
+//               each; rows past M_g are the TMA's zero fill) into the A
+//               ring; A is small and re-read from L2.
 //   warp 7      scale producer: the stage's A and B scales into a ring of NS
 //               small stages, running ahead of the operands.
 //   warps 8-11  scale writers: each turns a scale stage into the TMEM layout
@@ -103,10 +103,10 @@ struct Cfg {
     static constexpr int kOffARing = 0;
     static constexpr int kOffBRing = NA * kAStage;
     static constexpr int kOffSRing = kOffBRing + NB * kBStage;
-    static constexpr int kAccCols = kRowTilesPerUnit * kPairN;  // one accumulator: both row tiles
-    static_assert(MAXN <= kAccCols, "a one-row-tile unit uses the whole accumulator");
-    static constexpr int kNumAcc = (2 * kAccCols + 2 * kSfCols <= (int)kTmemCols) ? 2 : 1;
-    static constexpr int kSfBase = kNumAcc * kAccCols;
+    // accumulator columns: two halves of kPairN, one per row tile of a pair
+    static constexpr int kAccCols = kRowTilesPerUnit * kPairN;
+    static_assert(MAXN <= kAccCols, "a one-row-tile unit fits the accumulator columns");
+    static constexpr int kSfBase = kAccCols;
     static constexpr int kNT0 = ((int)kTmemCols - kSfBase) / kSfCols;
     static constexpr int kNT = kNT0 > 6 ? 6 : kNT0;  // TMEM scale buffers
     static constexpr int kOffBars = kOffSRing + NS * kSStage;
@@ -309,6 +309,28 @@ __device__ __forceinline__ void store_row_block(uint16_t *crow, int col0, int N,
     }
 }
 
+// The accumulator columns as two halves of kPairN columns, each with its own
+// full / empty barrier pair. A tile with one row tile at most kPairN columns
+// wide takes one half, the halves alternating, so that its MMAs run while
+// the epilogue drains the previous tile from the other half; any other tile
+// (two row tiles, or wider) takes both. The MMA thread and the epilogue walk
+// the same tiles and so make the same choices.
+struct AccTrack {
+    uint32_t parity = 0;  // bit h: phase parity of half h's barriers
+    int next = 0;         // the half a one-half tile takes
+    __device__ __forceinline__ uint32_t par(int h) const { return (parity >> h) & 1u; }
+    __device__ __forceinline__ void advance(int h0, bool both)
+    {
+        if (both) {
+            parity ^= 3u;
+            next = 0;
+        } else {
+            parity ^= 1u << h0;
+            next = h0 ^ 1;
+        }
+    }
+};
+
 // A ring of mbarrier-guarded stages: position (stage, phase) advanced in step.
 struct RingPos {
     int stage = 0;
@@ -338,8 +360,8 @@ __device__ __forceinline__ void sfb_blocks(int n0, int ncols, int N, int &b0, in
     nblk = last / 128 - b0 + 1;
 }
 
-// Per row tile of unit t: the 32-row boxes that hold rows < M (written to
-// live[]); returns their total.
+// Per row tile of unit t: the kBoxRows-row boxes that hold rows < M (written
+// to live[]); returns their total.
 __device__ __forceinline__ int row_boxes(const Unit &t, int M, int (&live)[kRowTilesPerUnit])
 {
     int total = 0;
@@ -542,8 +564,8 @@ struct Roles {
                     break;
                 }
                 ++seq;
-                // only the 32-row boxes that hold rows < M_g; the MMA rows past
-                // them read stale data and their accumulator rows are never stored
+                // the boxes that hold rows < M_g; rows past M_g inside a box are
+                // the TMA's zero fill, and their accumulator rows are never stored
                 const uint32_t fb = a_full(r.stage);
                 mbar_arrive_expect_tx(fb, (uint32_t)boxes * (kBoxRows * (kTileK / 2)));
 #pragma unroll
@@ -667,8 +689,9 @@ struct Roles {
             const int s0 = (t.n0 % 128) / 32;
             for (int kt = 0; kt < t.k_tiles; ++kt) {
                 const int sub = kt % C::kKS;  // k tile within the scale stage
-                if (!warp_wait_done(seq - NT, kSiteSfFree) ||
-                    (sub == 0 && !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull))) {
+                // gather from shared memory first, then wait for the TMEM scale
+                // buffer (the MMAs that read it two stages ago) only to write it
+                if (sub == 0 && !warp_wait_phase(s_full(rs.stage), rs.phase, abort_flag, p, kSiteSFull)) {
                     ok = false;
                     break;
                 }
@@ -731,6 +754,10 @@ struct Roles {
                             vb[8 * kk + c] = in ? *reinterpret_cast<const uint32_t *>(src + kk * kSfAtomBytes) : 0u;
                     }
                 }
+                if (!warp_wait_done(seq - 1 - NT, kSiteSfFree)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t col = (uint32_t)(C::kSfBase + rt.stage * kSfCols);
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + col;
                 tmem_st_32x32b_x32(taddr, va);
@@ -753,15 +780,20 @@ struct Roles {
     // ------------------------------------------------------------- MMA issuer
     __device__ void mma_issuer(uint32_t tmem)
     {
-        RingPos ra, rb, rt, racc;
+        RingPos ra, rb, rt;
+        AccTrack acc;
         int seq = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
-            if (!wait_phase(acc_empty(racc.stage), racc.phase ^ 1u, abort_flag, p, kSiteAccEmpty)) break;
+            const bool both = t.mtu > 1 || t.ncols > C::kPairN;
+            const int h0 = both ? 0 : acc.next;
+            if (!wait_phase(acc_empty(h0), acc.par(h0) ^ 1u, abort_flag, p, kSiteAccEmpty) ||
+                (both && !wait_phase(acc_empty(1), acc.par(1) ^ 1u, abort_flag, p, kSiteAccEmpty)))
+                break;
             tc_fence_after_sync();
-            const uint32_t d = tmem + (uint32_t)(racc.stage * C::kAccCols);
+            const uint32_t d = tmem + (uint32_t)(h0 * C::kPairN);
             const uint32_t idesc = idesc_mxf4nvf4_m128((uint32_t)t.ncols);
             for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_phase(b_full(rb.stage), rb.phase, abort_flag, p, kSiteBFull) ||
@@ -794,8 +826,9 @@ struct Roles {
                 rt.advance<NT>();
             }
             if (!ok) break;
-            tc_commit(acc_full(racc.stage));
-            racc.advance<C::kNumAcc>();
+            tc_commit(acc_full(h0));
+            if (both) tc_commit(acc_full(1));
+            acc.advance(h0, both);
         }
         // All tcgen05 work issued by this thread completes before TMEM is released.
         tc_commit(drain());
@@ -808,14 +841,18 @@ struct Roles {
         const int q = warp & 3;                    // the TMEM lane quarter this warp may read
         const int h = warp >= kWarpEpi1 ? 1 : 0;   // which half of the 32-column blocks
         const uint64_t pol_c = policy_evict_first();
-        RingPos racc;
+        AccTrack acc;
         Walker wk(p);
         Unit t;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
             const int N = gd->N;
             const int ldc = gd->ldc;
-            if (!warp_wait_phase(acc_full(racc.stage), racc.phase, abort_flag, p, kSiteAccFull)) break;
+            const bool both = t.mtu > 1 || t.ncols > C::kPairN;
+            const int h0 = both ? 0 : acc.next;
+            if (!warp_wait_phase(acc_full(h0), acc.par(h0), abort_flag, p, kSiteAccFull) ||
+                (both && !warp_wait_phase(acc_full(1), acc.par(1), abort_flag, p, kSiteAccFull)))
+                break;
             tc_fence_after_sync();
             // columns [n0, n0 + 32 * nblk) hold live data; this warp takes blocks
             // h, h + 2, ... with two tcgen05.ld in flight: the next block is read
@@ -831,7 +868,7 @@ struct Roles {
                 const bool live = row < t.M;
                 uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)ldc;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
-                                       (uint32_t)(racc.stage * C::kAccCols + mt * C::kPairN + 32 * h);
+                                       (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(tbase, v0);
 #pragma unroll 1
@@ -850,8 +887,11 @@ struct Roles {
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty(racc.stage));
-            racc.advance<C::kNumAcc>();
+            if (lane == 0) {
+                mbar_arrive(acc_empty(h0));
+                if (both) mbar_arrive(acc_empty(1));
+            }
+            acc.advance(h0, both);
         }
     }
 };

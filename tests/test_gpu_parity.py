@@ -311,6 +311,20 @@ def test_small_grids_split_the_chunks(O, grid):
             assert_close(got[g], ref[g], f"grid {grid} {layout}/{path} group {g}")
 
 
+@pytest.mark.parametrize("tile_n,grid", [(192, 1), (192, 2), (160, 5), (256, 1), (128, 3)])
+def test_accumulator_halves_alternate(O, tile_n, grid):
+    """A CTA walks many tiles: one-row-tile tiles of at most 192 columns take
+    one accumulator half each, alternating, while the epilogue drains the
+    other; two-row-tile or wider tiles take both halves. Small grids make
+    one CTA switch between the two kinds across groups."""
+    prob = synth.make_problem("custom", seed=15, M=[100, 0, 200, 50, 1, 256, 128], N=456, K=512)
+    ref, _ = O.grouped(prob)
+    for layout, path in PATHS:
+        got = run_gpu(prob, sf_layout=layout, sf_path=path, tile_n=tile_n, max_ctas=grid)
+        for g in range(prob.G):
+            assert_close(got[g], ref[g], f"tile_n {tile_n} grid {grid} {layout}/{path} group {g}")
+
+
 def test_single_group_plain_gemm_and_one_cta(O):
     prob = synth.make_problem("custom", seed=10, M=[300], N=512, K=1024)
     ref, _ = O.grouped(prob)
