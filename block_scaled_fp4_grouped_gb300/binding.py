@@ -50,6 +50,8 @@ EXPORTED = (
     "nvfp4_ggemm_schedule",
     "nvfp4_ggemm_plan_shapes",
     "nvfp4_ggemm_run_strided",
+    "nvfp4_ggemm_plan_batched",
+    "nvfp4_ggemm_run_batched",
 )
 
 
@@ -148,6 +150,12 @@ def lib() -> ctypes.CDLL:
     L.nvfp4_ggemm_plan_shapes.argtypes = [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]
+    L.nvfp4_ggemm_plan_batched.restype = ctypes.c_int
+    L.nvfp4_ggemm_plan_batched.argtypes = [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int, ctypes.c_int32,
+                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]
+    L.nvfp4_ggemm_run_batched.restype = ctypes.c_int
+    L.nvfp4_ggemm_run_batched.argtypes = [_VP, _VPP, _VPP, _VPP, _VPP, _VPP, ctypes.POINTER(ctypes.c_int64), _VP]
     _lib = L
     return L
 
@@ -224,6 +232,26 @@ def nvfp4_ggemm_plan(device: int, M: Sequence[int], N, K,
 def nvfp4_ggemm_run(plan: int, A, B, SFA, SFB, C, stream=None) -> int:
     return lib().nvfp4_ggemm_run(plan, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB),
                                  _ptr_array(C), _stream(stream))
+
+
+def nvfp4_ggemm_plan_batched(device: int, M: Sequence[int], N, K, batch: int,
+                             opt: Optional[nvfp4_ggemm_options_t] = None) -> Tuple[int, Optional[int]]:
+    """A plan of len(M) groups of `batch` problems each; N and K one value or one per group."""
+    handle = _VP()
+    Ns = list(N) if isinstance(N, (list, tuple)) else [int(N)] * len(M)
+    Ks = list(K) if isinstance(K, (list, tuple)) else [int(K)] * len(M)
+    o = ctypes.byref(opt) if opt is not None else None
+    st = lib().nvfp4_ggemm_plan_batched(ctypes.byref(handle), int(device), len(M), int(batch), _i32_array(M),
+                                        _i32_array(Ns), _i32_array(Ks), o)
+    return st, (handle.value if st == NVFP4_OK else None)
+
+
+def nvfp4_ggemm_run_batched(plan: int, A, B, SFA, SFB, C, batch_stride: Sequence[int], stream=None) -> int:
+    """One pointer per group (its batch 0) and 5 byte strides per group:
+    A, B, SFA, SFB, C."""
+    strides = (ctypes.c_int64 * max(1, len(batch_stride)))(*[int(v) for v in batch_stride])
+    return lib().nvfp4_ggemm_run_batched(plan, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB),
+                                         _ptr_array(C), strides, _stream(stream))
 
 
 def nvfp4_ggemm_run_strided(plan: int, A, B, SFA, SFB, C, ldc: Sequence[int], stream=None) -> int:
@@ -330,13 +358,17 @@ class GroupedGemm:
     A[g] uint8 [M_g, K/2], B[g] uint8 [N, K/2], SFA[g] / SFB[g] uint8 scale
     codes (raw [rows, K/16] or atom layout), C[g] float16 [M_g, N]."""
 
-    def __init__(self, M: Sequence[int], N: int, K: int, device: int = 0, **options):
+    def __init__(self, M: Sequence[int], N: int, K: int, device: int = 0, batch: int = 1, **options):
         self.M = [int(m) for m in M]
         # N and K: one value for every group, or one per group
         self.N = [int(n) for n in N] if isinstance(N, (list, tuple)) else int(N)
         self.K = [int(k) for k in K] if isinstance(K, (list, tuple)) else int(K)
+        self.batch = int(batch)
         self.opt = make_options(**options)
-        st, handle = nvfp4_ggemm_plan(device, self.M, self.N, self.K, self.opt)
+        if self.batch != 1:
+            st, handle = nvfp4_ggemm_plan_batched(device, self.M, self.N, self.K, self.batch, self.opt)
+        else:
+            st, handle = nvfp4_ggemm_plan(device, self.M, self.N, self.K, self.opt)
         if st != NVFP4_OK:
             raise Nvfp4Error(st, "nvfp4_ggemm_plan")
         self.handle = handle
@@ -353,6 +385,11 @@ class GroupedGemm:
         st = nvfp4_ggemm_run_strided(self.handle, A, B, SFA, SFB, C, ldc, stream)
         if st != NVFP4_OK:
             raise Nvfp4Error(st, "nvfp4_ggemm_run_strided")
+
+    def run_batched(self, A, B, SFA, SFB, C, batch_stride: Sequence[int], stream=None) -> None:
+        st = nvfp4_ggemm_run_batched(self.handle, A, B, SFA, SFB, C, batch_stride, stream)
+        if st != NVFP4_OK:
+            raise Nvfp4Error(st, "nvfp4_ggemm_run_batched")
 
     def bind(self, A, B, SFA, SFB, C, ldc: Optional[Sequence[int]] = None) -> "BoundCall":
         """Marshal one set of per-group buffers once, for repeated calls on

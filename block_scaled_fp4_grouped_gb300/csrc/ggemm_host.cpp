@@ -311,6 +311,7 @@ struct nvfp4_ggemm_plan_s {
     bool prep_used = false;
     bool b_prepared = false;
     // run_host device buffers
+    int batch = 1;  // problems per group of nvfp4_ggemm_plan_batched (plan groups = groups * batch)
     uint8_t *d_io = nullptr;
     std::vector<size_t> io_a, io_b, io_sfa, io_sfb, io_c;
     size_t io_bytes = 0;
@@ -699,6 +700,64 @@ nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *const *A, co
     DeviceGuard guard(plan->device);
     if (!guard.ok) return NVFP4_ERR_CUDA;
     nvfp4_status_t st = run_device(plan, A, B, SFA, SFB, C, nullptr, static_cast<cudaStream_t>(stream), false);
+    if (st == NVFP4_ERR_CUDA) cudaGetLastError();
+    return st;
+}
+
+nvfp4_status_t nvfp4_ggemm_plan_batched(nvfp4_ggemm_plan_t *out, int device, int num_groups, int32_t batch,
+                                        const int32_t *M, const int32_t *N, const int32_t *K,
+                                        const nvfp4_ggemm_options_t *opt)
+{
+    if (!out) return NVFP4_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_groups < 1 || batch < 1 || (long)num_groups * batch > kMaxGroups || !M || !N || !K)
+        return NVFP4_ERR_INVALID_ARG;
+    const int total = num_groups * batch;
+    std::vector<int32_t> Me(total), Ne(total), Ke(total);
+    for (int g = 0; g < num_groups; ++g)
+        for (int b = 0; b < batch; ++b) {
+            Me[g * batch + b] = M[g];
+            Ne[g * batch + b] = N[g];
+            Ke[g * batch + b] = K[g];
+        }
+    nvfp4_status_t st = nvfp4_ggemm_plan_shapes(out, device, total, Me.data(), Ne.data(), Ke.data(), opt);
+    if (st == NVFP4_OK) (*out)->batch = batch;
+    return st;
+}
+
+nvfp4_status_t nvfp4_ggemm_run_batched(nvfp4_ggemm_plan_t plan, const void *const *A, const void *const *B,
+                                       const void *const *SFA, const void *const *SFB, void *const *C,
+                                       const int64_t *batch_stride, void *stream)
+{
+    if (!plan || !batch_stride || plan->batch < 1 || !A || !B || !SFA || !C) return NVFP4_ERR_INVALID_ARG;
+    const int L = plan->batch, G = plan->G / L;
+    for (int g = 0; g < G; ++g) {
+        if (plan->M[g * L] == 0) continue;  // an empty group's pointers and strides are not read
+        for (int i = 5 * g; i < 5 * g + 5; ++i) {
+            if (batch_stride[i] < 0) return NVFP4_ERR_INVALID_ARG;
+            if (batch_stride[i] % 16 != 0) return NVFP4_ERR_ALIGNMENT;
+        }
+    }
+    // problem g * L + b: group g's pointers advanced by b strides
+    std::vector<const void *> a(plan->G), bb(plan->G), sa(plan->G), sb(plan->G);
+    std::vector<void *> c(plan->G);
+    auto at = [](const void *base, int64_t off) -> const void * {
+        return base ? static_cast<const void *>(static_cast<const uint8_t *>(base) + off) : nullptr;
+    };
+    for (int g = 0; g < G; ++g)
+        for (int b = 0; b < L; ++b) {
+            const int e = g * L + b;
+            const int64_t *st = batch_stride + 5 * g;
+            a[e] = at(A[g], b * st[0]);
+            bb[e] = at(B[g], b * st[1]);
+            sa[e] = at(SFA[g], b * st[2]);
+            sb[e] = SFB ? at(SFB[g], b * st[3]) : nullptr;
+            c[e] = const_cast<void *>(at(C[g], b * st[4]));
+        }
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return NVFP4_ERR_CUDA;
+    nvfp4_status_t st = run_device(plan, a.data(), bb.data(), sa.data(), SFB ? sb.data() : nullptr, c.data(),
+                                   nullptr, static_cast<cudaStream_t>(stream), false);
     if (st == NVFP4_ERR_CUDA) cudaGetLastError();
     return st;
 }

@@ -479,7 +479,7 @@ struct Roles {
     }
 
     // ------------------------------------------------------------- B producer
-    __device__ void b_producer()
+    __device__ void b_producer(Walker wk, Unit t, bool have)
     {
         const uint64_t pol_stream = policy_evict_first();  // read by one row tile only
         const uint64_t pol_keep = policy_evict_normal();    // read again by the group's other row tiles
@@ -487,9 +487,7 @@ struct Roles {
         uint32_t issued_mask = 0, issued_parity = 0;
         int last_g = first_group(), loads = 0, seq = 0;
         bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
-        Walker wk(p);
-        Unit t;
-        while (ok && wk.next(p, t)) {
+        for (bool more = have; ok && more; more = wk.next(p, t)) {
             if (!tile_fits(t)) {
                 ok = false;
                 break;
@@ -536,7 +534,7 @@ struct Roles {
     }
 
     // ------------------------------------------------------------- A producer
-    __device__ void a_producer()
+    __device__ void a_producer(Walker wk, Unit t, bool have)
     {
         const uint64_t pol = policy_evict_last();  // A tiles are re-read by every column tile
         RingPos r;
@@ -544,9 +542,7 @@ struct Roles {
         int last_g = first_group(), seq = 0;
         bool signalled = false;
         bool ok = true;
-        Walker wk(p);
-        Unit t;
-        while (ok && wk.next(p, t)) {
+        for (bool more = have; ok && more; more = wk.next(p, t)) {
             if (!tile_fits(t)) {
                 ok = false;
                 break;
@@ -588,7 +584,7 @@ struct Roles {
     }
 
     // --------------------------------------------------------- scale producer
-    __device__ void s_producer()
+    __device__ void s_producer(Walker wk, Unit t, bool have)
     {
         const uint64_t pol = policy_evict_normal();
         RingPos r;
@@ -597,9 +593,7 @@ struct Roles {
         bool signalled = false;
         bool ok = true;
 
-        Walker wk(p);
-        Unit t;
-        while (ok && wk.next(p, t)) {
+        for (bool more = have; ok && more; more = wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
             if (RAW && t.g != last_g) {
                 fence_tensormap_acquire(&gd->tmSFA);
@@ -926,17 +920,25 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
         tmem_relinquish();
     }
+    // The producers walk to their first tile (a chain of single-thread
+    // integer arithmetic of about a microsecond) while the barriers and TMEM
+    // are set up; each then continues the walk itself.
+    Walker wk0(p);
+    Unit t0{};
+    bool have0 = false;
+    if (lane == 0 && (warp == kWarpBProducer || warp == kWarpAProducer || warp == kWarpSProducer))
+        have0 = wk0.next(p, t0);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
 
     if (warp == kWarpBProducer) {
-        if (lane == 0) r.b_producer();
+        if (lane == 0) r.b_producer(wk0, t0, have0);
     } else if (warp == kWarpAProducer) {
-        if (lane == 0) r.a_producer();
+        if (lane == 0) r.a_producer(wk0, t0, have0);
     } else if (warp == kWarpSProducer) {
-        if (lane == 0) r.s_producer();
+        if (lane == 0) r.s_producer(wk0, t0, have0);
     } else if (warp == kWarpMma) {
         if (lane == 0) r.mma_issuer(tmem);
     } else if ((warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) || warp >= kWarpEpi1) {

@@ -161,6 +161,38 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_run(nvfp4_ggemm_plan_t plan, const void *co
                                void *stream);
 
 /*
+ * Batched groups. The pages' tensors carry a batch dimension l (A_g
+ * [m, k/2, l], C_g [m, n, l], ...; submission 503584's docstring, with l = 1
+ * there): every group is l independent problems of its shape.
+ * nvfp4_ggemm_plan_batched plans num_groups groups of `batch` problems each
+ * (M, N, K: host arrays of num_groups entries, as for
+ * nvfp4_ggemm_plan_shapes); internally problem b of group g is problem
+ * g * batch + b of a plan over num_groups * batch problems (at most 1024,
+ * else NVFP4_ERR_INVALID_ARG, as is batch < 1), so nvfp4_ggemm_run and the
+ * other calls on such a plan take num_groups * batch pointers in that order.
+ *
+ * nvfp4_ggemm_run_batched takes one pointer per group, to its batch 0, and
+ * batch_stride, a host array of 5 * num_groups byte strides: entries
+ * 5g .. 5g+4 are the distances between consecutive batches of A_g, B_g,
+ * SFA_g, SFB_g and C_g (a dense [l][rows][cols] tensor has stride rows *
+ * cols bytes of its element). Each stride of a group with M_g > 0 must be
+ * >= 0 (NVFP4_ERR_INVALID_ARG) and a multiple of 16 (NVFP4_ERR_ALIGNMENT); a
+ * stride of 0 shares one buffer between the batches, which is allowed for
+ * the inputs. SFB may be NULL when the
+ * plan caches B scales (nvfp4_ggemm_prepare_b_scales with num_groups *
+ * batch pointers). Otherwise as nvfp4_ggemm_run. A plan made by
+ * nvfp4_ggemm_plan or nvfp4_ggemm_plan_shapes counts as batch 1.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_batched(nvfp4_ggemm_plan_t *out, int device, int num_groups,
+                                        int32_t batch, const int32_t *M, const int32_t *N,
+                                        const int32_t *K, const nvfp4_ggemm_options_t *opt);
+
+NVFP4_API nvfp4_status_t nvfp4_ggemm_run_batched(nvfp4_ggemm_plan_t plan, const void *const *A,
+                                       const void *const *B, const void *const *SFA,
+                                       const void *const *SFB, void *const *C,
+                                       const int64_t *batch_stride, void *stream);
+
+/*
  * nvfp4_ggemm_run with a row stride for every C_g: ldc is a host array of G
  * strides in fp16 elements, each >= N_g and a multiple of 8 (16-byte rows);
  * row m of C_g starts at C[g] + m * ldc[g], and columns N_g .. ldc[g]-1 are

@@ -131,3 +131,12 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nb, "_lib", None)
     with pytest.raises(nb.NativeLibraryMissing):
         nb.lib()
+
+
+def test_batched_plan_and_run_argument_checks(L):
+    # batch < 1, groups x batch past the group limit, null arrays: before any device work
+    for G, batch in [(1, 0), (2, -1), (512, 3), (0, 2)]:
+        st, h = nb.nvfp4_ggemm_plan_batched(0, [64] * G, 256, 256, batch)
+        assert st == nb.NVFP4_ERR_INVALID_ARG and h is None, (G, batch)
+    assert L.nvfp4_ggemm_plan_batched(None, 0, 1, 2, None, None, None, None) == nb.NVFP4_ERR_INVALID_ARG
+    assert nb.nvfp4_ggemm_run_batched(None, [], [], [], [], [], [0] * 5) == nb.NVFP4_ERR_INVALID_ARG

@@ -226,3 +226,48 @@ def test_k_multiple_of_64_uniform_and_exact(O):
     got = run_gpu(prob)
     for g in range(prob.G):
         assert np.array_equal(got[g].view(np.uint16), ref[g].view(np.uint16)), f"group {g}"
+
+
+@pytest.mark.parametrize("layout", ["raw", "atom"])
+def test_batched_groups_match_the_oracle(O, layout):
+    """nvfp4_ggemm_plan_batched / run_batched: every group is `batch`
+    independent problems laid out [batch][rows][cols], one pointer per group
+    and a byte stride per operand. C's batches are padded apart; the padding
+    must keep its sentinel. K_g % 256 != 0 in one group (re-layout path for
+    raw scales)."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    shapes = [(100, 256, 512), (0, 128, 256), (200, 520, 320), (33, 64, 1024)]
+    L = 3
+    probs = [[synth.make_problem("custom", seed=1200 + 10 * g + b, M=[m], N=n, K=k) for b in range(L)]
+             for g, (m, n, k) in enumerate(shapes)]
+    dev = lambda arrs: torch.from_numpy(np.ascontiguousarray(np.stack(arrs))).cuda()
+    A = [dev([q.A[0] for q in ps]) for ps in probs]
+    B = [dev([q.B[0] for q in ps]) for ps in probs]
+    SFA = [dev([q.SFA[0] for q in ps]) for ps in probs]
+    SFB = [dev([q.SFB[0] for q in ps]) for ps in probs]
+    if layout == "atom":
+        SFA = [torch.stack([atom_copy(s[b], m, k) for b in range(L)]) for s, (m, n, k) in zip(SFA, shapes)]
+        SFB = [torch.stack([atom_copy(s[b], n, k) for b in range(L)]) for s, (m, n, k) in zip(SFB, shapes)]
+    pad = 64  # fp16 elements between C batches
+    Cbuf = [torch.full((L * (m * n + pad) + 8,), -3.0, dtype=torch.float16, device="cuda") for m, n, k in shapes]
+    strides = []
+    for g, (m, n, k) in enumerate(shapes):
+        strides += [A[g][0].numel(), B[g][0].numel(), SFA[g][0].numel(), SFB[g][0].numel(), 2 * (m * n + pad)]
+    with nb.GroupedGemm([m for m, _, _ in shapes], [n for _, n, _ in shapes], [k for _, _, k in shapes],
+                        batch=L, sf_layout=layout) as gg:
+        gg.run_batched(A, B, SFA, SFB, Cbuf, strides)
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+        with pytest.raises(nb.Nvfp4Error):
+            gg.run_batched(A, B, SFA, SFB, Cbuf, [s + 8 if i == 4 else s for i, s in enumerate(strides)])
+    torch.cuda.synchronize()
+    for g, (m, n, k) in enumerate(shapes):
+        buf = Cbuf[g].cpu().numpy()
+        for b in range(L):
+            off = b * (m * n + pad)
+            if m:
+                q = probs[g][b]
+                ref, _, _ = O.group_gemm(q.A[0], q.B[0], q.SFA[0], q.SFB[0], k)
+                assert_close(buf[off:off + m * n].reshape(m, n), ref, f"group {g} batch {b}")
+            assert (buf[off + m * n:off + m * n + pad] == -3.0).all(), f"group {g} batch {b}: padding written"
