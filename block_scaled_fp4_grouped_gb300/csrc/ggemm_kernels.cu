@@ -236,6 +236,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return wait_phase_slow(bar, parity, abort_flag, p, site);
 }
 
+// The same bounded wait written inline, for a call site that holds many live
+// registers (a call to the out-of-line slow path would spill them).
+__device__ __forceinline__ bool wait_phase_inline(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                  const GemmParams &p, uint32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            record_error(p.err, kStatusTimeout, site);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Bounded wait that ignores the abort flag: used at exit for a thread's own
 // asynchronous work, which always completes unless it was never issued.
 __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, const GemmParams &p, uint32_t site)
@@ -748,7 +766,10 @@ struct Roles {
                             vb[8 * kk + c] = in ? *reinterpret_cast<const uint32_t *>(src + kk * kSfAtomBytes) : 0u;
                     }
                 }
-                if (!warp_wait_done(seq - 1 - NT, kSiteSfFree)) {
+                const int jd = seq - 1 - NT;  // the stage whose MMAs last read this TMEM scale buffer
+                if (jd >= 0 && !__all_sync(0xffffffffu, wait_phase_inline(done(jd % kDoneRing),
+                                                                           (uint32_t)(jd / kDoneRing) & 1u,
+                                                                           abort_flag, p, kSiteSfFree))) {
                     ok = false;
                     break;
                 }
