@@ -307,7 +307,9 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  *
  * Arguments: as nvfp4_ggemm_plan + nvfp4_ggemm_run (M host array of G row
  * counts, A/B/SFA/SFB/C host arrays of G device pointers, raw scales), on
- * the current device. Limits: 1 <= num_groups <= 64, otherwise
+ * the current device. Limits: 1 <= num_groups <= 64 and K % 256 == 0
+ * (raw scale rows are loaded by the TMA, which needs 16-byte rows; there is
+ * no re-layout workspace to fall back on), otherwise
  * NVFP4_ERR_UNSUPPORTED_SHAPE before anything is enqueued; the other checks
  * and status codes are those of plan/run.
  *

@@ -140,3 +140,10 @@ def test_batched_plan_and_run_argument_checks(L):
         assert st == nb.NVFP4_ERR_INVALID_ARG and h is None, (G, batch)
     assert L.nvfp4_ggemm_plan_batched(None, 0, 1, 2, None, None, None, None) == nb.NVFP4_ERR_INVALID_ARG
     assert nb.nvfp4_ggemm_run_batched(None, [], [], [], [], [], [0] * 5) == nb.NVFP4_ERR_INVALID_ARG
+
+
+def test_noalloc_needs_k_multiple_of_256(L):
+    # raw scale rows are TMA rows only when K % 256 == 0; checked before any device work
+    for K in (320, 192, 64):
+        st, _ = nb.nvfp4_ggemm_run_noalloc([64], 256, K, [16], [16], [16], [16], [16])
+        assert st == nb.NVFP4_ERR_UNSUPPORTED_SHAPE, K
