@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,11 +47,20 @@ KERNEL_SOURCES = ["block_scaled_fp4_grouped_gb300/csrc/ggemm_kernels.cu",
                   "block_scaled_fp4_grouped_gb300/csrc/ggemm_internal.h"]
 
 
+def code_tokens(text: str) -> str:
+    """C/C++ source with comments removed and whitespace collapsed, so that a
+    comment edit does not change the hash of the code the counters were
+    taken on (string literals in these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,20 +11,25 @@
 //               ring; A is small and re-read from L2.
 //   warp 7      scale producer: the stage's A and B scales into a ring of NS
 //               small stages, running ahead of the operands.
-//   warps 8-11  scale writers: each turns a scale stage into the TMEM layout
-//               the block-scaled MMA reads (32 lanes x 4 columns per 128
-//               rows, the same in every lane quarter) and writes its quarter
-//               with tcgen05.st into one of two TMEM scale buffers. Raw
-//               row-major and atom-layout scales are both handled here, off
-//               the tensor pipe and ahead of the MMAs.
+//   warps 8-11  scale writers: each gathers a scale stage from shared memory
+//               into the TMEM layout the block-scaled MMA reads (32 lanes x
+//               4 columns per 128 rows, the same in every lane quarter), then
+//               waits for one of two TMEM scale buffers and writes its
+//               quarter with tcgen05.st. Raw row-major and atom-layout
+//               scales are both handled here, off the tensor pipe and ahead
+//               of the MMAs.
 //   warp 1      allocates TMEM; one lane issues kind::mxf4nvf4 block16 MMAs
 //               (M = 128 per row tile, N = tile width up to MAXN) into fp32
 //               accumulators, then commits one stage-completion barrier that
 //               frees the stage's A and B slots and its TMEM scale buffer.
+//               The accumulator columns are two halves: a one-row-tile tile
+//               of at most 192 columns takes one, alternating, so its MMAs
+//               overlap the previous tile's epilogue.
 //   warps 2-5,  epilogue: tcgen05.ld of the accumulators (lane quarter
 //   12-15       warp % 4; the two warps of a quarter split the 32-column
 //               blocks), RN to fp16, 32- or 16-byte stores of each row
 //               straight to C.
+// The producer lanes walk to their first tile before the prologue barrier.
 // Work: group g owns m_pairs_g x ceil(N_g/32) chunks (32 columns of one pair
 // of 128-row tiles); the chunks of all groups are numbered through prefix
 // sums, and the host gives every CTA a contiguous chunk range (its start
