@@ -17,7 +17,7 @@ using namespace nvfp4;
 
 namespace {
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0: K % 64, batched groups, plan_info.sf_path
 constexpr int kMaxGroups = 1024;
 constexpr int32_t kMaxM = 1 << 20;
 constexpr int32_t kMaxN = 1 << 20;
