@@ -973,7 +973,8 @@ const char *nvfp4_status_string(nvfp4_status_t status)
     case NVFP4_OK: return "ok";
     case NVFP4_ERR_INVALID_ARG: return "invalid argument";
     case NVFP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
-    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need K % 256 == 0, N % 8 == 0, sizes in range)";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE:
+        return "unsupported shape (need K % 64 == 0 (K % 256 == 0 without allocation), N % 8 == 0, sizes in range)";
     case NVFP4_ERR_UNSUPPORTED_DEVICE: return "no usable device (needs compute capability 10.3, GB300)";
     case NVFP4_ERR_CUDA: return "CUDA call failed";
     case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";

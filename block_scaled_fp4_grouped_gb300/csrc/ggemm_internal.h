@@ -202,7 +202,7 @@ int pair_cap_chunks(int max_n);
 // into per-CTA ranges, written to cta_begin[0..grid], and returns grid
 // (<= max_ctas <= kMaxCtas). With no more segments than max_ctas, every range
 // lies inside one segment: the split takes the smallest per-CTA budget of
-// k-stages (passes over K_g times K_g / 256) that fits max_ctas CTAs, and
+// k-stages (passes over K_g times ceil(K_g / 256)) that fits max_ctas CTAs, and
 // spare CTAs then shorten the longest ranges; otherwise the chunks are split
 // into equal contiguous ranges. counts is scratch for kMaxCtas ints.
 int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int32_t *cta_begin,
