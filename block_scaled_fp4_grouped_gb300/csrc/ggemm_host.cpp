@@ -747,6 +747,7 @@ nvfp4_status_t nvfp4_ggemm_run_batched(nvfp4_ggemm_plan_t plan, const void *cons
     for (int g = 0; g < G; ++g)
         for (int b = 0; b < L; ++b) {
             const int e = g * L + b;
+            if (plan->M[e] == 0) continue;  // left null: never read
             const int64_t *st = batch_stride + 5 * g;
             a[e] = at(A[g], b * st[0]);
             bb[e] = at(B[g], b * st[1]);
