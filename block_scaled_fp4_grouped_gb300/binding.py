@@ -396,6 +396,10 @@ class GroupedGemm:
         them (the per-call cost is then one C call)."""
         return BoundCall(self, A, B, SFA, SFB, C, ldc)
 
+    def bind_host(self, A, B, SFA, SFB, C) -> "BoundCall":
+        """bind for nvfp4_ggemm_run_host: host buffers marshalled once."""
+        return BoundCall(self, A, B, SFA, SFB, C, host=True)
+
     def run_host(self, A, B, SFA, SFB, C, stream=None) -> None:
         st = nvfp4_ggemm_run_host(self.handle, A, B, SFA, SFB, C, stream)
         if st != NVFP4_OK:
@@ -428,19 +432,23 @@ class GroupedGemm:
 
 
 class BoundCall:
-    """nvfp4_ggemm_run (or _run_strided) on one fixed set of device buffers:
-    the pointer arrays are built once and the tensors are kept alive for as
-    long as this object is."""
+    """nvfp4_ggemm_run (or _run_strided, or _run_host) on one fixed set of
+    buffers: the pointer arrays are built once and the tensors are kept
+    alive for as long as this object is."""
 
-    def __init__(self, gemm: GroupedGemm, A, B, SFA, SFB, C, ldc=None):
+    def __init__(self, gemm: GroupedGemm, A, B, SFA, SFB, C, ldc=None, host: bool = False):
         self.gemm = gemm
+        self.host = host
         self._keep = (A, B, SFA, SFB, C)
         self._args = (_ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C))
         self._ldc = _i32_array(ldc) if ldc is not None else None
 
     def __call__(self, stream=None) -> None:
         L = lib()
-        if self._ldc is None:
+        if self.host:
+            st = L.nvfp4_ggemm_run_host(self.gemm.handle, *self._args, _stream(stream))
+            name = "nvfp4_ggemm_run_host"
+        elif self._ldc is None:
             st = L.nvfp4_ggemm_run(self.gemm.handle, *self._args, _stream(stream))
             name = "nvfp4_ggemm_run"
         else:

@@ -271,3 +271,25 @@ def test_batched_groups_match_the_oracle(O, layout):
                 ref, _, _ = O.group_gemm(q.A[0], q.B[0], q.SFA[0], q.SFB[0], k)
                 assert_close(buf[off:off + m * n].reshape(m, n), ref, f"group {g} batch {b}")
             assert (buf[off + m * n:off + m * n + pad] == -3.0).all(), f"group {g} batch {b}: padding written"
+
+
+def test_bound_host_call_equals_run_host_bitwise():
+    """GroupedGemm.bind_host: nvfp4_ggemm_run_host on host buffers marshalled
+    once, called twice, equals the device-buffer call bit for bit."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import run_gpu
+    prob = synth.make_problem("custom", seed=950, M=[200, 0, 64], N=320, K=512)
+    dense = run_gpu(prob)
+    A = [np.ascontiguousarray(a) for a in prob.A]
+    B = [np.ascontiguousarray(b) for b in prob.B]
+    SFA = [np.ascontiguousarray(a) for a in prob.SFA]
+    SFB = [np.ascontiguousarray(b) for b in prob.SFB]
+    C = [np.full((m, prob.N), np.nan, np.float16) for m in prob.M]
+    with nb.GroupedGemm(prob.M, prob.N, prob.K) as gg:
+        call = gg.bind_host(A, B, SFA, SFB, C)
+        call()
+        call()
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+    for g in range(prob.G):
+        assert np.array_equal(C[g].view(np.uint16), dense[g].view(np.uint16))
