@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4_ggemm.so")
 
-SOURCES = ["ggemm_kernels.cu", "ggemm_host.cpp", "ggemm_noalloc.cu"]
+SOURCES = ["ggemm_kernels.cu", "ggemm_host.cpp", "ggemm_noalloc.cu", "io_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           f"-I{INCLUDE}", f"-I{CSRC}"]

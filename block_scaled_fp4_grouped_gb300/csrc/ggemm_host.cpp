@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include "ggemm_internal.h"
+#include "io_copy.h"
 #include "nvfp4_ggemm.h"
 
 using namespace nvfp4;
@@ -315,6 +316,11 @@ struct nvfp4_ggemm_plan_s {
     uint8_t *d_io = nullptr;
     std::vector<size_t> io_a, io_b, io_sfa, io_sfb, io_c;
     size_t io_bytes = 0;
+    // run_host through the SMs: the host pointers last checked, and for each
+    // (5 per group: A, B, SFA, SFB, C) the address the GPU uses, or none
+    std::vector<const void *> io_key;
+    std::vector<const void *> io_dev;
+    bool io_direct = false;
 
     bool raw() const { return opt.sf_layout == NVFP4_SF_RAW; }
     bool relayout() const { return raw() && opt.sf_path == NVFP4_SF_RELAYOUT; }
@@ -409,6 +415,19 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
     (void)dtab;
     *njobs_out = njobs;
     return true;
+}
+
+// The address through which the GPU can read and write host buffer `h`
+// (pinned or registered host memory), or nullptr (pageable memory).
+const void *device_view(const void *h)
+{
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return nullptr;
+    return attr.devicePointer;
 }
 
 int relayout_items(nvfp4_ggemm_plan_s *p, bool with_sfb)
@@ -814,12 +833,71 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
     std::vector<const void *> dA(p->G), dB(p->G), dSFA(p->G), dSFB(p->G);
     std::vector<void *> dC(p->G);
     for (int g = 0; g < p->G; ++g) {
-        const size_t m = (size_t)p->M[g], N = (size_t)p->N[g], K = (size_t)p->K[g];
         dA[g] = p->d_io + p->io_a[g];
         dB[g] = p->d_io + p->io_b[g];
         dSFA[g] = p->d_io + p->io_sfa[g];
         dSFB[g] = p->d_io + p->io_sfb[g];
         dC[g] = p->d_io + p->io_c[g];
+    }
+    // Host buffers the GPU can address, 16-byte aligned, in few enough jobs:
+    // one launch moves every input in and one moves C out. Otherwise one
+    // copy per buffer. The check is cached for the last set of pointers.
+    {
+        std::vector<const void *> key;
+        key.reserve(5 * (size_t)p->G);
+        for (int g = 0; g < p->G; ++g) {
+            const bool on = p->M[g] > 0;
+            key.push_back(on ? A[g] : nullptr);
+            key.push_back(on ? B[g] : nullptr);
+            key.push_back(on ? SFA[g] : nullptr);
+            key.push_back(on ? SFB[g] : nullptr);
+            key.push_back(on ? C[g] : nullptr);
+        }
+        if (key != p->io_key) {
+            p->io_key = key;
+            p->io_dev.assign(key.size(), nullptr);
+            int jobs = 0;
+            bool ok = true;
+            for (size_t i = 0; i < key.size() && ok; ++i) {
+                if (!key[i]) continue;
+                p->io_dev[i] = device_view(key[i]);
+                ok = p->io_dev[i] && aligned16(p->io_dev[i]);
+                ++jobs;
+            }
+            p->io_direct = ok && jobs <= kMaxIoJobs;
+        }
+    }
+    if (p->io_direct) {
+        IoCopyParams in{}, out{};
+        for (int g = 0; g < p->G; ++g) {
+            const size_t m = (size_t)p->M[g], N = (size_t)p->N[g], K = (size_t)p->K[g];
+            if (m == 0) continue;
+            const void *const *v = &p->io_dev[5 * (size_t)g];
+            const size_t bytes[4] = {m * K / 2, N * K / 2, sf_bytes(m, K), sf_bytes(N, K)};
+            const void *dst[4] = {dA[g], dB[g], dSFA[g], dSFB[g]};
+            for (int i = 0; i < 4; ++i)
+                in.jobs[in.njobs++] = IoJob{static_cast<const uint8_t *>(v[i]),
+                                            static_cast<uint8_t *>(const_cast<void *>(dst[i])), bytes[i]};
+            out.jobs[out.njobs++] = IoJob{static_cast<const uint8_t *>(dC[g]),
+                                          static_cast<uint8_t *>(const_cast<void *>(v[4])), m * N * 2};
+        }
+        if (io_copy_launch(in, p->sm_count, s) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+        nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true);
+        if (st != NVFP4_OK) {
+            cudaGetLastError();
+            return st;
+        }
+        if (io_copy_launch(out, p->sm_count, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+        return NVFP4_OK;
+    }
+    for (int g = 0; g < p->G; ++g) {
+        const size_t m = (size_t)p->M[g], N = (size_t)p->N[g], K = (size_t)p->K[g];
         if (m == 0) continue;
         if (cudaMemcpyAsync(const_cast<void *>(dA[g]), A[g], m * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(const_cast<void *>(dB[g]), B[g], N * K / 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||

@@ -293,3 +293,44 @@ def test_bound_host_call_equals_run_host_bitwise():
         assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
     for g in range(prob.G):
         assert np.array_equal(C[g].view(np.uint16), dense[g].view(np.uint16))
+
+
+def test_run_host_pinned_buffers_through_the_sms_bitwise():
+    """run_host on pinned host tensors: one launch moves every input over the
+    host link into the plan's buffers and one moves C back (SM loads and
+    stores of host memory the GPU can address). Equal, bit for bit, to the
+    device-buffer call; unaligned host views fall back to one copy per
+    buffer and must give the same result."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import run_gpu
+    parts = [synth.make_problem("custom", seed=960 + g, M=[m], N=n, K=k)
+             for g, (m, n, k) in enumerate([(200, 328, 768), (0, 512, 512), (64, 4096, 256), (17, 8, 320)])]
+    M = [p.M[0] for p in parts]
+    N = [p.N for p in parts]
+    K = [p.K for p in parts]
+    pin = lambda arrs: [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in arrs]
+    A, B = pin([p.A[0] for p in parts]), pin([p.B[0] for p in parts])
+    SFA, SFB = pin([p.SFA[0] for p in parts]), pin([p.SFB[0] for p in parts])
+    dense = []
+    for p in parts:
+        dense += run_gpu(p)
+    C = [torch.full((m, n), float("nan"), dtype=torch.float16).pin_memory() for m, n in zip(M, N)]
+    with nb.GroupedGemm(M, N, K) as gg:
+        call = gg.bind_host(A, B, SFA, SFB, C)
+        call()
+        call()
+        st, word = gg.sync_status()
+        assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+        for g in range(len(M)):
+            assert np.array_equal(C[g].numpy().view(np.uint16), dense[g].view(np.uint16)), f"group {g}"
+        # the same problem from host views that start 8 bytes in: one copy per buffer
+        big = [torch.zeros(a.numel() + 16, dtype=torch.uint8).pin_memory() for a in A]
+        A2 = []
+        for b, a in zip(big, A):
+            b[8:8 + a.numel()] = a.reshape(-1)
+            A2.append(b[8:8 + a.numel()].view(a.shape))
+        C2 = [torch.full((m, n), float("nan"), dtype=torch.float16).pin_memory() for m, n in zip(M, N)]
+        gg.run_host(A2, B, SFA, SFB, C2)
+        for g in range(len(M)):
+            assert np.array_equal(C2[g].numpy().view(np.uint16), dense[g].view(np.uint16)), f"unaligned, group {g}"
