@@ -208,9 +208,12 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_run_strided(nvfp4_ggemm_plan_t plan, const 
 /*
  * The same operation on HOST buffers: copies every input to plan-owned
  * device buffers (allocated on the first call), runs, and copies C back,
- * all on `stream`; returns after the stream has drained. Host buffers should
- * be pinned for the copies to be asynchronous. Scales as in the plan's
- * sf_layout (cache_b_scales is ignored here).
+ * all on `stream`; returns after the stream has drained. When every host
+ * buffer is one the GPU can address (pinned or registered) and 16-byte
+ * aligned, one kernel launch moves all the inputs over the host link and
+ * one moves C back; otherwise each buffer is one copy (pageable buffers
+ * then go through the driver's staging). Scales as in the plan's sf_layout
+ * (cache_b_scales is ignored here).
  */
 NVFP4_API nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *A,
                                     const void *const *B, const void *const *SFA,
