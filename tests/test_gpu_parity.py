@@ -30,7 +30,8 @@ def O():
 # ------------------------------------------------------------- scale re-layout
 
 @pytest.mark.parametrize("R,K", [(1, 256), (128, 256), (300, 512), (129, 1536), (4096, 7168), (7168, 2048),
-                                 (1, 64), (130, 320), (257, 832), (64, 192), (200, 1088), (33, 128)])
+                                 (1, 64), (130, 320), (257, 832), (64, 192), (200, 1088), (33, 128),
+                                 (100, 768), (513, 3840), (70000, 256), (255, 4160)])
 def test_relayout_bit_exact(O, R, K):
     import torch
     rng = np.random.default_rng(R + K)
