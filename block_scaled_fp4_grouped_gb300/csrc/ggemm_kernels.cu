@@ -866,8 +866,12 @@ struct Roles {
         Unit t;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
+            // the tile's C fields are read here, before the accumulator wait:
+            // the wait is ordered before every later load, so a load written
+            // after it would only start once the accumulator is full
             const int N = gd->N;
             const int ldc = gd->ldc;
+            uint16_t *const cbase = gd->C;
             const bool both = t.mtu > 1 || t.ncols > C::kPairN;
             const int h0 = both ? 0 : acc.next;
             if (!warp_wait_phase(acc_full(h0), acc.par(h0), abort_flag, p, kSiteAccFull) ||
@@ -879,14 +883,14 @@ struct Roles {
             // while the current one is converted and stored
             const int nblk = (min(t.ncols, N - t.n0) + 31) / 32;
             const int mine = (nblk - h + 1) / 2;
-            const bool wide_st = ((reinterpret_cast<uintptr_t>(gd->C) & 31u) == 0) && (N % 16 == 0) && (ldc % 16 == 0);
+            const bool wide_st = ((reinterpret_cast<uintptr_t>(cbase) & 31u) == 0) && (N % 16 == 0) && (ldc % 16 == 0);
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
                 if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
                 const int row = row0 + lane;
                 const bool live = row < t.M;
-                uint16_t *crow = gd->C + (size_t)(live ? row : 0) * (size_t)ldc;
+                uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
