@@ -41,6 +41,10 @@ UNIT = "µs/call"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_PER_BF16 = 13.5 / 2.25  # nominal dense ratio
+# Nominal GB300 figures (HBM3e ~8 TB/s, dense FP4 13.5 PFLOP/s): a second
+# roofline fraction beside the one against the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_FP4_TFLOPS = 13500.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["block_scaled_fp4_grouped_gb300/csrc/ggemm_kernels.cu",
                   "block_scaled_fp4_grouped_gb300/csrc/ptx.cuh",
@@ -452,6 +456,7 @@ def main():
     achieved_gbs = bytes_ / (r["us_mean"] * 1e-6) / 1e9
     tflops = flops / (r["us_mean"] * 1e-6) / 1e12
     t_roof_us = max(flops / (fp4_peak_tflops * 1e12), bytes_ / (hbm * 1e9)) * 1e6
+    t_roof_nominal_us = max(flops / (NOMINAL_FP4_TFLOPS * 1e12), bytes_ / (NOMINAL_HBM_GBS * 1e9)) * 1e6
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
@@ -466,6 +471,8 @@ def main():
         "tflops_fp4": tflops, "gbs": achieved_gbs,
         "roofline_fraction": t_roof_us / r["us_mean"],
         "roofline_time_us": t_roof_us,
+        "roofline_fraction_nominal": t_roof_nominal_us / r["us_mean"],
+        "roofline_time_us_nominal": t_roof_nominal_us,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": achieved_gbs / hbm, "traffic": traffic_for(args.config, args.sf_path),
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_,
@@ -485,11 +492,13 @@ def main():
                 q = time_config(name, path, max(20, args.steps // 2), args.warmup, torch=torch, flush=flush,
                                 tuning=tuning if path == args.sf_path else None, l2=args.l2)
                 t_roof = max(q["flops"] / (fp4_peak_tflops * 1e12), q["bytes"] / (hbm * 1e9)) * 1e6
+                t_nom = max(q["flops"] / (NOMINAL_FP4_TFLOPS * 1e12), q["bytes"] / (NOMINAL_HBM_GBS * 1e9)) * 1e6
                 per[f"{name}/{path}"] = {"us_mean": round(q["us_mean"], 2), "us_median": round(q["us_median"], 2),
                                          "us_min": round(q["us_min"], 2),
                                          "gbs": round(q["bytes"] / (q["us_mean"] * 1e-6) / 1e9, 1),
                                          "tflops": round(q["flops"] / (q["us_mean"] * 1e-6) / 1e12, 1),
                                          "roofline_fraction": round(t_roof / q["us_mean"], 3),
+                                         "roofline_fraction_nominal": round(t_nom / q["us_mean"], 3),
                                          "chunks": q["info"].chunks, "grid": q["info"].grid, "l2": q["l2"],
                                          "us_mean_flush": round(q["by_l2"]["flush"]["us_mean"], 2)}
         line["per_config"] = per
