@@ -1,9 +1,9 @@
 """Large shapes on the GPU against the oracle on sampled entries (the oracle
 computes each sampled C element on its own): more pairs of 128-row tiles
 than CTAs (the schedule falls back to equal contiguous chunk ranges that
-cross pairs and groups), a long K (a long pipeline per tile), and a wide N
-(one segment split over every CTA). Tolerance |gpu - ref| <= 1e-2 +
-1e-2 |ref| per element.
+cross pairs and groups), a long K (a long pipeline per tile), a wide N
+(one segment split over every CTA), and 256 or 1024 small groups (checked
+in full). Tolerance |gpu - ref| <= 1e-2 + 1e-2 |ref| per element.
 
 A long K (128 k tiles per tile) is checked with unit scales instead: there
 every fp32 partial sum is exact (terms are multiples of 1/4 and |sum| <
@@ -65,3 +65,18 @@ def test_long_k_unit_scales_bit_exact(O):
         ref16, _ = O.group_entries(prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], prob.K, rows, cols)
         assert_bit_exact(got[g][rows, cols], ref16, f"long K group {g}")
         assert not np.isnan(got[g]).any()
+
+
+@pytest.mark.parametrize("G,path", [(256, "fused"), (256, "relayout"), (1024, "fused")])
+def test_many_small_groups(O, G, path):
+    """Hundreds of experts with a few rows each, some empty: CTA ranges
+    cross many groups, so every role walks from group to group and the
+    producers fence each new group's tensor maps. Checked in full."""
+    rng = np.random.default_rng(1500 + G)
+    M = [int(rng.choice([0, rng.integers(1, 97)])) for _ in range(G)]
+    prob = synth.make_problem("custom", seed=1500 + G, M=M, N=256, K=512)
+    ref, _ = O.grouped(prob)
+    got = run_gpu(prob, sf_path=path)
+    for g in range(prob.G):
+        assert got[g].shape == ref[g].shape
+        assert_close(got[g], ref[g], f"G={G} group {g} M={prob.M[g]}")
