@@ -428,10 +428,11 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    world, rank, local = dist_setup()
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        # no collective on this arm: rank 0 times the oracle, the others exit
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
+    world, rank, local = dist_setup()
 
     import torch
     from block_scaled_fp4_grouped_gb300 import build as libbuild
