@@ -470,11 +470,6 @@ struct Roles {
         if (j < 0) return true;
         return wait_phase(done(j % kDoneRing), (uint32_t)(j / kDoneRing) & 1u, abort_flag, p, site);
     }
-    __device__ __forceinline__ bool warp_wait_done(int j, uint32_t site) const
-    {
-        if (j < 0) return true;
-        return warp_wait_phase(done(j % kDoneRing), (uint32_t)(j / kDoneRing) & 1u, abort_flag, p, site);
-    }
     __device__ __forceinline__ uint32_t b_stage(int s) const { return sbase + C::kOffBRing + (uint32_t)s * b_slot; }
     __device__ __forceinline__ uint32_t a_stage(int s) const { return sbase + C::kOffARing + (uint32_t)s * a_slot; }
     __device__ __forceinline__ uint32_t s_stage(int s) const { return sbase + C::kOffSRing + s * C::kSStage; }

@@ -120,40 +120,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-// 2-D tiled store shared -> global (rows/columns outside the map are dropped).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t x, int32_t y, uint32_t src)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
-                 "r"(y), "r"(src)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most N committed store groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until at most N committed store groups are still in flight at all.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group()
-{
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (TMA store, tcgen05.cp, tcgen05.mma operands).
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 
 // Whole warp: allocate `ncols` TMEM columns (power of two >= 32) and write the
@@ -200,17 +166,6 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr)
     return d;
 }
 
-// Descriptor of an unswizzled 32-row x 16-byte block (one 512-byte scale
-// atom): 8-row core matrices of 128 bytes, 128 bytes apart (SBO).
-__device__ __forceinline__ uint64_t desc_sf_atom(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    return d;
-}
-
 // Instruction descriptor, kind::mxf4nvf4 with block16 scales, M = 128:
 // A and B format E2M1 (1) in bits 7-9 and 10-12, both K-major, N>>3 in bits
 // 17-22, scale format UE4M3 (bit 23 = 0), M>>7 in bits 27-28, scale-factor
@@ -218,13 +173,6 @@ __device__ __forceinline__ uint64_t desc_sf_atom(uint32_t saddr)
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4_m128(uint32_t n)
 {
     return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 7) << 27);
-}
-
-// Copy one 512-byte scale atom from shared memory into 4 TMEM columns, the
-// same 32 lanes x 128 bits replicated into each of the four lane quarters.
-__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // D(tmem) (+)= (A * SFA) x (B * SFB)^T for one 128 x N x 64 block of E2M1
@@ -264,18 +212,8 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
-// Warp-wide: thread t writes 16 (32) consecutive 32-bit columns of TMEM lane
+// Warp-wide: thread t writes 32 consecutive 32-bit columns of TMEM lane
 // (quarter base + t), starting at the column of `taddr`.
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
