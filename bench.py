@@ -1,17 +1,20 @@
 """Benchmark of the NVFP4 block-scaled grouped GEMM on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--sf-path fused]
-                    [--impl ours|reference] [--all-configs]
+                    [--impl ours|reference] [--all-configs] [--serial-launch]
 
 One step = one nvfp4_ggemm_run call over the whole grouped problem (scale
 permutation, tile scheduling, loads, block-scaled MMAs, fp16 epilogue), with
-inputs resident in HBM. Every timed call starts with its inputs out of L2:
-by default the bench cycles through copies of the inputs that together hold
-at least three times the L2 (`--l2 rotate`); `--l2 flush` writes a 256 MB
-buffer before every call instead. Both are timed and reported; each call is
-timed with CUDA events on its stream.
+inputs resident in HBM. The headline times K steps back to back between one
+pair of CUDA events on the launching stream, the calls using in turn copies
+of the inputs that together hold at least three times the L2 (so every call
+starts with its inputs out of L2); a device-side sleep ahead of the start
+event covers the host's enqueue. Also reported, labelled: one call between
+its own events (isolated), one call after a 256 MB flush write, back-to-back
+calls on one copy (warm L2), the host's cost per call, the same call on host
+buffers (e2e), every config c0-c4, and the CPU oracle's time.
 Prints one JSON line (rank 0). `--impl reference` times the CPU oracle on
-the host cores instead (bounded samples of the same workload).
+the host cores instead (the whole problem every step).
 
 N > 1 (torchrun): every rank runs its own replica of the workload (the
 operation needs no exchange); the reported time is the maximum over ranks.
@@ -181,24 +184,11 @@ L2_BYTES = 129 << 20
 ROTATE_FACTOR = 3       # rotated input sets hold at least 3x the L2
 ROTATE_MAX_SETS = 64
 SLEEP_CYCLES = 200_000  # ~100 us at 2 GHz: longer than the host's enqueue of one call
+SM_GHZ_FOR_SLEEP = 2.2  # cycles per ns used to size device sleeps (>= the top SM clock)
+MAX_STREAM_SLEEP_NS = 400e6
 
 
-def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0, torch=None, flush=None,
-                want_e2e: bool = False, tuning=None, l2: str = "rotate"):
-    """Device timing of one config. Returns a dict of measurements.
-
-    Two ways to start every timed call with its inputs out of L2:
-    "rotate" keeps R copies of the inputs and outputs (R * their size >= 3x
-    the L2, each copy with its own plan, so no table upload happens inside
-    the timed region) and cycles through them, so a call's inputs were last
-    read R - 1 calls ago with at least twice the L2 of other data read since;
-    "flush" writes a 256 MB buffer before every call, which leaves L2 full of
-    dirty lines that the call's reads must first write back. Both are
-    timed; `l2` picks the one reported as the headline (problems too small
-    for R <= 64 copies to cover 3x the L2 always use "flush")."""
-    from block_scaled_fp4_grouped_gb300 import binding as nb
-    prob = synth.make_problem(name, seed=seed)
-    K, N = prob.K, prob.N
+def _flavour(sf_path: str):
     kw = dict(sf_layout="raw", sf_path="fused")
     if sf_path == "relayout":
         kw = dict(sf_layout="raw", sf_path="relayout")
@@ -206,12 +196,45 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
         kw = dict(sf_layout="raw", sf_path="relayout", cache_b_scales=True)
     elif sf_path == "atom":
         kw = dict(sf_layout="atom", sf_path="fused")
+    return kw
+
+
+def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0, torch=None, flush=None,
+                want_e2e: bool = False, tuning=None, host_calls: int = 50, prob=None):
+    """Device timing of one config. Returns a dict of measurements.
+
+    Every timed call starts with its inputs out of L2 (except the labelled
+    warm-L2 protocol): R copies of the inputs and outputs (R * their size >=
+    3x the L2, each copy with its own plan, so no table upload happens inside
+    a timed region) are used in turn, so a call's inputs were last read R - 1
+    calls earlier with at least twice the L2 of other data read since.
+    Protocols, all timed with CUDA events on the launching stream:
+
+    * "stream" (the headline): `steps` calls back to back between one pair
+      of events, cycling through the copies; a device-side sleep ahead of the
+      start event covers the host's enqueue of all of them, so the timed
+      region holds GPU work only. Per call = elapsed / steps.
+    * "isolated": one call between its own events, a short device sleep
+      before each (the host has enqueued the call before its start event
+      runs), cycling through the copies.
+    * "flush": one call between its own events after a 256 MB write, on one
+      copy (it leaves L2 full of dirty lines the call's reads write back).
+    * "warm": `steps` calls back to back on one copy, nothing flushed
+      (warm L2 as far as the copy fits in it).
+    Problems too small for 64 copies to cover 3x the L2 (c0) run "flush"
+    and "warm" only, and report "flush" as the headline.
+    Host cost: the enqueue time of one call (the C call from Python, plan
+    cached) and the wall time of one call followed by a stream
+    synchronisation."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    if prob is None:
+        prob = synth.make_problem(name, seed=seed)
+    K, N = prob.K, prob.N
+    kw = _flavour(sf_path)
     kw.update(tuning or {})
     set_bytes = synth.algorithmic_bytes(prob.M, N, K)
     n_sets = -(-ROTATE_FACTOR * L2_BYTES // set_bytes)
     rotate_ok = n_sets <= ROTATE_MAX_SETS
-    if not rotate_ok:
-        l2 = "flush"
     n_sets = max(2, n_sets) if rotate_ok else 1
 
     def make_set():
@@ -239,49 +262,86 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
             if st != nb.NVFP4_OK:
                 raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
 
-    def before_call(mode):
-        # Something for the GPU to do while the host enqueues the call, so
-        # that the start event is not followed by host launch latency: the
-        # flush itself, or (rotation) a short device-side sleep that touches
-        # no memory.
-        if mode == "flush":
-            flush.zero_()
-        else:
-            torch.cuda._sleep(SLEEP_CYCLES)
+    # warm-up: every copy at least once (uploads its table), then W calls;
+    # the enqueue time of a call is taken here too
+    enq = []
+    for i in range(max(warmup, len(sets))):
+        _, call = sets[i % len(sets)]
+        torch.cuda._sleep(SLEEP_CYCLES)
+        t0 = time.perf_counter()
+        call()
+        enq.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    check()
+    enqueue_s = statistics.median(enq[len(sets):] or enq)
 
-    def timed(mode):
-        # warm-up: every set at least once (uploads its table), then W calls
-        for i in range(max(warmup, len(sets) if mode == "rotate" else 1)):
-            _, call = sets[i % len(sets)] if mode == "rotate" else sets[0]
-            before_call(mode)
-            call()
-        check()
+    def stream_block(order):
+        """Calls sets[order[i]] back to back between one event pair. Returns
+        (µs per call, whether the device waited for the host)."""
+        sleep_ns = 50e3 + 3.0 * enqueue_s * 1e9 * len(order)
+        for _attempt in range(4):
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(int(min(sleep_ns, MAX_STREAM_SLEEP_NS) * SM_GHZ_FOR_SLEEP))
+            start.record(stream)
+            for j in order:
+                sets[j][1]()
+            end.record(stream)
+            late = start.query()  # the timed region had begun before the last call was enqueued
+            torch.cuda.synchronize()
+            if not late or sleep_ns >= MAX_STREAM_SLEEP_NS:
+                return start.elapsed_time(end) * 1e3 / len(order), late
+            sleep_ns *= 4
+        return start.elapsed_time(end) * 1e3 / len(order), late
+
+    def per_call(mode):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
         for i in range(steps):
-            _, call = sets[i % len(sets)] if mode == "rotate" else sets[0]
-            before_call(mode)
+            _, call = sets[i % len(sets)] if mode == "isolated" else sets[0]
+            if mode == "flush":
+                flush.zero_()
+            else:
+                torch.cuda._sleep(SLEEP_CYCLES)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        check()
-        return [a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends)], wall
+        return [a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends)]
 
-    modes = {m: timed(m) for m in (["rotate", "flush"] if rotate_ok else ["flush"])}
-    us, wall = modes[l2]
-    out = {
-        "prob": prob, "info": info, "us": us, "wall_s": wall, "l2": l2, "n_sets": n_sets,
-        "us_mean": statistics.fmean(us), "us_median": statistics.median(us),
-        "us_min": min(us), "us_p90": sorted(us)[int(0.9 * (len(us) - 1))],
-        "by_l2": {m: {"us_mean": statistics.fmean(v[0]), "us_median": statistics.median(v[0]),
-                      "us_min": min(v[0])} for m, v in modes.items()},
-        "bytes": set_bytes, "flops": synth.algorithmic_flops(prob.M, N, K),
-        "launches_per_call": info.kernels_per_run,
-    }
+    out = {"prob": prob, "info": info, "n_sets": n_sets, "rotate": rotate_ok,
+           "bytes": set_bytes, "flops": synth.algorithmic_flops(prob.M, N, K),
+           "launches_per_call": info.kernels_per_run}
+    by = {}
+    t_wall0 = time.perf_counter()
+    if rotate_ok:
+        us, late = stream_block([i % len(sets) for i in range(steps)])
+        by["stream"] = {"us_mean": us, "host_bound": bool(late)}
+        v = per_call("isolated")
+        by["isolated"] = {"us_mean": statistics.fmean(v), "us_median": statistics.median(v), "us_min": min(v),
+                          "us_p90": sorted(v)[int(0.9 * (len(v) - 1))]}
+    v = per_call("flush")
+    by["flush"] = {"us_mean": statistics.fmean(v), "us_median": statistics.median(v), "us_min": min(v),
+                   "us_p90": sorted(v)[int(0.9 * (len(v) - 1))]}
+    us, late = stream_block([0] * steps)
+    by["warm"] = {"us_mean": us, "host_bound": bool(late)}
+    out["timed_wall_s"] = time.perf_counter() - t_wall0
+    check()
+    out["headline"] = "stream" if rotate_ok else "flush"
+    out["us_mean"] = by[out["headline"]]["us_mean"]
+    out["by"] = by
+    # host cost per call with the plan cached
+    _, call = sets[0]
+    torch.cuda.synchronize()
+    walls = []
+    for _ in range(host_calls):
+        t0 = time.perf_counter()
+        call()
+        torch.cuda.synchronize()
+        walls.append(time.perf_counter() - t0)
+    out["host"] = {"enqueue_us": enqueue_s * 1e6, "call_and_sync_us": statistics.median(walls) * 1e6}
     if want_e2e:
         out["e2e"] = time_e2e(prob, kw, steps, warmup, torch, nb)
     for gg, _ in sets:
@@ -290,9 +350,9 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
 
 
 def l2_text(r):
-    if r["l2"] == "rotate":
+    if r["rotate"]:
         return (f"inputs larger than L2: {r['n_sets']} copies of the inputs and outputs "
-                f"({r['n_sets']} x {r['bytes'] / 1e6:.1f} MB), cycled call by call, no flush write")
+                f"({r['n_sets']} x {r['bytes'] / 1e6:.1f} MB) used in turn, no flush write")
     return "flushed before every timed call (256 MB write)"
 
 
@@ -327,63 +387,39 @@ def time_e2e(prob, kw, steps, warmup, torch, nb):
             "d2h_bytes_per_step": int(d2h), "steps": n, "median": statistics.median(times)}
 
 
-def oracle_sample_time(prob, budget_s: float):
-    """Time the oracle (as it stands) on a bounded sample of `prob`: whole
-    groups while they fit the budget, else a row subset of the largest
-    group. Returns (µs per full call extrapolated by flops, threads, sample
-    text)."""
+def oracle_time(prob, nthreads: int = 0, groups=None):
+    """Wall time (s) of the oracle, as it stands, on `prob` (every group, or
+    the listed ones) with `nthreads` host threads (0 = all cores). Returns
+    (seconds, threads used)."""
     import oracle as oracle_pkg
     O = oracle_pkg.get()
-    threads = os.cpu_count() or 1
-    total_flops = synth.algorithmic_flops(prob.M, prob.N, prob.K)
-    g0 = int(np.argmax(prob.M))
-    # size the sample from 4 rows per thread of the largest group (after a warm-up call)
-    probe = max(1, min(prob.M[g0], 4 * threads))
-    O.group_gemm(prob.A[g0][:4], prob.B[g0], prob.SFA[g0][:4], prob.SFB[g0], prob.K, nthreads=threads)
+    threads = nthreads or (os.cpu_count() or 1)
     t0 = time.perf_counter()
-    O.group_gemm(prob.A[g0][:probe], prob.B[g0], prob.SFA[g0][:probe], prob.SFB[g0], prob.K, nthreads=threads)
-    per_row = max((time.perf_counter() - t0) / probe, 1e-7)
-    groups, est = [], 0.0
-    for g, m in enumerate(prob.M):
-        if m > 0 and est + m * per_row <= budget_s:
-            groups.append(g)
-            est += m * per_row
-    if groups:
-        t0 = time.perf_counter()
-        for g in groups:
+    for g in (range(prob.G) if groups is None else groups):
+        if prob.M[g] > 0:
             O.group_gemm(prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], prob.K, nthreads=threads)
-        dt = time.perf_counter() - t0
-        rows = sum(prob.M[g] for g in groups)
-        sample_flops = 2 * rows * prob.N * prob.K
-        what = (f"{len(groups)} of {sum(1 for m in prob.M if m > 0)} groups ({rows} of {sum(prob.M)} rows) "
-                f"x N={prob.N} x K={prob.K} ({dt:.2f} s)")
-    else:
-        take = int(max(8, min(prob.M[g0], budget_s / per_row)))
-        t0 = time.perf_counter()
-        O.group_gemm(prob.A[g0][:take], prob.B[g0], prob.SFA[g0][:take], prob.SFB[g0], prob.K, nthreads=threads)
-        dt = time.perf_counter() - t0
-        sample_flops = 2 * take * prob.N * prob.K
-        what = f"group {g0}: {take} of {prob.M[g0]} rows x N={prob.N} x K={prob.K} ({dt:.2f} s)"
-    us_full = dt * 1e6 * total_flops / sample_flops
-    if sample_flops < total_flops:
-        what += ", scaled by flops"
-    return us_full, threads, what
+    return time.perf_counter() - t0, threads
 
 
 def run_reference(args, world, rank):
-    """The CPU oracle as the reference arm (rank 0 only)."""
+    """The CPU oracle as the reference arm (rank 0 only): every timed step is
+    the whole problem of the workload; the warm-up steps run its smallest
+    group (they only load the oracle and warm the caches)."""
     if rank != 0:
         return
     prob = synth.make_problem(args.config, seed=0)
-    per_step = []
-    cores = os.cpu_count() or 1
-    sample = ""
-    budget = max(0.5, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
-    for i in range(args.warmup + args.steps):
-        us, cores, sample = oracle_sample_time(prob, budget)
-        if i >= args.warmup:
-            per_step.append(us)
+    g_small = int(np.argmin([m if m > 0 else 1 << 30 for m in prob.M]))
+    for _ in range(args.warmup):
+        oracle_time(prob, groups=[g_small])
+    per_step, cores = [], os.cpu_count() or 1
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        sec, cores = oracle_time(prob)
+        per_step.append(sec * 1e6)
+    wall = time.perf_counter() - t_all
     value = statistics.fmean(per_step)
+    sample = (f"the whole {args.config} problem every step ({len(prob.M)} groups, {sum(prob.M)} rows x "
+              f"N={prob.N} x K={prob.K}), {args.steps} steps in {wall:.1f} s; warm-up steps: group {g_small} only")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
@@ -391,6 +427,7 @@ def run_reference(args, world, rank):
         "config": workload_config(args.config, prob),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "timed_wall_s": wall,
     }
     print(json.dumps(line), flush=True)
 
@@ -409,22 +446,47 @@ def workload_config(name, prob):
             "scales": "raw row-major [rows, K/16] E4M3 per call"}
 
 
+PER_CONFIGS = ["c0", "c1", "c2", "c3", "c4"]
+PAGE_CONFIGS = ["c1_page", "c2_page", "c3_page", "c4_page"]
+
+
+def roofline_time_us(flops, bytes_, fp4_tflops, hbm_gbs):
+    return max(flops / (fp4_tflops * 1e12), bytes_ / (hbm_gbs * 1e9)) * 1e6
+
+
+def config_summary(q, fp4_peak_tflops, hbm):
+    """Per-config figures of one time_config result."""
+    us = q["us_mean"]
+    t_roof = roofline_time_us(q["flops"], q["bytes"], fp4_peak_tflops, hbm)
+    t_nom = roofline_time_us(q["flops"], q["bytes"], NOMINAL_FP4_TFLOPS, NOMINAL_HBM_GBS)
+    by = {m: {k: (round(v, 2) if isinstance(v, float) else v) for k, v in d.items()} for m, d in q["by"].items()}
+    return {"us": round(us, 2), "protocol": q["headline"], "us_by_protocol": by,
+            "gbs": round(q["bytes"] / (us * 1e-6) / 1e9, 1), "tflops": round(q["flops"] / (us * 1e-6) / 1e12, 1),
+            "roofline_fraction": round(t_roof / us, 3), "roofline_time_us": round(t_roof, 2),
+            "roofline_fraction_nominal": round(t_nom / us, 3),
+            "algorithmic_bytes": q["bytes"], "flops": q["flops"],
+            "host_us": {k: round(v, 2) for k, v in q["host"].items()},
+            "grid": q["info"].grid, "chunks": q["info"].chunks, "M": list(q["prob"].M)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="c4")
     ap.add_argument("--sf-path", default="fused", choices=["fused", "relayout", "relayout-cached", "atom"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--all-configs", action="store_true", help="also time every config (extra key)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also time the pages' M lists and the re-layout paths (extra key)")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the c0-c4 table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0, help="widest output tile (0 = library default)")
     ap.add_argument("--b-stages", type=int, default=0)
     ap.add_argument("--a-stages", type=int, default=0)
-    ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
-                    help="how every timed call starts with its inputs out of L2 (both are timed)")
+    ap.add_argument("--serial-launch", action="store_true",
+                    help="plain kernel launches (no overlap of a call's set-up with the previous call)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -444,35 +506,43 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     hbm, bf16, peak_src = measured_peaks()
     fp4_peak_tflops = bf16 * FP4_PER_BF16
+    tuning = dict(tile_n=args.tile_n, b_stages=args.b_stages, a_stages=args.a_stages,
+                  serial_launch=args.serial_launch)
 
     barrier(world)
     with ClockSampler(local) as clocks:
-        tuning = dict(tile_n=args.tile_n, b_stages=args.b_stages, a_stages=args.a_stages)
         r = time_config(args.config, args.sf_path, args.steps, args.warmup, torch=torch, flush=flush,
-                        want_e2e=not args.no_e2e, tuning=tuning, l2=args.l2)
+                        want_e2e=not args.no_e2e, tuning=tuning)
     barrier(world)
     us = max_over_ranks(world, r["us_mean"], device)
     prob = r["prob"]
     bytes_, flops = r["bytes"], r["flops"]
-    achieved_gbs = bytes_ / (r["us_mean"] * 1e-6) / 1e9
-    tflops = flops / (r["us_mean"] * 1e-6) / 1e12
-    t_roof_us = max(flops / (fp4_peak_tflops * 1e12), bytes_ / (hbm * 1e9)) * 1e6
-    t_roof_nominal_us = max(flops / (NOMINAL_FP4_TFLOPS * 1e12), bytes_ / (NOMINAL_HBM_GBS * 1e9)) * 1e6
+    achieved_gbs = bytes_ / (us * 1e-6) / 1e9
+    tflops = flops / (us * 1e-6) / 1e12
+    t_roof_us = roofline_time_us(flops, bytes_, fp4_peak_tflops, hbm)
+    t_roof_nominal_us = roofline_time_us(flops, bytes_, NOMINAL_FP4_TFLOPS, NOMINAL_HBM_GBS)
+    iso = r["by"].get("isolated", r["by"]["flush"])
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
         "config": dict(workload_config(args.config, prob), sf_path=args.sf_path,
                        l2=l2_text(r),
+                       timing=("K calls back to back between one event pair (a device sleep ahead of the "
+                               "start event covers the host's enqueue); value = elapsed / K"
+                               if r["headline"] == "stream" else "one call between its own events"),
+                       launch="plain" if args.serial_launch else "set-up overlaps the previous call",
                        max_tile_n=r["info"].tile_n, grid=r["info"].grid, chunks=r["info"].chunks,
                        b_stages=r["info"].b_stages, a_stages=r["info"].a_stages,
                        parallelism=f"replicas x{world}"),
-        "us_median": r["us_median"], "us_min": r["us_min"], "us_p90": r["us_p90"],
-        "us_by_l2_protocol": {m: {k: round(v, 2) for k, v in d.items()} for m, d in r["by_l2"].items()},
+        "us_isolated_call": {k: round(v, 2) for k, v in iso.items()},
+        "us_by_protocol": {m: {k: (round(v, 2) if isinstance(v, float) else v) for k, v in d.items()}
+                           for m, d in r["by"].items()},
+        "host_us_per_call": {k: round(v, 2) for k, v in r["host"].items()},
         "tflops_fp4": tflops, "gbs": achieved_gbs,
-        "roofline_fraction": t_roof_us / r["us_mean"],
+        "roofline_fraction": t_roof_us / us,
         "roofline_time_us": t_roof_us,
-        "roofline_fraction_nominal": t_roof_nominal_us / r["us_mean"],
+        "roofline_fraction_nominal": t_roof_nominal_us / us,
         "roofline_time_us_nominal": t_roof_nominal_us,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": achieved_gbs / hbm, "traffic": traffic_for(args.config, args.sf_path),
@@ -480,32 +550,42 @@ def main():
                      "kernel": "ggemm_kernel" if args.sf_path != "relayout" else "ggemm_kernel + sf_relayout_kernel"},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": clocks.summary(),
-        "timed_wall_s": r["wall_s"],
+        "timed_wall_s": r["timed_wall_s"],
     }
     if "e2e" in r:
         e2e = r["e2e"]
         line["e2e"] = {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                        "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]}
-    if args.all_configs and rank == 0:
+    if rank == 0 and not args.no_per_config:
         per = {}
-        for name in ["c0", "c1", "c2", "c3", "c4", "c1_page", "c2_page", "c3_page", "c4_page"]:
-            for path in ["fused", "relayout", "relayout-cached"]:
-                q = time_config(name, path, max(20, args.steps // 2), args.warmup, torch=torch, flush=flush,
-                                tuning=tuning if path == args.sf_path else None, l2=args.l2)
-                t_roof = max(q["flops"] / (fp4_peak_tflops * 1e12), q["bytes"] / (hbm * 1e9)) * 1e6
-                t_nom = max(q["flops"] / (NOMINAL_FP4_TFLOPS * 1e12), q["bytes"] / (NOMINAL_HBM_GBS * 1e9)) * 1e6
-                per[f"{name}/{path}"] = {"us_mean": round(q["us_mean"], 2), "us_median": round(q["us_median"], 2),
-                                         "us_min": round(q["us_min"], 2),
-                                         "gbs": round(q["bytes"] / (q["us_mean"] * 1e-6) / 1e9, 1),
-                                         "tflops": round(q["flops"] / (q["us_mean"] * 1e-6) / 1e12, 1),
-                                         "roofline_fraction": round(t_roof / q["us_mean"], 3),
-                                         "roofline_fraction_nominal": round(t_nom / q["us_mean"], 3),
-                                         "chunks": q["info"].chunks, "grid": q["info"].grid, "l2": q["l2"],
-                                         "us_mean_flush": round(q["by_l2"]["flush"]["us_mean"], 2)}
+        names = PER_CONFIGS + (PAGE_CONFIGS if args.all_configs else [])
+        paths = ["fused"] + (["relayout", "relayout-cached"] if args.all_configs else [])
+        with ClockSampler(local) as clocks_pc:
+            for name in names:
+                for path in paths:
+                    if name == args.config and path == args.sf_path:
+                        q = r
+                    else:
+                        q = time_config(name, path, args.steps, args.warmup, torch=torch, flush=flush,
+                                        tuning=tuning)
+                    per[name if path == "fused" else f"{name}/{path}"] = config_summary(q, fp4_peak_tflops, hbm)
         line["per_config"] = per
+        line["per_config_clocks"] = clocks_pc.summary()
     if rank == 0 and not args.no_cpu_baseline:
-        us_cpu, cores, sample = oracle_sample_time(prob, budget_s=10.0)
-        line["cpu_baseline"] = {"value": us_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        # the oracle as it stands, whole problems, all host cores; and c2 on one thread
+        by_cfg = {}
+        for name in PER_CONFIGS:
+            p = prob if name == args.config else synth.make_problem(name, seed=0)
+            sec, cores = oracle_time(p)
+            by_cfg[name] = {"s": round(sec, 3), "threads": cores}
+        p2 = synth.make_problem("c2", seed=0)
+        sec1, _ = oracle_time(p2, nthreads=1)
+        by_cfg["c2_1thread"] = {"s": round(sec1, 3), "threads": 1}
+        line["cpu_baseline"] = {"value": by_cfg[args.config]["s"] * 1e6, "unit": UNIT,
+                                "cores": by_cfg[args.config]["threads"], "kind": "oracle",
+                                "sample": f"the whole {args.config} problem once (all {len(prob.M)} groups, "
+                                          f"{sum(prob.M)} rows), not scaled"}
+        line["cpu_baseline_by_config"] = by_cfg
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

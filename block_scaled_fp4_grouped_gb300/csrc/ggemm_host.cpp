@@ -368,6 +368,7 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
     if (ggemm_variant_index(variant_width(out->tile_n), out->b_stages, out->a_stages, raw_fused) < 0)
         return NVFP4_ERR_INVALID_ARG;
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
+    if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
     return NVFP4_OK;
 }
@@ -484,6 +485,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     key.push_back(reinterpret_cast<const void *>(static_cast<uintptr_t>(force_sfb ? 1 : 0)));
 
     int slot = p->cur;
+    bool uploaded = false;
     if (slot < 0 || p->slots[slot].key != key) {
         slot = (p->cur + 1) % kSlots;
         Slot &s = p->slots[slot];
@@ -494,6 +496,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
             return NVFP4_ERR_CUDA;
         s.key = key;
         p->cur = slot;
+        uploaded = true;
     }
     Slot &s = p->slots[slot];
 
@@ -518,7 +521,11 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     gp.cap_pair = p->cap_pair;
     gp.wide_rows = p->var.max_n;
     gp.debug_skip_load = p->opt.debug_skip_load;
-    if (ggemm_launch(p->variant, gp, p->grid, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    // The GEMM may overlap its set-up with the previous kernel of the stream
+    // (it reads only the problem table before that kernel completes). Not
+    // right after a table upload: the copy, not a kernel, precedes it then.
+    const bool overlap = !p->opt.serial_launch && (p->relayout() || !uploaded);
+    if (ggemm_launch(p->variant, gp, p->grid, stream, overlap) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (cudaEventRecord(s.ev, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     s.used = true;
     return NVFP4_OK;
@@ -542,6 +549,7 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->debug_skip_load = 0;
     opt->b_stages = 0;
     opt->a_stages = 0;
+    opt->serial_launch = 0;
 }
 
 nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,

@@ -188,7 +188,10 @@ GemmVariant ggemm_variant(int index);
 int ggemm_smem_bytes(int index);
 int ggemm_threads();
 cudaError_t ggemm_configure(int index);  // raises the dynamic shared-memory limit (per device)
-cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream);
+// overlap_prev: launch with programmatic stream serialisation, so that the
+// kernel's set-up overlaps the end of the previous kernel on the stream (the
+// kernel waits for that kernel to complete before its first operand load).
+cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream, bool overlap_prev);
 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream);
 

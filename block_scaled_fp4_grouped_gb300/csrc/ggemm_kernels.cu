@@ -957,6 +957,14 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
+    // Launched after another kernel of the stream with programmatic
+    // serialisation, everything above (barriers, TMEM, the problem table,
+    // tensor-map prefetch, the walk to the first tile) overlaps that kernel's
+    // last CTAs; nothing below (operand loads, C stores) starts before it has
+    // completed. The next kernel may be scheduled from here on: its CTAs
+    // find an SM only as this grid's CTAs exit.
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == kWarpBProducer) {
         if (lane == 0) r.b_producer(wk0, t0, have0);
@@ -1088,10 +1096,19 @@ cudaError_t ggemm_configure(int index)
                                 kVariants[index].smem);
 }
 
-cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream)
+cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream, bool overlap_prev)
 {
-    kVariants[index].fn<<<grid, kThreads, kVariants[index].smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = (size_t)kVariants[index].smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap_prev ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kVariants[index].fn, p);
 }
 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream)

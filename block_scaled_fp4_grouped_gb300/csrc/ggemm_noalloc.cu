@@ -163,7 +163,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.cap_pair = cap_pair;
     gp.wide_rows = kMaxTileN;
     gp.debug_skip_load = 0;
-    if (ggemm_launch(variant, gp, grid, s) != cudaSuccess) {
+    if (ggemm_launch(variant, gp, grid, s, false) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
     }

@@ -23,6 +23,24 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+
+// Blocks until the grid this one was launched to depend on (the previous
+// kernel of the stream, under programmatic stream serialisation) has
+// completed and its memory operations are visible. A no-op for a grid
+// launched without that attribute.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid of the stream be scheduled (its CTAs still need free
+// SMs) once every CTA of this grid has executed this or exited.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

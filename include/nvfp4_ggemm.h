@@ -117,7 +117,13 @@ typedef struct {
                                  each CTA cuts them into more slots when its tiles are
                                  narrower or have one row tile */
     int32_t a_stages;         /* shared-memory stages of the A ring (see b_stages) */
-    int32_t reserved[3];
+    int32_t serial_launch;    /* 0 (default): a GEMM launch that follows another kernel on its
+                                 stream may start its set-up (barriers, TMEM, tensor-map
+                                 prefetch, the walk to its first tile) while that kernel's last
+                                 CTAs finish (programmatic dependent launch); its loads and
+                                 stores still wait until that kernel has completed. 1: plain
+                                 launches, every kernel starts after the previous one ends */
+    int32_t reserved[2];
 } nvfp4_ggemm_options_t;
 
 typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;

@@ -35,6 +35,9 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("c0")
+    # every timed step is the whole problem, and the steps fit in the run's own wall time
+    assert "whole" in d["cpu_baseline"]["sample"]
+    assert d["timed_wall_s"] >= 0.99 * d["steps"] * d["value"] * 1e-6
 
 
 def test_reference_arm_other_ranks_exit_quietly():

@@ -1,0 +1,85 @@
+"""Back-to-back calls on one stream, through the C ABI.
+
+A GEMM launched right after another kernel of its stream starts its set-up
+while that kernel finishes (programmatic dependent launch) and must not load
+an operand before that kernel has completed. Here the second GEMM reads, as
+its A operand, the bytes the first GEMM writes to C (any byte is a valid
+pair of E2M1 codes), so a load issued too early would see the previous
+contents of that buffer. Both plans' tables are uploaded by a first round
+of calls; the checked round changes the first GEMM's inputs with a torch
+kernel and then enqueues both GEMMs with nothing between them, so both
+launches overlap their predecessor. The expected values are the oracle's on
+the bytes read back after the stream has drained."""
+import numpy as np
+import pytest
+
+import oracle
+from block_scaled_fp4_grouped_gb300 import synth
+from gpu_util import assert_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_scaled_fp4_grouped_gb300 import build
+    build.build()
+
+
+def _new_inputs(prob, seed):
+    other = synth.make_problem("custom", seed=seed, M=prob.M, N=prob.N, K=prob.K)
+    return other
+
+
+@pytest.mark.parametrize("serial", [False, True], ids=["overlapped", "plain"])
+def test_second_gemm_reads_what_the_first_wrote(serial):
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    # first GEMM: one group, 256 x 4096 x 7168 (a few microseconds of work)
+    p1 = synth.make_problem("custom", seed=41, M=[256], N=4096, K=7168)
+    A1, B1, SFA1, SFB1 = to_device(p1.A), to_device(p1.B), to_device(p1.SFA), to_device(p1.SFB)
+    C1 = [torch.zeros((256, 4096), dtype=torch.float16, device="cuda")]
+    # second GEMM: A2 is the first 256 x 4096 bytes of C1 (K2 = 8192)
+    p2 = synth.make_problem("custom", seed=42, M=[256], N=512, K=8192)
+    A2 = [C1[0].view(torch.uint8).reshape(-1)[: 256 * 4096].view(256, 4096)]
+    B2, SFA2, SFB2 = to_device(p2.B), to_device(p2.SFA), to_device(p2.SFB)
+    C2 = [torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")]
+    g1 = nb.GroupedGemm(p1.M, p1.N, p1.K, serial_launch=serial)
+    g2 = nb.GroupedGemm(p2.M, p2.N, p2.K, serial_launch=serial)
+    try:
+        call1 = g1.bind(A1, B1, SFA1, SFB1, C1)
+        call2 = g2.bind(A2, B2, SFA2, SFB2, C2)
+        call1()
+        call2()
+        torch.cuda.synchronize()
+        for rnd in range(3):
+            q = _new_inputs(p1, 100 + rnd)
+            a_new = torch.from_numpy(q.A[0]).cuda()
+            sfa_new = torch.from_numpy(q.SFA[0]).cuda()
+            torch.cuda.synchronize()
+            # torch kernels write the first GEMM's new A and SFA, then both
+            # GEMMs follow with nothing between them
+            torch.bitwise_xor(a_new, 0, out=A1[0])
+            torch.bitwise_xor(sfa_new, 0, out=SFA1[0])
+            call1()
+            call2()
+            for gg in (g1, g2):
+                st, word = gg.sync_status()
+                assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+            c1 = C1[0].cpu().numpy()
+            a2 = A2[0].cpu().numpy()
+            c2 = C2[0].cpu().numpy()
+            O = oracle.get()
+            # the first GEMM used the new inputs (sampled entries)
+            rng = np.random.default_rng(rnd)
+            rows = rng.integers(0, 256, 300).astype(np.int32)
+            cols = rng.integers(0, 4096, 300).astype(np.int32)
+            want1, _ = O.group_entries(q.A[0], p1.B[0], q.SFA[0], p1.SFB[0], p1.K, rows, cols)
+            assert_close(c1[rows, cols], want1, f"round {rnd}: first GEMM")
+            # the second GEMM read the first GEMM's output of this round
+            want2, _, _ = O.group_gemm(a2, p2.B[0], p2.SFA[0], p2.SFB[0], p2.K)
+            assert not np.isnan(c2).any()
+            assert_close(c2, want2, f"round {rnd}: second GEMM on the first GEMM's output")
+    finally:
+        g1.close()
+        g2.close()
