@@ -28,6 +28,14 @@ constexpr int kSlots = 4;  // problem-table ring: a table is rewritten only afte
 constexpr int kDefaultTileN = 256;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+#ifdef NVFP4_TRACE
+// Timeline build: launch i of the process stores its stamps in block
+// i % g_trace_calls of g_trace (kMaxCtas x kTraceSlots entries each).
+unsigned long long *g_trace = nullptr;
+int g_trace_calls = 0;
+long g_trace_next = 0;
+#endif
 std::once_flag g_encode_once;
 
 bool load_encode()
@@ -101,6 +109,7 @@ struct Slot {
     cudaEvent_t ev = nullptr;
     bool used = false;
     std::vector<const void *> key;
+    GemmParams *params = nullptr;  // the kernel parameters for this table (built when it is filled)
 };
 
 }  // namespace
@@ -247,7 +256,7 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
 }
 
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw, int wide_rows)
+                     const void *SFB, void *C, bool sf_raw)
 {
     if (!load_encode()) return false;
     const uint64_t Mg = (uint64_t)M;
@@ -261,21 +270,22 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
     d.n_chunks = ceil_div(N, kChunkN);
     d.ldc = N;
     d.C = static_cast<uint16_t *>(C);
-    bool ok = encode_2d(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kBoxRows,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&d.tmB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&d.tmBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, wide_rows,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+    bool ok = true;
+    for (int i = 0; i < 2 && ok; ++i)
+        ok = encode_2d(&d.maps.tmA[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, Mg, K / 2, kTileK / 2, kTileM << i,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    for (int i = 0; i < kNumRowBoxes && ok; ++i)
+        ok = encode_2d(&d.maps.tmB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, kChunkN << i,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return false;
     if (sf_raw) {
         const uint32_t sf_box = kSfKTiles * (kTileK / 16);  // bytes of one scale row per box
-        ok = encode_2d(&d.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, sf_box, kBoxRows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-             encode_2d(&d.tmSFB32, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, 32,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-             encode_2d(&d.tmSFBw, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, wide_rows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        for (int i = 0; i < 2 && ok; ++i)
+            ok = encode_2d(&d.maps.tmSFA[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, sf_box, kTileM << i,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+        for (int i = 0; i < kNumRowBoxes && ok; ++i)
+            ok = encode_2d(&d.maps.tmSFB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, kChunkN << i,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
         d.sfa_atoms = static_cast<const uint8_t *>(SFA);
         d.sfb_atoms = static_cast<const uint8_t *>(SFB);
@@ -338,6 +348,7 @@ void release(nvfp4_ggemm_plan_s *p)
         }
         if (s.h_table) cudaFreeHost(s.h_table);
         if (s.d_table) cudaFree(s.d_table);
+        delete s.params;
     }
     if (p->ev_prep) {
         if (p->prep_used) cudaEventSynchronize(p->ev_prep);
@@ -400,7 +411,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
             items += ceil_div(p->M[g], 128) * pieces;
             ++njobs;
         }
-        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->var.max_n)) return false;
+        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused())) return false;
         d.chunk_begin = p->chunk_prefix[g];
         if (ldc) d.ldc = ldc[g];
     }
@@ -497,6 +508,21 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         s.key = key;
         p->cur = slot;
         uploaded = true;
+        // the kernel parameters of this table: start records, the first
+        // groups' tensor maps, pointers into the device copy
+        GemmParams &gp = *s.params;
+        gp = GemmParams{};
+        gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
+        gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
+        pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks, p->shapes.data());
+        const GroupDesc *hg = reinterpret_cast<const GroupDesc *>(s.h_table);
+        for (int g = 0; g < std::min(p->G, kParamGroups); ++g) gp.pmaps[g] = hg[g].maps;
+        gp.err = p->d_err;
+        gp.timeout_ns = p->opt.wait_timeout_ns;
+        gp.G = p->G;
+        gp.cap_single = p->cap_single;
+        gp.cap_pair = p->cap_pair;
+        gp.debug_skip_load = p->opt.debug_skip_load;
     }
     Slot &s = p->slots[slot];
 
@@ -510,17 +536,10 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         if (relayout_launch(rp, p->sm_count, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
     }
 
-    GemmParams gp{};
-    gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
-    gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
-    pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks, p->shapes.data());
-    gp.err = p->d_err;
-    gp.timeout_ns = p->opt.wait_timeout_ns;
-    gp.G = p->G;
-    gp.cap_single = p->cap_single;
-    gp.cap_pair = p->cap_pair;
-    gp.wide_rows = p->var.max_n;
-    gp.debug_skip_load = p->opt.debug_skip_load;
+    GemmParams &gp = *s.params;
+#ifdef NVFP4_TRACE
+    gp.trace = g_trace ? g_trace + (size_t)(g_trace_next++ % g_trace_calls) * kMaxCtas * kTraceSlots : nullptr;
+#endif
     // The GEMM may overlap its set-up with the previous kernel of the stream
     // (it reads only the problem table before that kernel completes). Not
     // right after a table upload: the copy, not a kernel, precedes it then.
@@ -690,7 +709,8 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     bool ok = cudaMalloc(&p->d_err, sizeof(uint32_t)) == cudaSuccess &&
               cudaMemset(p->d_err, 0, sizeof(uint32_t)) == cudaSuccess;
     for (Slot &s : p->slots) {
-        ok = ok && cudaMallocHost(&s.h_table, p->table_bytes) == cudaSuccess &&
+        s.params = new (std::nothrow) GemmParams();
+        ok = ok && s.params && cudaMallocHost(&s.h_table, p->table_bytes) == cudaSuccess &&
              cudaMalloc(&s.d_table, p->table_bytes) == cudaSuccess &&
              cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) == cudaSuccess;
     }
@@ -1072,5 +1092,16 @@ const char *nvfp4_status_string(nvfp4_status_t status)
 }
 
 int nvfp4_ggemm_version(void) { return kVersion; }
+
+#ifdef NVFP4_TRACE
+// Timeline build only: device buffer of calls x kMaxCtas x kTraceSlots
+// 64-bit entries (NULL: off); stamps of the next launches go to it in turn.
+NVFP4_API void nvfp4_debug_trace(void *buf, int calls)
+{
+    g_trace = static_cast<unsigned long long *>(buf);
+    g_trace_calls = calls > 0 ? calls : 1;
+    g_trace_next = 0;
+}
+#endif
 
 }  // extern "C"

@@ -17,8 +17,7 @@ constexpr int kChunkN = 32;        // scheduling grain along N (columns)
 constexpr int kMaxTileN = 256;     // widest output tile any kernel variant supports
 constexpr int kMaxCtas = 192;      // largest persistent grid (the CTA start records travel in the kernel parameters)
 constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B stage
-constexpr int kBoxRows = 128;      // rows of the A and raw SFA TMA boxes: one box per row tile; rows past
-                                   // M_g are the TMA's zero fill (the maps end at M_g), no memory traffic
+constexpr int kNumRowBoxes = 4;    // B / SFB box heights 32, 64, 128, 256 rows (32 << i)
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
 
 // Wait sites recorded in the error word (bits 8-15).
@@ -38,17 +37,54 @@ enum WaitSite : uint32_t {
     kSiteTileCheck = 13, // a tile larger than the CTA's ring slots (never expected)
 };
 
+// Timeline build (compiled with -DNVFP4_TRACE only; the library built for
+// use has none of it): the kernel stores %globaltimer at the points below,
+// one row of kTraceSlots per CTA, into the buffer GemmParams::trace names.
+constexpr int kTraceSlots = 64;
+enum TraceSlot : int {
+    kTrStart = 0,        // CTA entry
+    kTrPrologue = 1,     // after the prologue barrier (TMEM address known)
+    kTrDepWait = 2,      // A producer: released by the previous kernel of the stream
+    kTrBFirst = 3,       // B producer: first load issued
+    kTrAFirst = 4,       // A producer: first load issued
+    kTrSFirst = 5,       // scale producer: first load issued
+    kTrMmaFirstData = 6, // MMA thread: first B stage landed
+    kTrMmaFirstCommit = 7,
+    kTrBLast = 8,        // B producer: last load issued
+    kTrEnd = 9,          // CTA exit (after the final barrier)
+    kTrTiles = 10,       // number of tiles the MMA thread walked
+    kTrStages = 11,      // number of k stages the MMA thread issued
+    kTrSfFirst = 12,     // scale writers: first TMEM scale buffer written
+    kTrSmId = 13,        // the SM the CTA ran on (a value, not a time)
+    kTrBarInit = 14,     // thread 0: barriers initialised
+    kTrTmemAlloc = 15,   // warp 1: TMEM allocated
+    kTrWalked = 57,      // the last producer lane at its first tile
+    kTrTileMmaEnd = 16,  // + tile (< 8): last commit of the tile's MMAs
+    kTrTileEpiStart = 24,// + tile: epilogue warp 2 saw the accumulator full
+    kTrTileEpiEnd = 32,  // + tile: epilogue warp 2 released the accumulator
+    kTrTileFirstData = 40, // + tile: MMA thread saw the tile's first B stage land
+    kTrTileEpiEndAll = 48, // + tile: the last epilogue warp released the accumulator
+};
+
 // One entry of the device-resident problem table. Every tensor map
 // describes one group's buffer exactly, so the TMA zero-fills rows past
-// M_g / N_g. Two B maps: boxes as wide as the kernel's widest tile for
-// full-width tiles, 32-row boxes for the rest.
+// M_g / N_g (no memory traffic). A stage of a tile loads each operand with
+// as few boxes as its row count allows: the tile's one or two 128-row tiles
+// of A (and SFA) in one box of 128 or 256 rows, its 32c columns of B (and
+// SFB) in the boxes of 256, 128, 64 and 32 rows that sum to 32c (at most
+// three). Each TMA instruction costs issue time in the SM's copy unit, so
+// few large boxes keep a CTA's stages at the memory's pace.
+struct alignas(128) GroupMaps {
+    CUtensorMap tmA[2];    // A_g bytes [M_g][K_g/2];  boxes 128 B x 128 / 256 rows; 128-byte swizzle
+    CUtensorMap tmB[kNumRowBoxes];    // B_g bytes [N_g][K_g/2]; boxes 128 B x (32 << i) rows; 128-byte swizzle
+    CUtensorMap tmSFA[2];  // raw SFA_g [M_g][K_g/16]; boxes 32 B x 128 / 256 rows (raw-scale path)
+    CUtensorMap tmSFB[kNumRowBoxes];  // raw SFB_g [N_g][K_g/16]; boxes 32 B x (32 << i) rows (raw-scale path)
+};
+constexpr int kNumMaps = 2 + kNumRowBoxes + 2 + kNumRowBoxes;
+static_assert(sizeof(GroupMaps) == kNumMaps * sizeof(CUtensorMap), "the maps are consecutive");
+
 struct alignas(128) GroupDesc {
-    CUtensorMap tmA;       // A_g bytes [M_g][K_g/2];   box 128 B x 128 rows; 128-byte swizzle
-    CUtensorMap tmB32;     // B_g bytes [N_g][K_g/2];   box 128 B x 32 rows;  128-byte swizzle
-    CUtensorMap tmBw;      // B_g bytes [N_g][K_g/2];   box 128 B x wide rows; 128-byte swizzle
-    CUtensorMap tmSFA;     // raw SFA_g [M_g][K_g/16];  box 32 B x 128 rows   (raw-scale path)
-    CUtensorMap tmSFB32;   // raw SFB_g [N_g][K_g/16];  box 32 B x 32 rows    (raw-scale path)
-    CUtensorMap tmSFBw;    // raw SFB_g [N_g][K_g/16];  box 32 B x wide rows  (raw-scale path)
+    GroupMaps maps;
     const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
     const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
     uint16_t *C;               // C_g fp16 [M_g][ldc], columns [0, N_g) written
@@ -136,7 +172,15 @@ NVFP4_HD int cta_n_chunks(uint32_t packed) { return (int)(packed >> 16); }
 // CTA c takes the chunk range [cta_begin[c], cta_begin[c+1]) and walks it as
 // tiles inside one segment of up to cap_pair chunks (segments with two row
 // tiles, whose accumulators share TMEM) or cap_single chunks (one row tile).
+// The tensor maps of the first kParamGroups groups also travel in the
+// kernel parameters: a map in parameter space needs no proxy fence before
+// the TMA reads it (a map in global memory, written by a host copy, needs an
+// acquire fence, a memory round trip that takes microseconds while the
+// other SMs stream at full bandwidth).
+constexpr int kParamGroups = 8;
+
 struct GemmParams {
+    GroupMaps pmaps[kParamGroups];  // maps of groups 0 .. min(G, kParamGroups) - 1
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
     CtaStart cta[kMaxCtas + 1];    // [grid + 1]
@@ -145,8 +189,10 @@ struct GemmParams {
     int32_t G;
     int32_t cap_single;            // chunks per tile, one row tile (1..MAXN/32)
     int32_t cap_pair;              // chunks per tile, two row tiles
-    int32_t wide_rows;             // rows of the wide B boxes (the kernel's widest tile)
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
+#ifdef NVFP4_TRACE
+    unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null
+#endif
 };
 
 // Fills ranges[0..grid) from cta_begin[0..grid] and the group layout, walking
@@ -219,6 +265,6 @@ TensorMapEncodeFn tensor_map_encoder();  // nullptr when the driver has none
 // Fills one table entry (tensor maps, pointers, counts) for group g with
 // M_g > 0. sf_raw: encode the raw-scale maps; else store the atom pointers.
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw, int wide_rows);
+                     const void *SFB, void *C, bool sf_raw);
 
 }  // namespace nvfp4

@@ -88,6 +88,29 @@ constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 // more stages in flight.
 constexpr int kDoneRing = 16;
 
+// Timeline stamps (the -DNVFP4_TRACE build only; nothing otherwise).
+#ifdef NVFP4_TRACE
+__device__ __forceinline__ void trace_at(const GemmParams &p, int slot)
+{
+    if (p.trace) p.trace[(size_t)blockIdx.x * kTraceSlots + slot] = globaltimer_ns();
+}
+__device__ __forceinline__ void trace_val(const GemmParams &p, int slot, unsigned long long v)
+{
+    if (p.trace) p.trace[(size_t)blockIdx.x * kTraceSlots + slot] = v;
+}
+__device__ __forceinline__ void trace_max(const GemmParams &p, int slot)
+{
+    if (p.trace) atomicMax(p.trace + (size_t)blockIdx.x * kTraceSlots + slot, (unsigned long long)globaltimer_ns());
+}
+#define NVFP4_TRACE_AT(slot) trace_at(p, (slot))
+#define NVFP4_TRACE_VAL(slot, v) trace_val(p, (slot), (v))
+#define NVFP4_TRACE_MAX(slot) trace_max(p, (slot))
+#else
+#define NVFP4_TRACE_AT(slot) ((void)0)
+#define NVFP4_TRACE_VAL(slot, v) ((void)0)
+#define NVFP4_TRACE_MAX(slot) ((void)0)
+#endif
+
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Cfg {
     static_assert(MAXN % 32 == 0 && MAXN >= 32 && MAXN <= kMaxTileN, "tile width");
@@ -383,22 +406,62 @@ __device__ __forceinline__ void sfb_blocks(int n0, int ncols, int N, int &b0, in
     nblk = last / 128 - b0 + 1;
 }
 
-// Per row tile of unit t: the kBoxRows-row boxes that hold rows < M (written
-// to live[]); returns their total.
-__device__ __forceinline__ int row_boxes(const Unit &t, int M, int (&live)[kRowTilesPerUnit])
+// Rows [row0, row0 + 32 * chunks) of an operand (chunks 1..8) in the fewest
+// boxes: 256, 128, 64 and 32 rows from maps[3], maps[2], maps[1], maps[0]
+// (those whose bit is set in `chunks`), placed one after another from dst,
+// `row_bytes` of shared memory per row.
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap *maps, int32_t x, int32_t row0, int chunks,
+                                         uint32_t row_bytes, uint32_t bar, uint64_t policy)
 {
-    int total = 0;
 #pragma unroll
-    for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
-        const int rows = mt < t.mtu ? min(kTileM, M - (t.mt0 + mt) * kTileM) : 0;
-        live[mt] = (rows + kBoxRows - 1) / kBoxRows;
-        total += live[mt];
+    for (int i = kNumRowBoxes - 1; i >= 0; --i) {
+        if (chunks & (1 << i)) {
+            tma_load_2d(dst, maps + i, x, row0, bar, policy);
+            dst += (uint32_t)(kChunkN << i) * row_bytes;
+            row0 += kChunkN << i;
+        }
     }
-    return total;
 }
 
-static_assert(offsetof(GroupDesc, tmSFBw) == offsetof(GroupDesc, tmA) + 5 * sizeof(CUtensorMap),
-              "the six tensor maps are consecutive");
+// The tensor maps of group g: in the kernel parameters for the first
+// kParamGroups groups, else in the problem table.
+__device__ __forceinline__ const GroupMaps *maps_of(const GemmParams &p, int g)
+{
+    return g < kParamGroups ? &p.pmaps[g] : &p.groups[g].maps;
+}
+
+// The maps a producer thread has prepared, for one group at a time: on a
+// map's first use the thread prefetches it, after an acquire fence when the
+// map is in the problem table (written to global memory by a host copy, so
+// the tensormap proxy must be ordered after that write; a memory round trip
+// that can take microseconds while the other SMs stream). Parameter-space
+// maps need no fence. For its first tile a producer does this before it
+// waits for the previous kernel of the stream.
+struct MapUse {
+    int g = -1;
+    uint32_t done = 0;  // bit i: map i of group g prepared
+    __device__ __forceinline__ const CUtensorMap *use(const GroupMaps *gm, int group, const CUtensorMap *m)
+    {
+        if (group != g) {
+            g = group;
+            done = 0;
+        }
+        const uint32_t bit = 1u << (uint32_t)(m - &gm->tmA[0]);
+        if (!(done & bit)) {
+            if (group >= kParamGroups) fence_tensormap_acquire(m);
+            prefetch_tensormap(m);
+            done |= bit;
+        }
+        return m;
+    }
+    // the boxes of tma_rows for `chunks` rows of 32
+    __device__ __forceinline__ void use_rows(const GroupMaps *gm, int group, const CUtensorMap *maps, int chunks)
+    {
+#pragma unroll
+        for (int i = 0; i < kNumRowBoxes; ++i)
+            if (chunks & (1 << i)) use(gm, group, maps + i);
+    }
+};
 
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Roles {
@@ -457,13 +520,6 @@ struct Roles {
     // load, so the small, scattered A and scale reads of the first stage do
     // not queue behind every CTA's burst of B stages at kernel start.
     __device__ __forceinline__ uint32_t first_issued() const { return bar(kBarDone + kDoneRing + 5); }
-    // The group whose tensor maps the kernel prologue has fenced (-1: none).
-    __device__ __forceinline__ int first_group() const
-    {
-        const int g = cta_group(p.cta[blockIdx.x].packed);
-        return g < p.G ? g : -1;
-    }
-
     // Wait until the MMAs of stage j (< 0: none) have completed.
     __device__ __forceinline__ bool wait_done(int j, uint32_t site) const
     {
@@ -503,22 +559,19 @@ struct Roles {
         const uint64_t pol_keep = policy_evict_normal();    // read again by the group's other row tiles
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = first_group(), loads = 0, seq = 0;
+        MapUse maps;
+        int loads = 0, seq = 0;
+        if (have) maps.use_rows(maps_of(p, t.g), t.g, maps_of(p, t.g)->tmB, t.ncols / kChunkN);
         bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
         for (bool more = have; ok && more; more = wk.next(p, t)) {
             if (!tile_fits(t)) {
                 ok = false;
                 break;
             }
-            const GroupDesc *gd = p.groups + t.g;
-            if (t.g != last_g) {
-                fence_tensormap_acquire(&gd->tmB32);
-                fence_tensormap_acquire(&gd->tmBw);
-                last_g = t.g;
-            }
+            const GroupMaps *gm = maps_of(p, t.g);
+            maps.use_rows(gm, t.g, gm->tmB, t.ncols / kChunkN);
             const uint64_t pol = t.keep ? pol_keep : pol_stream;
-            const bool wide = (t.ncols == p.wide_rows);
-            const int boxes = t.ncols / 32;
+            const int chunks = t.ncols / kChunkN;
             const uint32_t bytes = (uint32_t)t.ncols * (kTileK / 2);
             for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_done(seq - nb, kSiteBEmpty)) {
@@ -530,17 +583,13 @@ struct Roles {
                 const bool skip = (p.debug_skip_load > 0 && blockIdx.x == 0 && loads == p.debug_skip_load);
                 if (!skip) {
                     const uint32_t fb = b_full(r.stage);
-                    const uint32_t st = b_stage(r.stage);
                     mbar_arrive_expect_tx(fb, bytes);
-                    if (wide) {
-                        tma_load_2d(st, &gd->tmBw, kt * (kTileK / 2), t.n0, fb, pol);
-                    } else {
-                        for (int i = 0; i < boxes; ++i)
-                            tma_load_2d(st + i * kBRowBoxBytes, &gd->tmB32, kt * (kTileK / 2), t.n0 + 32 * i, fb,
-                                        pol);
-                    }
+                    if (loads == 1) griddep_wait();  // B may be written by the previous kernel
+                    tma_rows(b_stage(r.stage), gm->tmB, kt * (kTileK / 2), t.n0, chunks, kTileK / 2, fb, pol);
                     issued_mask |= 1u << r.stage;
                     issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
+                    if (loads == 1) NVFP4_TRACE_AT(kTrBFirst);
+                    NVFP4_TRACE_AT(kTrBLast);
                 } else {
                     issued_mask &= ~(1u << r.stage);  // nothing in flight for this stage
                 }
@@ -557,7 +606,8 @@ struct Roles {
         const uint64_t pol = policy_evict_last();  // A tiles are re-read by every column tile
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = first_group(), seq = 0;
+        MapUse maps;
+        int seq = 0;
         bool signalled = false;
         bool ok = true;
         for (bool more = have; ok && more; more = wk.next(p, t)) {
@@ -565,31 +615,27 @@ struct Roles {
                 ok = false;
                 break;
             }
-            const GroupDesc *gd = p.groups + t.g;
-            if (t.g != last_g) {
-                fence_tensormap_acquire(&gd->tmA);
-                last_g = t.g;
-            }
-            int live_boxes[kRowTilesPerUnit];
-            const int boxes = row_boxes(t, t.M, live_boxes);
+            const GroupMaps *gm = maps_of(p, t.g);
+            // the unit's one or two 128-row tiles in one box; rows past M_g
+            // are the TMA's zero fill, and their accumulator rows are never stored
+            const CUtensorMap *map = maps.use(gm, t.g, &gm->tmA[t.mtu - 1]);
             for (int kt = 0; kt < t.k_tiles; ++kt) {
                 if (!wait_done(seq - na, kSiteAEmpty)) {
                     ok = false;
                     break;
                 }
                 ++seq;
-                // the boxes that hold rows < M_g; rows past M_g inside a box are
-                // the TMA's zero fill, and their accumulator rows are never stored
                 const uint32_t fb = a_full(r.stage);
-                mbar_arrive_expect_tx(fb, (uint32_t)boxes * (kBoxRows * (kTileK / 2)));
-#pragma unroll
-                for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                    for (int b = 0; b < live_boxes[mt]; ++b)
-                        tma_load_2d(a_stage(r.stage) + mt * kATileBytes + b * (kBoxRows * (kTileK / 2)), &gd->tmA,
-                                    kt * (kTileK / 2), (t.mt0 + mt) * kTileM + b * kBoxRows, fb, pol);
+                mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
+                if (!signalled) {
+                    griddep_wait();  // A may be written by the previous kernel
+                    NVFP4_TRACE_AT(kTrDepWait);
+                }
+                tma_load_2d(a_stage(r.stage), map, kt * (kTileK / 2), t.mt0 * kTileM, fb, pol);
                 if (!signalled) {
                     mbar_arrive(first_issued());
                     signalled = true;
+                    NVFP4_TRACE_AT(kTrAFirst);
                 }
                 issued_mask |= 1u << r.stage;
                 issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
@@ -607,30 +653,26 @@ struct Roles {
         const uint64_t pol = policy_evict_normal();
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int last_g = first_group();
+        MapUse maps;
         bool signalled = false;
         bool ok = true;
 
         for (bool more = have; ok && more; more = wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
-            if (RAW && t.g != last_g) {
-                fence_tensormap_acquire(&gd->tmSFA);
-                fence_tensormap_acquire(&gd->tmSFB32);
-                fence_tensormap_acquire(&gd->tmSFBw);
-                last_g = t.g;
+            const GroupMaps *gm = maps_of(p, t.g);
+            const int chunks = t.ncols / kChunkN;
+            if (RAW) {
+                maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
+                maps.use_rows(gm, t.g, gm->tmSFB, chunks);
             }
-            const bool wide = (t.ncols == p.wide_rows);
-            const int bboxes = t.ncols / 32;
             int b0 = 0, nblk = 0;
             sfb_blocks(t.n0, t.ncols, t.N, b0, nblk);
-            int live_boxes[kRowTilesPerUnit];
-            const int aboxes = row_boxes(t, t.M, live_boxes);
             const size_t katoms = (size_t)(t.k_tiles - 1) * 4 + t.k_last;  // 64-k atoms per 128-row block
             const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;          // scale stages of this tile
             for (int ks = 0; ks < s_tiles; ++ks) {
                 // atom layout: the atoms of k tile ks (fewer in a partial last one)
                 const uint32_t piece = ks + 1 == s_tiles ? (uint32_t)t.k_last * kSfAtomBytes : kSfTileBytes;
-                const uint32_t bytes = RAW ? (uint32_t)(aboxes * kBoxRows + t.ncols) * C::kSfRow
+                const uint32_t bytes = RAW ? (uint32_t)(t.mtu * kTileM + t.ncols) * C::kSfRow
                                            : (uint32_t)(t.mtu + nblk) * piece;
                 if (!wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
                     ok = false;
@@ -639,21 +681,13 @@ struct Roles {
                 const uint32_t fb = s_full(r.stage);
                 const uint32_t st = s_stage(r.stage);
                 mbar_arrive_expect_tx(fb, bytes);
+                if (!signalled) griddep_wait();  // the scales may be written by the previous kernel
                 if (RAW) {
-                    // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1
+                    // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1;
+                    // the unit's row tiles in one box, the tile's columns in the fewest boxes
                     const int x = ks * C::kSfRow;
-#pragma unroll
-                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                        for (int bx = 0; bx < live_boxes[mt]; ++bx)
-                            tma_load_2d(st + mt * C::kSfaTile + bx * (kBoxRows * C::kSfRow), &gd->tmSFA, x,
-                                        (t.mt0 + mt) * kTileM + bx * kBoxRows, fb, pol);
-                    if (wide) {
-                        tma_load_2d(st + C::kSfaBytes, &gd->tmSFBw, x, t.n0, fb, pol);
-                    } else {
-                        for (int i = 0; i < bboxes; ++i)
-                            tma_load_2d(st + C::kSfaBytes + i * (32 * C::kSfRow), &gd->tmSFB32, x, t.n0 + 32 * i, fb,
-                                        pol);
-                    }
+                    tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
+                    tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
                 } else {
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
@@ -669,6 +703,7 @@ struct Roles {
                 if (!signalled) {
                     mbar_arrive(first_issued());
                     signalled = true;
+                    NVFP4_TRACE_AT(kTrSFirst);
                 }
                 issued_mask |= 1u << r.stage;
                 issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
@@ -781,6 +816,7 @@ struct Roles {
                 tc_fence_before_sync();
                 __syncwarp();
                 const bool stage_done = (sub == C::kKS - 1) || (kt == t.k_tiles - 1);
+                if (seq == 1 && lane == 0 && q == 0) NVFP4_TRACE_AT(kTrSfFirst);
                 if (lane == 0) {
                     if (stage_done) mbar_arrive(s_empty(rs.stage));
                     mbar_arrive(sf_ready(rt.stage));
@@ -797,7 +833,7 @@ struct Roles {
     {
         RingPos ra, rb, rt;
         AccTrack acc;
-        int seq = 0;
+        int seq = 0, tile = 0;
         bool ok = true;
         Walker wk(p);
         Unit t;
@@ -818,6 +854,8 @@ struct Roles {
                     break;
                 }
                 tc_fence_after_sync();
+                if (seq == 0) NVFP4_TRACE_AT(kTrMmaFirstData);
+                if (kt == 0 && tile < 8) NVFP4_TRACE_AT(kTrTileFirstData + tile);
                 const uint32_t sa = a_stage(ra.stage);
                 const uint32_t sb = b_stage(rb.stage);
                 const uint32_t sf = tmem + (uint32_t)(C::kSfBase + rt.stage * kSfCols);
@@ -835,6 +873,7 @@ struct Roles {
                 }
                 // the stages and the scale buffer are free once these MMAs have read them
                 tc_commit(done(seq % kDoneRing));
+                if (seq == 0) NVFP4_TRACE_AT(kTrMmaFirstCommit);
                 ++seq;
                 ra.advance(na);
                 rb.advance(nb);
@@ -844,7 +883,11 @@ struct Roles {
             tc_commit(acc_full(h0));
             if (both) tc_commit(acc_full(1));
             acc.advance(h0, both);
+            if (tile < 8) NVFP4_TRACE_AT(kTrTileMmaEnd + tile);
+            ++tile;
         }
+        NVFP4_TRACE_VAL(kTrTiles, (unsigned long long)tile);
+        NVFP4_TRACE_VAL(kTrStages, (unsigned long long)seq);
         // All tcgen05 work issued by this thread completes before TMEM is released.
         tc_commit(drain());
         wait_drain(drain(), 0, p, kSiteMmaDrain);
@@ -859,6 +902,7 @@ struct Roles {
         AccTrack acc;
         Walker wk(p);
         Unit t;
+        int tile = 0;
         while (wk.next(p, t)) {
             const GroupDesc *gd = p.groups + t.g;
             // the tile's C fields are read here, before the accumulator wait:
@@ -873,6 +917,8 @@ struct Roles {
                 (both && !warp_wait_phase(acc_full(1), acc.par(1), abort_flag, p, kSiteAccFull)))
                 break;
             tc_fence_after_sync();
+            if (warp == kWarpEpi0 && lane == 0 && tile < 8) NVFP4_TRACE_AT(kTrTileEpiStart + tile);
+            if (tile == 0) griddep_wait();  // C may be read or written by the previous kernel
             // columns [n0, n0 + 32 * nblk) hold live data; this warp takes blocks
             // h, h + 2, ... with two tcgen05.ld in flight: the next block is read
             // while the current one is converted and stored
@@ -909,8 +955,13 @@ struct Roles {
             if (lane == 0) {
                 mbar_arrive(acc_empty(h0));
                 if (both) mbar_arrive(acc_empty(1));
+                if (tile < 8) {
+                    if (warp == kWarpEpi0) NVFP4_TRACE_AT(kTrTileEpiEnd + tile);
+                    NVFP4_TRACE_MAX(kTrTileEpiEndAll + tile);
+                }
             }
             acc.advance(h0, both);
+            ++tile;
         }
     }
 };
@@ -925,25 +976,20 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    if (threadIdx.x == 0) r.init_barriers();
-    if (warp == kWarpEpi0 && lane < 6) {
-        // The tensor maps of this CTA's first group: one lane per map takes
-        // the tensormap-proxy acquire fence (a round trip to memory each, so
-        // they run side by side here, under the barrier and TMEM set-up, not
-        // one after another in the producers) and starts fetching the map.
-        // The __syncthreads below orders these fences before every
-        // producer's first TMA; the producers fence later groups themselves.
-        const int g = cta_group(p.cta[blockIdx.x].packed);
-        const GroupDesc *gd = p.groups + g;
-        // tmA, tmB32, tmBw, tmSFA, tmSFB32, tmSFBw are consecutive (checked below)
-        if (g < p.G && (RAW || lane < 3)) {
-            fence_tensormap_acquire(&gd->tmA + lane);
-            prefetch_tensormap(&gd->tmA + lane);
-        }
+    if (threadIdx.x == 0) {
+        NVFP4_TRACE_AT(kTrStart);
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        NVFP4_TRACE_VAL(kTrSmId, smid);
+    }
+    if (threadIdx.x == 0) {
+        r.init_barriers();
+        NVFP4_TRACE_AT(kTrBarInit);
     }
     if (warp == kWarpMma) {
         tmem_alloc(r.sbase + C::kOffTmemSlot, kTmemCols);
         tmem_relinquish();
+        if (lane == 0) NVFP4_TRACE_AT(kTrTmemAlloc);
     }
     // The producers walk to their first tile (a chain of single-thread
     // integer arithmetic of about a microsecond) while the barriers and TMEM
@@ -952,19 +998,27 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     Unit t0{};
     bool have0 = false;
     if (lane == 0 && (warp == kWarpBProducer || warp == kWarpAProducer || warp == kWarpSProducer))
+    {
         have0 = wk0.next(p, t0);
+        NVFP4_TRACE_MAX(kTrWalked);
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kOffTmemSlot);
+    if (threadIdx.x == 0) NVFP4_TRACE_AT(kTrPrologue);
     // Launched after another kernel of the stream with programmatic
     // serialisation, everything above (barriers, TMEM, the problem table,
     // tensor-map prefetch, the walk to the first tile) overlaps that kernel's
-    // last CTAs; nothing below (operand loads, C stores) starts before it has
-    // completed. The next kernel may be scheduled from here on: its CTAs
-    // find an SM only as this grid's CTAs exit.
+    // last CTAs. The threads that touch global memory the previous kernel
+    // may use (the three producers before their first load, the epilogue
+    // before its first store) wait for it to complete right there, after
+    // preparing that first load: code and parameters a thread touches for
+    // the first time cost it memory round trips, which are better spent
+    // before the wait than after it. The MMA thread and the scale writers
+    // work on shared memory and TMEM only. The next kernel may be scheduled
+    // from here on: its CTAs find an SM only as this grid's CTAs exit.
     griddep_launch_dependents();
-    griddep_wait();
 
     if (warp == kWarpBProducer) {
         if (lane == 0) r.b_producer(wk0, t0, have0);
@@ -986,6 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (threadIdx.x == 0) NVFP4_TRACE_AT(kTrEnd);
 }
 
 // ------------------------------------------------------------ scale re-layout

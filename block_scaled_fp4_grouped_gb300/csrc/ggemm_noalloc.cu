@@ -20,12 +20,12 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kNoAllocMaxGroups = 64;
-constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 56 KB
+constexpr size_t kTableBytes = sizeof(GroupDesc) * kNoAllocMaxGroups;          // 104 KB
 constexpr size_t kPrefixOffset = kTableBytes;                                   // int32[G+1]
 constexpr size_t kErrOffset = kPrefixOffset + 512;                              // uint32 error word
 constexpr size_t kScratchBytes = kErrOffset + 256;
 static_assert(sizeof(int32_t) * (kNoAllocMaxGroups + 1) <= 512, "prefix area");
-static_assert(kScratchBytes <= 64 * 1024, "the array stays within 64 KB");
+static_assert(kScratchBytes <= 112 * 1024, "the array stays within 112 KB");
 
 // The scratch: problem table, chunk prefix sums, error word (the CTA start
 // records travel in the kernel parameters). In host code this
@@ -87,6 +87,17 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     const int variant = ggemm_variant_index(kMaxTileN, 0, 0, true);
     if (variant < 0) return NVFP4_ERR_CUDA;
 
+    // --- a call made while `stream` is being captured into a graph is refused
+    //     before anything is enqueued: the copy below reads a host buffer
+    //     that later calls rewrite
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    if (capture != cudaStreamCaptureStatusNone) return NVFP4_ERR_INVALID_ARG;
+
     // --- device and one-time set-up
     int dev = -1, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -106,8 +117,8 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     }
     uint8_t *scratch = g_scratch_addr[dev];
 
-    // --- schedule and tensor maps, built in a host buffer on this thread's stack
-    alignas(128) uint8_t table[kTableBytes + 512];
+    // --- schedule and tensor maps, built in a host buffer of this thread
+    alignas(128) static thread_local uint8_t table[kTableBytes + 512];
     std::memset(table, 0, sizeof(table));
     auto *groups = reinterpret_cast<GroupDesc *>(table);
     auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
@@ -124,7 +135,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
         prefix[g] = (int32_t)total;
         total += (long)d.m_pairs * n_chunks;
         if (M[g] == 0) continue;
-        if (!fill_group_desc(d, M[g], N, K, A[g], B[g], SFA[g], SFB[g], C[g], true, kMaxTileN))
+        if (!fill_group_desc(d, M[g], N, K, A[g], B[g], SFA[g], SFB[g], C[g], true))
             return NVFP4_ERR_CUDA;
         d.chunk_begin = prefix[g];
     }
@@ -141,9 +152,9 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     CtaRange ranges[kMaxCtas];
     fill_cta_ranges(ranges, cta_begin, grid, prefix, shapes, num_groups, cap_single, cap_pair);
 
-    // --- upload (pageable source: the call returns once the bytes are staged,
-    //     so the stack buffer may go away), clear the error word, launch
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // --- upload (pageable source: the copy call returns once the bytes are
+    //     staged, so the buffer may be rewritten by the next call), clear the
+    //     error word, launch
     const size_t used = sizeof(GroupDesc) * (size_t)num_groups;
     if (cudaMemcpyAsync(scratch, table, used, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(scratch + kPrefixOffset, prefix, sizeof(int32_t) * (size_t)(num_groups + 1),
@@ -153,6 +164,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
         return NVFP4_ERR_CUDA;
     }
     GemmParams gp{};
+    for (int g = 0; g < std::min(num_groups, kParamGroups); ++g) gp.pmaps[g] = groups[g].maps;
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
     pack_cta_starts(gp.cta, ranges, grid, (int)total, shapes);
@@ -161,7 +173,6 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.G = num_groups;
     gp.cap_single = cap_single;
     gp.cap_pair = cap_pair;
-    gp.wide_rows = kMaxTileN;
     gp.debug_skip_load = 0;
     if (ggemm_launch(variant, gp, grid, s, false) != cudaSuccess) {
         cudaGetLastError();

@@ -311,8 +311,8 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  * not grow the process's device footprint). It computes what
  * nvfp4_ggemm_run computes for raw row-major scales, with the same kernel,
  * but needs no plan: the per-group tensor maps and the device error word it
- * needs live in a static device array of under 64 KB that every GPU loading the
- * library holds until the process exits.
+ * needs live in a static device array of under 112 KB that every GPU loading
+ * the library holds until the process exits.
  *
  * Arguments: as nvfp4_ggemm_plan + nvfp4_ggemm_run (M host array of G row
  * counts, A/B/SFA/SFB/C host arrays of G device pointers, raw scales), on
@@ -324,14 +324,17 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  *
  * The first call on a device looks up the array's device address and
  * configures the kernel; make that first call before any stream capture.
- * Every call reuses the same array (it keeps the last call's contents; the
- * error word is cleared at the start of each call), so calls whose work
- * overlaps on the GPU (different streams, or different host threads) race:
- * serialise them on one stream. Asynchronous on `stream`; if `status_out`
- * is not NULL the call waits for the stream and stores the device error
- * word there (0 = fine), returning NVFP4_ERR_TIMEOUT or
- * NVFP4_ERR_DEVICE_FAULT when it is not 0. Never calls cudaMalloc,
- * cudaFree or any other allocating routine.
+ * A call made while `stream` is being captured returns
+ * NVFP4_ERR_INVALID_ARG and enqueues nothing (its table is staged in a host
+ * buffer that the next call rewrites). Every call reuses the same array (it
+ * keeps the last call's contents; the error word is cleared at the start of
+ * each call), so calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race: serialise them on one stream. Asynchronous
+ * on `stream`; if `status_out` is not NULL the call waits for the stream and
+ * stores the device error word there (0 = fine), returning NVFP4_ERR_TIMEOUT
+ * or NVFP4_ERR_DEVICE_FAULT when it is not 0. A device error of a call made
+ * without `status_out` is not reported: the next call clears the word.
+ * Never calls cudaMalloc, cudaFree or any other allocating routine.
  */
 NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, const int32_t *M, int32_t N, int32_t K,
                                                  const void *const *A, const void *const *B,

@@ -241,7 +241,14 @@ static int sum_is_exact(const double *ad, size_t na, const double *bd, size_t nb
     if (amax == 0.0 || bmax == 0.0) return 1;
     /* every term is a multiple of 2^(alsb+blsb); every partial sum is below K*amax*bmax */
     double span = log2((double)K * amax * bmax) - (double)(alsb + blsb);
+#if ORACLE_MUTANT == 10
+    (void)span;
+    return 1; /* planted: every sum declared exact */
+#elif ORACLE_MUTANT == 11
+    return span < 54.0; /* planted: one bit more than fp64 holds */
+#else
     return span < 52.0;
+#endif
 }
 
 /* --------------------------------------------------------- one group GEMM */

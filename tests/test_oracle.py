@@ -255,6 +255,38 @@ def pin_exact_power_of_two_scales(o):
     assert same_fp16(C, ref.astype(np.float16)).all()
 
 
+def _two_term_rows(K: int, big: int):
+    """One row of A (and the same row of B) whose products are `big` terms of
+    (4 * 2^8)^2 = 2^20 (E2M1 code 6 under scale code 0x78) followed by one
+    term of (0.5 * 2^-9)^2 = 2^-20 (E2M1 code 1 under the smallest E4M3
+    code 0x01), zeros after it. `big` is a multiple of 16."""
+    codes = np.zeros((1, K), np.int64)
+    codes[0, :big] = 6
+    codes[0, big] = 1
+    q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sf = np.full((1, K // 16), 0x38, np.uint8)
+    sf[0, : big // 16] = 0x78
+    sf[0, big // 16] = 0x01
+    return q, sf
+
+
+def pin_exactness_flag(o):
+    """The `exact` flag promises that the fp64 sum in ascending k is the exact
+    real sum. Checked against exact rationals on two rows: 2048 * 2^20 + 2^-20
+    = 2^31 + 2^-20 needs 52 significant bits (fp64 holds 53: the sum is
+    exact, and the flag must say so); 8192 * 2^20 + 2^-20 = 2^33 + 2^-20 needs
+    54 (fp64 rounds the last term away: the flag must be 0)."""
+    for big, want_exact in ((2048, 1), (8192, 0)):
+        K = big + 16
+        q, sf = _two_term_rows(K, big)
+        C, X, exact = o.group_gemm(q, q, sf, sf, K, want_exact=True)
+        true_sum = Fraction(big) * 2 ** 20 + Fraction(1, 2 ** 20)
+        assert (Fraction(float(X[0, 0])) == true_sum) == bool(want_exact), (big, X[0, 0])
+        if exact == 1:  # soundness: a sum declared exact is exact
+            assert Fraction(float(X[0, 0])) == true_sum, (big, exact)
+        assert exact == want_exact, (big, exact)
+
+
 def pin_invariants(o):
     rng = np.random.default_rng(3)
     from block_scaled_fp4_grouped_gb300 import synth
@@ -360,6 +392,7 @@ ALL_PINS = [
     pin_products_16x16,
     pin_matmul_single_group,
     pin_exact_power_of_two_scales,
+    pin_exactness_flag,
     pin_invariants,
     pin_relayout,
 ]

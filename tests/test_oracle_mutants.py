@@ -15,6 +15,8 @@ MUTANTS = {
     7: "E2M1 sign from the wrong bit",
     8: "scale atoms ordered row-block fastest",
     9: "fp16 ties away from zero",
+    10: "every sum declared exact",
+    11: "exactness bound one bit past fp64",
 }
 
 
