@@ -145,10 +145,16 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
         return grid;
     }
     auto seg_cap = [&](int g, int t) { return (shapes[g].m_tiles - t) >= 2 ? cap_pair : cap_single; };
-    // CTAs a segment needs when a CTA may spend `budget` k-stages on it (at least one pass)
+    // CTAs a segment needs when a CTA may spend `budget` k-stages on it (at
+    // least one pass). A CTA that walks two or more tiles of two row tiles
+    // takes them one chunk narrower: such tiles fill both accumulator halves,
+    // so each tile boundary waits for the previous tile's epilogue; narrower
+    // tiles shorten that wait and spread the pair over more CTAs.
     auto ctas_for = [&](int g, int t, long budget) {
         const long passes = std::max<long>(1, budget / shapes[g].k_tiles);
-        const long per_cta = passes * seg_cap(g, t);
+        const bool pair = (shapes[g].m_tiles - t) >= 2;
+        const long cap = seg_cap(g, t);
+        const long per_cta = passes * (pair && passes > 1 && cap > 2 ? cap - 1 : cap);
         return (shapes[g].n_chunks + per_cta - 1) / per_cta;
     };
     auto need = [&](long budget) {

@@ -140,7 +140,7 @@ struct Cfg {
     static constexpr int kOffBars = kOffSRing + NS * kSStage;
     static constexpr int kBRing = NB * kBStage;  // bytes
     static constexpr int kARing = NA * kAStage;
-    static constexpr int kNumBars = kDoneRing + kDoneRing + 2 * NS + kNT + kDoneRing + 2 + 2 + 1 + 1;
+    static constexpr int kNumBars = kDoneRing + kDoneRing + 2 * NS + kNT + kDoneRing + 2 + 2 + 1;
     static constexpr int kOffTmemSlot = kOffBars + 8 * kNumBars;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
@@ -515,11 +515,6 @@ struct Roles {
     __device__ __forceinline__ uint32_t acc_full(int a) const { return bar(kBarDone + kDoneRing + a); }
     __device__ __forceinline__ uint32_t acc_empty(int a) const { return bar(kBarDone + kDoneRing + 2 + a); }
     __device__ __forceinline__ uint32_t drain() const { return bar(kBarDone + kDoneRing + 4); }
-    // The A and scale producers arrive once their first stage is issued (or
-    // when they have none); the B producer waits for it before its first
-    // load, so the small, scattered A and scale reads of the first stage do
-    // not queue behind every CTA's burst of B stages at kernel start.
-    __device__ __forceinline__ uint32_t first_issued() const { return bar(kBarDone + kDoneRing + 5); }
     // Wait until the MMAs of stage j (< 0: none) have completed.
     __device__ __forceinline__ bool wait_done(int j, uint32_t site) const
     {
@@ -547,7 +542,6 @@ struct Roles {
             mbar_init(acc_empty(a), kNumEpiWarps);
         }
         mbar_init(drain(), 1);
-        mbar_init(first_issued(), 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -562,7 +556,7 @@ struct Roles {
         MapUse maps;
         int loads = 0, seq = 0;
         if (have) maps.use_rows(maps_of(p, t.g), t.g, maps_of(p, t.g)->tmB, t.ncols / kChunkN);
-        bool ok = wait_phase(first_issued(), 0, abort_flag, p, kSiteBEmpty);
+        bool ok = true;
         for (bool more = have; ok && more; more = wk.next(p, t)) {
             if (!tile_fits(t)) {
                 ok = false;
@@ -608,7 +602,7 @@ struct Roles {
         uint32_t issued_mask = 0, issued_parity = 0;
         MapUse maps;
         int seq = 0;
-        bool signalled = false;
+        bool first = true;
         bool ok = true;
         for (bool more = have; ok && more; more = wk.next(p, t)) {
             if (!tile_fits(t)) {
@@ -627,14 +621,13 @@ struct Roles {
                 ++seq;
                 const uint32_t fb = a_full(r.stage);
                 mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
-                if (!signalled) {
+                if (first) {
                     griddep_wait();  // A may be written by the previous kernel
                     NVFP4_TRACE_AT(kTrDepWait);
                 }
                 tma_load_2d(a_stage(r.stage), map, kt * (kTileK / 2), t.mt0 * kTileM, fb, pol);
-                if (!signalled) {
-                    mbar_arrive(first_issued());
-                    signalled = true;
+                if (first) {
+                    first = false;
                     NVFP4_TRACE_AT(kTrAFirst);
                 }
                 issued_mask |= 1u << r.stage;
@@ -642,7 +635,6 @@ struct Roles {
                 r.advance(na);
             }
         }
-        if (!signalled) mbar_arrive(first_issued());
         for (int s = 0; s < na; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(a_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
@@ -654,7 +646,7 @@ struct Roles {
         RingPos r;
         uint32_t issued_mask = 0, issued_parity = 0;
         MapUse maps;
-        bool signalled = false;
+        bool first = true;
         bool ok = true;
 
         for (bool more = have; ok && more; more = wk.next(p, t)) {
@@ -681,7 +673,7 @@ struct Roles {
                 const uint32_t fb = s_full(r.stage);
                 const uint32_t st = s_stage(r.stage);
                 mbar_arrive_expect_tx(fb, bytes);
-                if (!signalled) griddep_wait();  // the scales may be written by the previous kernel
+                if (first) griddep_wait();  // the scales may be written by the previous kernel
                 if (RAW) {
                     // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1;
                     // the unit's row tiles in one box, the tile's columns in the fewest boxes
@@ -700,9 +692,8 @@ struct Roles {
                                   gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
                                   piece, fb, pol);
                 }
-                if (!signalled) {
-                    mbar_arrive(first_issued());
-                    signalled = true;
+                if (first) {
+                    first = false;
                     NVFP4_TRACE_AT(kTrSFirst);
                 }
                 issued_mask |= 1u << r.stage;
@@ -710,7 +701,6 @@ struct Roles {
                 r.advance<NS>();
             }
         }
-        if (!signalled) mbar_arrive(first_issued());
         for (int s = 0; s < NS; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
