@@ -221,6 +221,10 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
       copy (it leaves L2 full of dirty lines the call's reads write back).
     * "warm": `steps` calls back to back on one copy, nothing flushed
       (warm L2 as far as the copy fits in it).
+    * "stream_b_static": as "stream", with plans that declare B and SFB
+      static (the b_static option: no kernel before a call writes them, as
+      for model weights), so each call streams B while the previous one
+      finishes. Reported beside the headline, not as it.
     Problems too small for 64 copies to cover 3x the L2 (c0) run "flush"
     and "warm" only, and report "flush" as the headline.
     Host cost: the enqueue time of one call (the C call from Python, plan
@@ -245,39 +249,44 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
             SFB = [_atom(torch, nb, s, N, K) for s in SFB]
         C = [torch.empty((m, N), dtype=torch.float16, device="cuda") for m in prob.M]
         gg = nb.GroupedGemm(prob.M, N, K, **kw)
+        gs = nb.GroupedGemm(prob.M, N, K, **dict(kw, b_static=True))
         if kw.get("cache_b_scales"):
             gg.prepare_b_scales(SFB)
+            gs.prepare_b_scales(SFB)
             SFB_run = [None] * len(SFB)
         else:
             SFB_run = SFB
-        return gg, gg.bind(A, B, SFA, SFB_run, C)
+        return gg, gg.bind(A, B, SFA, SFB_run, C), gs, gs.bind(A, B, SFA, SFB_run, C)
 
     sets = [make_set() for _ in range(n_sets)]
     info = sets[0][0].info()
     stream = torch.cuda.current_stream()
 
     def check():
-        for gg, _ in sets:
-            st, detail = gg.sync_status()
-            if st != nb.NVFP4_OK:
-                raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
+        for gg, _, gs, _ in sets:
+            for plan in (gg, gs):
+                st, detail = plan.sync_status()
+                if st != nb.NVFP4_OK:
+                    raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
 
     # warm-up: every copy at least once (uploads its table), then W calls;
     # the enqueue time of a call is taken here too
     enq = []
     for i in range(max(warmup, len(sets))):
-        _, call = sets[i % len(sets)]
+        _, call, _, call_s = sets[i % len(sets)]
         torch.cuda._sleep(SLEEP_CYCLES)
         t0 = time.perf_counter()
         call()
         enq.append(time.perf_counter() - t0)
+        call_s()
     torch.cuda.synchronize()
     check()
     enqueue_s = statistics.median(enq[len(sets):] or enq)
 
-    def stream_block(order):
-        """Calls sets[order[i]] back to back between one event pair. Returns
-        (µs per call, whether the device waited for the host)."""
+    def stream_block(order, which=1):
+        """Calls sets[order[i]] back to back between one event pair (which: 1
+        the default plans, 3 the plans that declare B static). Returns (µs
+        per call, whether the device waited for the host)."""
         sleep_ns = 50e3 + 3.0 * enqueue_s * 1e9 * len(order)
         for _attempt in range(4):
             start = torch.cuda.Event(enable_timing=True)
@@ -286,7 +295,7 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
             torch.cuda._sleep(int(min(sleep_ns, MAX_STREAM_SLEEP_NS) * SM_GHZ_FOR_SLEEP))
             start.record(stream)
             for j in order:
-                sets[j][1]()
+                sets[j][which]()
             end.record(stream)
             late = start.query()  # the timed region had begun before the last call was enqueued
             torch.cuda.synchronize()
@@ -300,7 +309,7 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         torch.cuda.synchronize()
         for i in range(steps):
-            _, call = sets[i % len(sets)] if mode == "isolated" else sets[0]
+            call = sets[i % len(sets)][1] if mode == "isolated" else sets[0][1]
             if mode == "flush":
                 flush.zero_()
             else:
@@ -319,6 +328,8 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
     if rotate_ok:
         us, late = stream_block([i % len(sets) for i in range(steps)])
         by["stream"] = {"us_mean": us, "host_bound": bool(late)}
+        us, late = stream_block([i % len(sets) for i in range(steps)], which=3)
+        by["stream_b_static"] = {"us_mean": us, "host_bound": bool(late)}
         v = per_call("isolated")
         by["isolated"] = {"us_mean": statistics.fmean(v), "us_median": statistics.median(v), "us_min": min(v),
                           "us_p90": sorted(v)[int(0.9 * (len(v) - 1))]}
@@ -333,7 +344,7 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
     out["us_mean"] = by[out["headline"]]["us_mean"]
     out["by"] = by
     # host cost per call with the plan cached
-    _, call = sets[0]
+    call = sets[0][1]
     torch.cuda.synchronize()
     walls = []
     for _ in range(host_calls):
@@ -344,8 +355,9 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
     out["host"] = {"enqueue_us": enqueue_s * 1e6, "call_and_sync_us": statistics.median(walls) * 1e6}
     if want_e2e:
         out["e2e"] = time_e2e(prob, kw, steps, warmup, torch, nb)
-    for gg, _ in sets:
+    for gg, _, gs, _ in sets:
         gg.close()
+        gs.close()
     return out
 
 
@@ -536,6 +548,10 @@ def main():
                        b_stages=r["info"].b_stages, a_stages=r["info"].a_stages,
                        parallelism=f"replicas x{world}"),
         "us_isolated_call": {k: round(v, 2) for k, v in iso.items()},
+        "us_b_static": (round(r["by"]["stream_b_static"]["us_mean"], 2) if "stream_b_static" in r["by"] else None),
+        "b_static_note": ("the same back-to-back calls with the b_static option (the caller declares B and "
+                          "SFB unwritten by the previous kernel, as for inference weights): each call streams "
+                          "B while the previous call's last CTAs finish; A, SFA and C still wait"),
         "us_by_protocol": {m: {k: (round(v, 2) if isinstance(v, float) else v) for k, v in d.items()}
                            for m, d in r["by"].items()},
         "host_us_per_call": {k: round(v, 2) for k, v in r["host"].items()},

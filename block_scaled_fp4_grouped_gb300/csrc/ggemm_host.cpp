@@ -386,6 +386,7 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
         return NVFP4_ERR_INVALID_ARG;
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
+    if (out->b_static != 0 && out->b_static != 1) return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
     return NVFP4_OK;
 }
@@ -476,7 +477,7 @@ nvfp4_status_t check_group_ptrs(nvfp4_ggemm_plan_s *p, const void *const *A, con
 
 nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const void *const *B,
                           const void *const *SFA, const void *const *SFB, void *const *C, const int32_t *ldc,
-                          cudaStream_t stream, bool force_sfb)
+                          cudaStream_t stream, bool force_sfb, bool early_ok = true)
 {
     const bool sfb_cached = p->relayout() && p->opt.cache_b_scales && !force_sfb;
     if (sfb_cached && !p->b_prepared) return NVFP4_ERR_NOT_PREPARED;
@@ -543,6 +544,10 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     }
 
     GemmParams &gp = *s.params;
+    // Loads that may start before the previous kernel completes (the caller's
+    // b_static): B, and SFB unless the re-layout kernel that runs just before
+    // the GEMM writes it. Never behind run_host's own copy of the inputs.
+    gp.b_static = (early_ok && p->opt.b_static) ? (p->relayout() ? 1 : 2) : 0;
 #ifdef NVFP4_TRACE
     gp.trace = g_trace ? g_trace + (size_t)(g_trace_next++ % g_trace_calls) * kMaxCtas * kTraceSlots : nullptr;
 #endif
@@ -575,6 +580,7 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->b_stages = 0;
     opt->a_stages = 0;
     opt->serial_launch = 0;
+    opt->b_static = 0;
 }
 
 nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,
@@ -919,7 +925,7 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
             cudaGetLastError();
             return NVFP4_ERR_CUDA;
         }
-        nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true);
+        nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true, false);
         if (st != NVFP4_OK) {
             cudaGetLastError();
             return st;
@@ -943,7 +949,7 @@ nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const void *const *
             return NVFP4_ERR_CUDA;
         }
     }
-    nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true);
+    nvfp4_status_t st = run_device(p, dA.data(), dB.data(), dSFA.data(), dSFB.data(), dC.data(), nullptr, s, true, false);
     if (st != NVFP4_OK) {
         cudaGetLastError();
         return st;

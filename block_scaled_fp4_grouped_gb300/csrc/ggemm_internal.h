@@ -190,6 +190,7 @@ struct GemmParams {
     int32_t cap_single;            // chunks per tile, one row tile (1..MAXN/32)
     int32_t cap_pair;              // chunks per tile, two row tiles
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
+    int32_t b_static;              // B (1), or B and SFB (2), are loaded before the previous kernel completes
 #ifdef NVFP4_TRACE
     unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null
 #endif

@@ -578,7 +578,8 @@ struct Roles {
                 if (!skip) {
                     const uint32_t fb = b_full(r.stage);
                     mbar_arrive_expect_tx(fb, bytes);
-                    if (loads == 1) griddep_wait();  // B may be written by the previous kernel
+                    // B may be written by the previous kernel, unless the caller says otherwise
+                    if (loads == 1 && !p.b_static) griddep_wait();
                     tma_rows(b_stage(r.stage), gm->tmB, kt * (kTileK / 2), t.n0, chunks, kTileK / 2, fb, pol);
                     issued_mask |= 1u << r.stage;
                     issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
@@ -673,24 +674,34 @@ struct Roles {
                 const uint32_t fb = s_full(r.stage);
                 const uint32_t st = s_stage(r.stage);
                 mbar_arrive_expect_tx(fb, bytes);
-                if (first) griddep_wait();  // the scales may be written by the previous kernel
-                if (RAW) {
-                    // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1;
-                    // the unit's row tiles in one box, the tile's columns in the fewest boxes
-                    const int x = ks * C::kSfRow;
-                    tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
-                    tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
-                } else {
+                // the scales may be written by the previous kernel; B's scales are
+                // loaded before waiting for it when the caller says they are not
+                const bool sfb_early = first && p.b_static == 2;
+                for (int part = 0; part < 2; ++part) {
+                    const bool sfb_now = part == 0 ? sfb_early : !sfb_early;
+                    if (part == 1 && first) griddep_wait();
+                    if (RAW) {
+                        // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1;
+                        // the unit's row tiles in one box, the tile's columns in the fewest boxes
+                        const int x = ks * C::kSfRow;
+                        if (part == 1) tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
+                        if (sfb_now) tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
+                    } else {
+                        if (part == 1) {
 #pragma unroll
-                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                        if (mt < t.mtu)
-                            bulk_load(st + mt * kSfTileBytes,
-                                      gd->sfa_atoms + ((size_t)(t.mt0 + mt) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                      piece, fb, pol);
-                    for (int b = 0; b < nblk; ++b)
-                        bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
-                                  gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                  piece, fb, pol);
+                            for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+                                if (mt < t.mtu)
+                                    bulk_load(st + mt * kSfTileBytes,
+                                              gd->sfa_atoms +
+                                                  ((size_t)(t.mt0 + mt) * katoms + (size_t)ks * 4) * kSfAtomBytes,
+                                              piece, fb, pol);
+                        }
+                        if (sfb_now)
+                            for (int b = 0; b < nblk; ++b)
+                                bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
+                                          gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
+                                          piece, fb, pol);
+                    }
                 }
                 if (first) {
                     first = false;

@@ -123,7 +123,13 @@ typedef struct {
                                  CTAs finish (programmatic dependent launch); its loads and
                                  stores still wait until that kernel has completed. 1: plain
                                  launches, every kernel starts after the previous one ends */
-    int32_t reserved[2];
+    int32_t b_static;         /* 0 (default), or 1: the caller guarantees that no kernel that may
+                                 still run when this GEMM starts (the kernel before it on its
+                                 stream) writes B or SFB, e.g. model weights in inference. The
+                                 GEMM then starts streaming B and SFB before that kernel has
+                                 completed, during its last CTAs; A, SFA and the C stores still
+                                 wait for it. With serial_launch the flag has no effect */
+    int32_t reserved[1];
 } nvfp4_ggemm_options_t;
 
 typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;

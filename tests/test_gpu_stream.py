@@ -31,8 +31,12 @@ def _new_inputs(prob, seed):
     return other
 
 
-@pytest.mark.parametrize("serial", [False, True], ids=["overlapped", "plain"])
-def test_second_gemm_reads_what_the_first_wrote(serial):
+@pytest.mark.parametrize("serial,b_static", [(False, False), (True, False), (False, True)],
+                         ids=["overlapped", "plain", "overlapped_b_static"])
+def test_second_gemm_reads_what_the_first_wrote(serial, b_static):
+    """b_static (B and SFB never written by the previous kernel) lets a GEMM
+    stream B before the previous kernel completes; A, which the previous
+    kernel writes here, must still be read only after it."""
     import torch
     from block_scaled_fp4_grouped_gb300 import binding as nb
     # first GEMM: one group, 256 x 4096 x 7168 (a few microseconds of work)
@@ -44,8 +48,8 @@ def test_second_gemm_reads_what_the_first_wrote(serial):
     A2 = [C1[0].view(torch.uint8).reshape(-1)[: 256 * 4096].view(256, 4096)]
     B2, SFA2, SFB2 = to_device(p2.B), to_device(p2.SFA), to_device(p2.SFB)
     C2 = [torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")]
-    g1 = nb.GroupedGemm(p1.M, p1.N, p1.K, serial_launch=serial)
-    g2 = nb.GroupedGemm(p2.M, p2.N, p2.K, serial_launch=serial)
+    g1 = nb.GroupedGemm(p1.M, p1.N, p1.K, serial_launch=serial, b_static=b_static)
+    g2 = nb.GroupedGemm(p2.M, p2.N, p2.K, serial_launch=serial, b_static=b_static)
     try:
         call1 = g1.bind(A1, B1, SFA1, SFB1, C1)
         call2 = g2.bind(A2, B2, SFA2, SFB2, C2)
