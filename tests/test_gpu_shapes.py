@@ -183,6 +183,9 @@ SHAPES_K64 = [  # (M_g, N_g, K_g): most K_g are not multiples of 256
     (17, 8, 128),
     (96, 520, 256),
     (33, 4096, 448),
+    (3, 64, 320),
+    (1, 40, 64),
+    (6, 96, 1216),
 ]
 
 
@@ -226,6 +229,27 @@ def test_k_multiple_of_64_uniform_and_exact(O):
     got = run_gpu(prob)
     for g in range(prob.G):
         assert np.array_equal(got[g].view(np.uint16), ref[g].view(np.uint16)), f"group {g}"
+
+
+def test_k_multiple_of_64_mixed_with_256_bit_exact(O):
+    """One plan whose groups mix K_g % 256 == 0 and K_g % 256 != 0 (so raw
+    scales take the re-layout path for all of them), M_g % 4 != 0 and
+    M_g < 4, with power-of-two scales of span 4 so that every fp32 partial
+    sum is exact: the GPU must equal the oracle bit for bit, every row of
+    every group."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    shapes = [(141, 392, 704), (3, 64, 320), (66, 256, 512), (299, 128, 1088), (7, 520, 64), (130, 200, 1024)]
+    parts = [synth.make_problem("custom", seed=1200 + g, M=[m], N=n, K=k) for g, (m, n, k) in enumerate(shapes)]
+    rng = np.random.default_rng(1200)
+    for p in parts:
+        p.SFA[0] = (((rng.integers(-2, 2, p.SFA[0].shape) + 7) << 3)).astype(np.uint8)
+        p.SFB[0] = (((rng.integers(-2, 2, p.SFB[0].shape) + 7) << 3)).astype(np.uint8)
+    with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts]) as gg:
+        assert gg.info().sf_path == nb.NVFP4_SF_RELAYOUT and gg.info().kernels_per_run == 2
+    got = _run(parts)
+    for g, p in enumerate(parts):
+        ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
+        assert np.array_equal(got[g].view(np.uint16), ref.view(np.uint16)), f"group {g} {shapes[g]}"
 
 
 @pytest.mark.parametrize("layout", ["raw", "atom"])
