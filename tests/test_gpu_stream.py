@@ -9,7 +9,10 @@ contents of that buffer. Both plans' tables are uploaded by a first round
 of calls; the checked round changes the first GEMM's inputs with a torch
 kernel and then enqueues both GEMMs with nothing between them, so both
 launches overlap their predecessor. The expected values are the oracle's on
-the bytes read back after the stream has drained."""
+the bytes read back after the stream has drained. A second test does the same
+for the scale re-layout kernel that K % 256 != 0 puts ahead of the GEMM: it
+must read scales a kernel wrote just before it only after that kernel has
+completed."""
 import numpy as np
 import pytest
 
@@ -84,6 +87,60 @@ def test_second_gemm_reads_what_the_first_wrote(serial, b_static):
             want2, _, _ = O.group_gemm(a2, p2.B[0], p2.SFA[0], p2.SFB[0], p2.K)
             assert not np.isnan(c2).any()
             assert_close(c2, want2, f"round {rnd}: second GEMM on the first GEMM's output")
+    finally:
+        g1.close()
+        g2.close()
+
+
+@pytest.mark.parametrize("cached", [False, True], ids=["relayout", "relayout_cached_b_scales"])
+def test_relayout_reads_scales_the_previous_kernel_wrote(cached):
+    """K % 256 != 0 runs the scale re-layout kernel ahead of the GEMM, both
+    launched to overlap their predecessor. Here a torch kernel writes the
+    second GEMM's A scales (from the first GEMM's output, masked to finite
+    E4M3 codes) right before the call, so a re-layout kernel that read its
+    input before that kernel completed would see the previous contents."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    p1 = synth.make_problem("custom", seed=43, M=[256], N=4096, K=7168)
+    A1, B1, SFA1, SFB1 = to_device(p1.A), to_device(p1.B), to_device(p1.SFA), to_device(p1.SFB)
+    C1 = [torch.zeros((256, 4096), dtype=torch.float16, device="cuda")]
+    K2 = 8128  # K % 256 == 192: the re-layout path
+    p2 = synth.make_problem("custom", seed=44, M=[256], N=512, K=K2)
+    c1_bytes = C1[0].view(torch.uint8).reshape(-1)
+    A2 = [c1_bytes[: 256 * K2 // 2].view(256, K2 // 2)]
+    src_sfa = c1_bytes[1 << 20: (1 << 20) + 256 * K2 // 16].view(256, K2 // 16)
+    SFA2 = [torch.zeros((256, K2 // 16), dtype=torch.uint8, device="cuda")]
+    B2, SFB2 = to_device(p2.B), to_device(p2.SFB)
+    C2 = [torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")]
+    g1 = nb.GroupedGemm(p1.M, p1.N, p1.K)
+    g2 = nb.GroupedGemm(p2.M, p2.N, K2, cache_b_scales=cached)
+    try:
+        assert g2.info().sf_path == nb.NVFP4_SF_RELAYOUT and g2.info().kernels_per_run == 2
+        if cached:
+            g2.prepare_b_scales(SFB2)
+        call1 = g1.bind(A1, B1, SFA1, SFB1, C1)
+        call2 = g2.bind(A2, B2, SFA2, SFB2, C2)
+        call1()
+        call2()
+        torch.cuda.synchronize()
+        for rnd in range(3):
+            q = _new_inputs(p1, 200 + rnd)
+            a_new = torch.from_numpy(q.A[0]).cuda()
+            torch.cuda.synchronize()
+            torch.bitwise_xor(a_new, 0, out=A1[0])
+            call1()
+            # finite scale codes (sign 0, exponent <= 5) from the first GEMM's output
+            torch.bitwise_and(src_sfa, 0x2F, out=SFA2[0])
+            call2()
+            for gg in (g1, g2):
+                st, word = gg.sync_status()
+                assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+            a2 = A2[0].cpu().numpy()
+            sfa2 = SFA2[0].cpu().numpy()
+            c2 = C2[0].cpu().numpy()
+            want2, _, _ = oracle.get().group_gemm(a2, p2.B[0], sfa2, p2.SFB[0], K2)
+            assert not np.isnan(c2).any()
+            assert_close(c2, want2, f"round {rnd}: re-layout of scales the previous kernel wrote")
     finally:
         g1.close()
         g2.close()
