@@ -15,7 +15,10 @@ import os
 from typing import List, Optional, Sequence, Tuple
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libnvfp4_ggemm.so")
+# NVFP4_GGEMM_LIB names another build of the library to load instead (for
+# example the device-check build, libnvfp4_ggemm_debug.so)
+LIB_PATH = os.environ.get("NVFP4_GGEMM_LIB") or os.path.join(_PKG, "libnvfp4_ggemm.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "libnvfp4_ggemm_debug.so")
 
 NVFP4_OK = 0
 NVFP4_ERR_INVALID_ARG = 1
@@ -69,7 +72,7 @@ class nvfp4_ggemm_options_t(ctypes.Structure):
         ("a_stages", ctypes.c_int32),
         ("serial_launch", ctypes.c_int32),
         ("b_static", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 1),
+        ("debug_check_fail", ctypes.c_int32),
     ]
 
 
@@ -340,7 +343,8 @@ def nvfp4_ggemm_schedule(M: Sequence[int], N, tile_n: int = 0, max_ctas: int = 1
 def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales: bool = False,
                  wait_timeout_ns: int = 0, tile_n: int = 0, max_ctas: int = 0,
                  debug_skip_load: int = 0, b_stages: int = 0, a_stages: int = 0,
-                 serial_launch: bool = False, b_static: bool = False) -> nvfp4_ggemm_options_t:
+                 serial_launch: bool = False, b_static: bool = False,
+                 debug_check_fail: int = 0) -> nvfp4_ggemm_options_t:
     opt = nvfp4_ggemm_default_options()
     opt.sf_layout = {"raw": NVFP4_SF_RAW, "atom": NVFP4_SF_ATOM}[sf_layout]
     opt.sf_path = {"fused": NVFP4_SF_FUSED, "relayout": NVFP4_SF_RELAYOUT}[sf_path]
@@ -354,6 +358,7 @@ def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales:
     opt.a_stages = int(a_stages)
     opt.serial_launch = 1 if serial_launch else 0
     opt.b_static = 1 if b_static else 0
+    opt.debug_check_fail = int(debug_check_fail)
     return opt
 
 

@@ -1,10 +1,15 @@
 """Build libnvfp4_ggemm.so in-tree with nvcc for sm_103a.
 
-    python -m block_scaled_fp4_grouped_gb300.build [--force] [--verbose]
+    python -m block_scaled_fp4_grouped_gb300.build [--force] [--verbose] [--debug]
 
 Each translation unit is compiled in parallel to an object under `_build/`,
 then linked (CUDA runtime linked statically; the driver's tensor-map encoder
 is fetched at run time, so loading the library needs no GPU driver).
+--debug builds libnvfp4_ggemm_debug.so (objects under `_build_debug/`) with
+-DNVFP4_DEBUG: the GEMM kernel then checks every shared-memory and TMEM
+range, TMA coordinate and alignment before the operation it guards, and a
+failed check is reported through the plan's error word (the operation is
+skipped and the kernel ends through its abort flag) instead of running.
 """
 from __future__ import annotations
 
@@ -21,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4_ggemm.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libnvfp4_ggemm_debug.so")
 
 SOURCES = ["ggemm_kernels.cu", "ggemm_host.cpp", "ggemm_noalloc.cu", "io_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,9 +48,9 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + COMMON
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.basename(src) + ".o")
+    cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + COMMON + (["-DNVFP4_DEBUG"] if debug else [])
     if src.endswith(".cu"):
         cmd += ARCH
         if verbose:
@@ -56,25 +63,28 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libnvfp4_ggemm.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile (if stale) and return the path of libnvfp4_ggemm.so, or of
+    libnvfp4_ggemm_debug.so with debug."""
+    lib, out_dir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), SOURCES))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true", help="print ptxas register/smem usage")
+    ap.add_argument("--debug", action="store_true", help="the device-check build, libnvfp4_ggemm_debug.so")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, debug=a.debug))

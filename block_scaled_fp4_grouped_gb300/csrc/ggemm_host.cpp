@@ -387,6 +387,8 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
     if (out->b_static != 0 && out->b_static != 1) return NVFP4_ERR_INVALID_ARG;
+    if (out->debug_check_fail != 0 && (out->debug_check_fail < kSiteCheckLoadB || out->debug_check_fail > kSiteCheckEpi))
+        return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
     return NVFP4_OK;
 }
@@ -530,6 +532,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         gp.cap_single = p->cap_single;
         gp.cap_pair = p->cap_pair;
         gp.debug_skip_load = p->opt.debug_skip_load;
+        gp.debug_check_fail = p->opt.debug_check_fail;
     }
     Slot &s = p->slots[slot];
 

@@ -35,6 +35,14 @@ enum WaitSite : uint32_t {
     kSiteSEmpty = 11,    // scale producer waiting for a free scale stage
     kSiteSFull = 12,     // scale writers waiting for a scale stage
     kSiteTileCheck = 13, // a tile larger than the CTA's ring slots (never expected)
+    // device checks of the debug build (-DNVFP4_DEBUG), each guarding one
+    // kind of operation; a failed check skips the operation
+    kSiteCheckLoadB = 0x21,  // B stage load: shared-memory range, 1024-byte alignment, 16-byte x
+    kSiteCheckLoadA = 0x22,  // A stage load: the same
+    kSiteCheckLoadSf = 0x23, // scale stage loads: range inside the stage, source alignment
+    kSiteCheckMma = 0x24,    // a stage's MMAs: accumulator and scale columns in TMEM, operand ranges
+    kSiteCheckSfSt = 0x25,   // scale writers: TMEM scale-buffer columns
+    kSiteCheckEpi = 0x26,    // epilogue: accumulator columns read, C row alignment of wide stores
 };
 
 // Timeline build (compiled with -DNVFP4_TRACE only; the library built for
@@ -191,6 +199,7 @@ struct GemmParams {
     int32_t cap_pair;              // chunks per tile, two row tiles
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
     int32_t b_static;              // B (1), or B and SFB (2), are loaded before the previous kernel completes
+    int32_t debug_check_fail;      // debug build, test only: the check site forced to fail (0 = none)
 #ifdef NVFP4_TRACE
     unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null
 #endif

@@ -111,6 +111,21 @@ __device__ __forceinline__ void trace_max(const GemmParams &p, int slot)
 #define NVFP4_TRACE_MAX(slot) ((void)0)
 #endif
 
+// Device checks of the debug build (-DNVFP4_DEBUG): NVFP4_CHECK(cond, site)
+// is a Roles member call that, when cond is false (or the test-only option
+// names the site), records (device fault, site) in the error word, raises the
+// CTA's abort flag and returns false, and the caller skips the operation it
+// guards; NVFP4_CHECK_WARP is the same for a whole warp, true only if it
+// holds on every lane. In the release build both are the constant true and
+// cost nothing.
+#ifdef NVFP4_DEBUG
+#define NVFP4_CHECK(cond, site) check((cond), (site))
+#define NVFP4_CHECK_WARP(cond, site) __all_sync(0xffffffffu, check((cond), (site)))
+#else
+#define NVFP4_CHECK(cond, site) true
+#define NVFP4_CHECK_WARP(cond, site) true
+#endif
+
 template <int MAXN, int NB, int NA, int NS, bool RAW>
 struct Cfg {
     static_assert(MAXN % 32 == 0 && MAXN >= 32 && MAXN <= kMaxTileN, "tile width");
@@ -504,6 +519,22 @@ struct Roles {
         return false;
     }
 
+#ifdef NVFP4_DEBUG
+    __device__ __forceinline__ bool check(bool cond, uint32_t site) const
+    {
+        if (cond && p.debug_check_fail != (int)site) return true;
+        record_error(p.err, kStatusFault, site);
+        *abort_flag = 1;
+        return false;
+    }
+#endif
+    // `bytes` of shared memory from dst lie inside [sbase + lo, sbase + hi)
+    // and dst is 1024-byte aligned (the 128-byte swizzle's atom)
+    __device__ __forceinline__ bool smem_in(uint32_t dst, uint32_t bytes, int lo, int hi) const
+    {
+        return dst >= sbase + (uint32_t)lo && dst + bytes <= sbase + (uint32_t)hi && (dst & 1023u) == 0;
+    }
+
     static constexpr int kBarDone = 2 * kDoneRing + 2 * NS + NT;
     __device__ __forceinline__ uint32_t bar(int i) const { return sbase + C::kOffBars + 8 * i; }
     __device__ __forceinline__ uint32_t b_full(int s) const { return bar(s); }
@@ -574,7 +605,12 @@ struct Roles {
                 }
                 ++seq;
                 ++loads;
-                const bool skip = (p.debug_skip_load > 0 && blockIdx.x == 0 && loads == p.debug_skip_load);
+                const bool skip =
+                    (p.debug_skip_load > 0 && blockIdx.x == 0 && loads == p.debug_skip_load) ||
+                    !NVFP4_CHECK(smem_in(b_stage(r.stage), bytes, C::kOffBRing, C::kOffBRing + C::kBRing) &&
+                                     chunks >= 1 && chunks <= MAXN / kChunkN && t.n0 >= 0 &&
+                                     ((kt * (kTileK / 2)) & 15) == 0,
+                                 kSiteCheckLoadB);
                 if (!skip) {
                     const uint32_t fb = b_full(r.stage);
                     mbar_arrive_expect_tx(fb, bytes);
@@ -620,6 +656,13 @@ struct Roles {
                     break;
                 }
                 ++seq;
+                if (!NVFP4_CHECK(smem_in(a_stage(r.stage), (uint32_t)t.mtu * kATileBytes, C::kOffARing,
+                                         C::kOffARing + C::kARing) &&
+                                     t.mtu >= 1 && t.mtu <= kRowTilesPerUnit && t.mt0 >= 0,
+                                 kSiteCheckLoadA)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t fb = a_full(r.stage);
                 mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
                 if (first) {
@@ -673,6 +716,18 @@ struct Roles {
                 }
                 const uint32_t fb = s_full(r.stage);
                 const uint32_t st = s_stage(r.stage);
+                if (!NVFP4_CHECK(st >= sbase + C::kOffSRing && st + C::kSStage <= sbase + C::kOffSRing + NS * C::kSStage &&
+                                     (RAW ? (uint32_t)t.mtu * kTileM * C::kSfRow <= (uint32_t)C::kSfaBytes &&
+                                                (uint32_t)t.ncols * C::kSfRow <= (uint32_t)C::kSfbRegion &&
+                                                ((ks * C::kSfRow) & 15) == 0
+                                          : nblk >= 1 && nblk * kSfTileBytes <= C::kSfbRegion &&
+                                                (piece & 15u) == 0 &&
+                                                ((reinterpret_cast<uintptr_t>(gd->sfa_atoms) |
+                                                  reinterpret_cast<uintptr_t>(gd->sfb_atoms)) & 15u) == 0),
+                                 kSiteCheckLoadSf)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(fb, bytes);
                 // the scales may be written by the previous kernel; B's scales are
                 // loaded before waiting for it when the caller says they are not
@@ -810,6 +865,10 @@ struct Roles {
                     break;
                 }
                 const uint32_t col = (uint32_t)(C::kSfBase + rt.stage * kSfCols);
+                if (!NVFP4_CHECK_WARP(col >= (uint32_t)C::kSfBase && col + kSfCols <= kTmemCols, kSiteCheckSfSt)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + col;
                 tmem_st_32x32b_x32(taddr, va);
                 tmem_st_32x32b_x32(taddr + 32, vb);
@@ -862,8 +921,17 @@ struct Roles {
                 const uint32_t sf = tmem + (uint32_t)(C::kSfBase + rt.stage * kSfCols);
                 // a last k tile of K % 256 != 0 holds fewer live 64-k slices
                 const int slices = kt + 1 == t.k_tiles ? t.k_last : 4;
+                // (debug build) accumulator and scale columns inside their TMEM
+                // regions, operands inside their rings; a failed check skips
+                // the stage's MMAs, and the commit below still frees the stage
+                const bool issue = NVFP4_CHECK(
+                    (h0 + t.mtu - 1) * C::kPairN + t.ncols <= C::kAccCols &&
+                        C::kSfBase + rt.stage * kSfCols + kSfCols <= (int)kTmemCols &&
+                        smem_in(sa, (uint32_t)t.mtu * kATileBytes, C::kOffARing, C::kOffARing + C::kARing) &&
+                        smem_in(sb, (uint32_t)t.ncols * (kTileK / 2), C::kOffBRing, C::kOffBRing + C::kBRing),
+                    kSiteCheckMma);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4 && issue; ++kk) {
                     const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
@@ -926,6 +994,7 @@ struct Roles {
             const int nblk = (min(t.ncols, N - t.n0) + 31) / 32;
             const int mine = (nblk - h + 1) / 2;
             const bool wide_st = ((reinterpret_cast<uintptr_t>(cbase) & 31u) == 0) && (N % 16 == 0) && (ldc % 16 == 0);
+            bool failed = false;
 #pragma unroll
             for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
                 const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
@@ -933,6 +1002,15 @@ struct Roles {
                 const int row = row0 + lane;
                 const bool live = row < t.M;
                 uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
+                // (debug build) the accumulator columns this warp reads, and the
+                // 32-byte alignment of its rows' wide stores
+                if (!NVFP4_CHECK_WARP((h0 + mt) * C::kPairN + 32 * (h + 2 * (mine - 1) + 1) <= C::kAccCols &&
+                                          (!wide_st || !live ||
+                                           (reinterpret_cast<uintptr_t>(crow + t.n0 + 32 * h) & 31u) == 0),
+                                      kSiteCheckEpi)) {
+                    failed = true;
+                    break;
+                }
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
@@ -951,6 +1029,7 @@ struct Roles {
                     }
                 }
             }
+            if (failed) break;
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {

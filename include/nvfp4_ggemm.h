@@ -129,7 +129,15 @@ typedef struct {
                                  GEMM then starts streaming B and SFB before that kernel has
                                  completed, during its last CTAs; A, SFA and the C stores still
                                  wait for it. With serial_launch the flag has no effect */
-    int32_t reserved[1];
+    int32_t debug_check_fail; /* test only, and only in the debug build of the library (compiled
+                                 with -DNVFP4_DEBUG, whose kernel checks every shared-memory and
+                                 TMEM range, TMA coordinate and alignment before the operation it
+                                 guards): 0 = off; a check site (0x21..0x26) = that check reports
+                                 a failure as if its condition were false, so the error path
+                                 (NVFP4_ERR_DEVICE_FAULT with the site in bits 8-15 of the
+                                 detail word, the operation skipped, the kernel ending through
+                                 its abort flag) runs without any invalid operation. The
+                                 release build ignores it */
 } nvfp4_ggemm_options_t;
 
 typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;

@@ -36,6 +36,17 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == set(nb.EXPORTED)
 
 
+def test_device_check_build_loads_and_exports_the_same_symbols(L):
+    """The -DNVFP4_DEBUG build (built by the same script) is a drop-in
+    replacement: same exports, same option checks."""
+    path = nbuild.build(debug=True)
+    D = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(D, n), f"{n} not exported by the device-check build"
+    D.nvfp4_ggemm_version.restype = ctypes.c_int
+    assert D.nvfp4_ggemm_version() == nb.nvfp4_ggemm_version()
+
+
 def test_version_and_strings(L):
     assert nb.nvfp4_ggemm_version() >= 10000
     for st in range(0, 9):
@@ -71,7 +82,8 @@ def test_plan_rejects_bad_shapes(L, M, N, K, want):
 def test_plan_rejects_bad_options(L):
     for field, val in [("sf_layout", 2), ("sf_path", 5), ("cache_b_scales", 3), ("tile_n", 80),
                        ("tile_n", 288), ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8),
-                       ("b_stages", 3), ("a_stages", 9)]:
+                       ("b_stages", 3), ("a_stages", 9), ("debug_check_fail", 0x20), ("debug_check_fail", 0x27),
+                       ("debug_check_fail", -1)]:
         opt = nb.nvfp4_ggemm_default_options()
         setattr(opt, field, val)
         st, h = nb.nvfp4_ggemm_plan(0, [64], 256, 256, opt)
