@@ -225,6 +225,10 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
       static (the b_static option: no kernel before a call writes them, as
       for model weights), so each call streams B while the previous one
       finishes. Reported beside the headline, not as it.
+    * "stream_inputs_static": as "stream", with plans that declare all four
+      inputs static (b_static = 2: every load may start while the previous
+      call finishes; only the C stores wait for it). Reported beside the
+      headline, not as it.
     Problems too small for 64 copies to cover 3x the L2 (c0) run "flush"
     and "warm" only, and report "flush" as the headline.
     Host cost: the enqueue time of one call (the C call from Python, plan
@@ -249,22 +253,24 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
             SFB = [_atom(torch, nb, s, N, K) for s in SFB]
         C = [torch.empty((m, N), dtype=torch.float16, device="cuda") for m in prob.M]
         gg = nb.GroupedGemm(prob.M, N, K, **kw)
-        gs = nb.GroupedGemm(prob.M, N, K, **dict(kw, b_static=True))
+        gs = nb.GroupedGemm(prob.M, N, K, **dict(kw, b_static=1))
+        gi = nb.GroupedGemm(prob.M, N, K, **dict(kw, b_static=2))
         if kw.get("cache_b_scales"):
-            gg.prepare_b_scales(SFB)
-            gs.prepare_b_scales(SFB)
+            for plan in (gg, gs, gi):
+                plan.prepare_b_scales(SFB)
             SFB_run = [None] * len(SFB)
         else:
             SFB_run = SFB
-        return gg, gg.bind(A, B, SFA, SFB_run, C), gs, gs.bind(A, B, SFA, SFB_run, C)
+        return (gg, gg.bind(A, B, SFA, SFB_run, C), gs, gs.bind(A, B, SFA, SFB_run, C),
+                gi, gi.bind(A, B, SFA, SFB_run, C))
 
     sets = [make_set() for _ in range(n_sets)]
     info = sets[0][0].info()
     stream = torch.cuda.current_stream()
 
     def check():
-        for gg, _, gs, _ in sets:
-            for plan in (gg, gs):
+        for gg, _, gs, _, gi, _ in sets:
+            for plan in (gg, gs, gi):
                 st, detail = plan.sync_status()
                 if st != nb.NVFP4_OK:
                     raise RuntimeError(f"{name}: device status {nb.nvfp4_status_string(st)} ({detail:#x})")
@@ -273,20 +279,22 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
     # the enqueue time of a call is taken here too
     enq = []
     for i in range(max(warmup, len(sets))):
-        _, call, _, call_s = sets[i % len(sets)]
+        _, call, _, call_s, _, call_i = sets[i % len(sets)]
         torch.cuda._sleep(SLEEP_CYCLES)
         t0 = time.perf_counter()
         call()
         enq.append(time.perf_counter() - t0)
         call_s()
+        call_i()
     torch.cuda.synchronize()
     check()
     enqueue_s = statistics.median(enq[len(sets):] or enq)
 
     def stream_block(order, which=1):
         """Calls sets[order[i]] back to back between one event pair (which: 1
-        the default plans, 3 the plans that declare B static). Returns (µs
-        per call, whether the device waited for the host)."""
+        the default plans, 3 the plans that declare B static, 5 those that
+        declare every input static). Returns (µs per call, whether the
+        device waited for the host)."""
         sleep_ns = 50e3 + 3.0 * enqueue_s * 1e9 * len(order)
         for _attempt in range(4):
             start = torch.cuda.Event(enable_timing=True)
@@ -330,6 +338,8 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
         by["stream"] = {"us_mean": us, "host_bound": bool(late)}
         us, late = stream_block([i % len(sets) for i in range(steps)], which=3)
         by["stream_b_static"] = {"us_mean": us, "host_bound": bool(late)}
+        us, late = stream_block([i % len(sets) for i in range(steps)], which=5)
+        by["stream_inputs_static"] = {"us_mean": us, "host_bound": bool(late)}
         v = per_call("isolated")
         by["isolated"] = {"us_mean": statistics.fmean(v), "us_median": statistics.median(v), "us_min": min(v),
                           "us_p90": sorted(v)[int(0.9 * (len(v) - 1))]}
@@ -355,9 +365,10 @@ def time_config(name: str, sf_path: str, steps: int, warmup: int, seed: int = 0,
     out["host"] = {"enqueue_us": enqueue_s * 1e6, "call_and_sync_us": statistics.median(walls) * 1e6}
     if want_e2e:
         out["e2e"] = time_e2e(prob, kw, steps, warmup, torch, nb)
-    for gg, _, gs, _ in sets:
+    for gg, _, gs, _, gi, _ in sets:
         gg.close()
         gs.close()
+        gi.close()
     return out
 
 
@@ -552,6 +563,11 @@ def main():
         "b_static_note": ("the same back-to-back calls with the b_static option (the caller declares B and "
                           "SFB unwritten by the previous kernel, as for inference weights): each call streams "
                           "B while the previous call's last CTAs finish; A, SFA and C still wait"),
+        "us_inputs_static": (round(r["by"]["stream_inputs_static"]["us_mean"], 2)
+                             if "stream_inputs_static" in r["by"] else None),
+        "inputs_static_note": ("the same back-to-back calls with b_static = 2 (the caller declares all four "
+                               "inputs unwritten by the previous kernel): every load may start while the previous "
+                               "call finishes, only the C stores wait"),
         "us_by_protocol": {m: {k: (round(v, 2) if isinstance(v, float) else v) for k, v in d.items()}
                            for m, d in r["by"].items()},
         "host_us_per_call": {k: round(v, 2) for k, v in r["host"].items()},

@@ -343,7 +343,7 @@ def nvfp4_ggemm_schedule(M: Sequence[int], N, tile_n: int = 0, max_ctas: int = 1
 def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales: bool = False,
                  wait_timeout_ns: int = 0, tile_n: int = 0, max_ctas: int = 0,
                  debug_skip_load: int = 0, b_stages: int = 0, a_stages: int = 0,
-                 serial_launch: bool = False, b_static: bool = False,
+                 serial_launch: bool = False, b_static: int = 0,
                  debug_check_fail: int = 0) -> nvfp4_ggemm_options_t:
     opt = nvfp4_ggemm_default_options()
     opt.sf_layout = {"raw": NVFP4_SF_RAW, "atom": NVFP4_SF_ATOM}[sf_layout]
@@ -357,7 +357,7 @@ def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales:
     opt.b_stages = int(b_stages)
     opt.a_stages = int(a_stages)
     opt.serial_launch = 1 if serial_launch else 0
-    opt.b_static = 1 if b_static else 0
+    opt.b_static = int(b_static)  # False/True = 0/1; 2 = every input static
     opt.debug_check_fail = int(debug_check_fail)
     return opt
 

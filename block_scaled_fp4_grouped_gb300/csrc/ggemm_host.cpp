@@ -386,7 +386,7 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
         return NVFP4_ERR_INVALID_ARG;
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
-    if (out->b_static != 0 && out->b_static != 1) return NVFP4_ERR_INVALID_ARG;
+    if (out->b_static < 0 || out->b_static > 2) return NVFP4_ERR_INVALID_ARG;
     if (out->debug_check_fail != 0 && (out->debug_check_fail < kSiteCheckLoadB || out->debug_check_fail > kSiteCheckEpi))
         return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
@@ -548,9 +548,14 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
 
     GemmParams &gp = *s.params;
     // Loads that may start before the previous kernel completes (the caller's
-    // b_static): B, and SFB unless the re-layout kernel that runs just before
-    // the GEMM writes it. Never behind run_host's own copy of the inputs.
-    gp.b_static = (early_ok && p->opt.b_static) ? (p->relayout() ? 1 : 2) : 0;
+    // b_static: 1 for B and SFB, 2 for every input): never the scales on the
+    // re-layout path (the re-layout kernel just before the GEMM writes them),
+    // and nothing behind run_host's own copy of the inputs.
+    gp.early = 0;
+    if (early_ok && p->opt.b_static) {
+        gp.early = kEarlyB | (p->relayout() ? 0 : kEarlySfb);
+        if (p->opt.b_static == 2) gp.early |= kEarlyA | (p->relayout() ? 0 : kEarlySfa);
+    }
 #ifdef NVFP4_TRACE
     gp.trace = g_trace ? g_trace + (size_t)(g_trace_next++ % g_trace_calls) * kMaxCtas * kTraceSlots : nullptr;
 #endif

@@ -20,6 +20,11 @@ constexpr int kRowTilesPerUnit = 2;  // 128-row tiles of A that share every B st
 constexpr int kNumRowBoxes = 4;    // B / SFB box heights 32, 64, 128, 256 rows (32 << i)
 constexpr int kSfKTiles = 2;       // k tiles (of 256) per raw-scale TMA box: 32 bytes of each scale row
 
+// Operands a GEMM launch may load before the previous kernel of its stream
+// has completed (GemmParams::early), because the caller declared that
+// kernel does not write them; all others, and the C stores, wait for it.
+constexpr int32_t kEarlyB = 1, kEarlySfb = 2, kEarlyA = 4, kEarlySfa = 8;
+
 // Wait sites recorded in the error word (bits 8-15).
 enum WaitSite : uint32_t {
     kSiteBEmpty = 1,     // B producer waiting for a free stage
@@ -198,7 +203,7 @@ struct GemmParams {
     int32_t cap_single;            // chunks per tile, one row tile (1..MAXN/32)
     int32_t cap_pair;              // chunks per tile, two row tiles
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
-    int32_t b_static;              // B (1), or B and SFB (2), are loaded before the previous kernel completes
+    int32_t early;                 // kEarly* bits: operands loaded before the previous kernel completes
     int32_t debug_check_fail;      // debug build, test only: the check site forced to fail (0 = none)
 #ifdef NVFP4_TRACE
     unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null

@@ -615,7 +615,7 @@ struct Roles {
                     const uint32_t fb = b_full(r.stage);
                     mbar_arrive_expect_tx(fb, bytes);
                     // B may be written by the previous kernel, unless the caller says otherwise
-                    if (loads == 1 && !p.b_static) griddep_wait();
+                    if (loads == 1 && !(p.early & kEarlyB)) griddep_wait();
                     tma_rows(b_stage(r.stage), gm->tmB, kt * (kTileK / 2), t.n0, chunks, kTileK / 2, fb, pol);
                     issued_mask |= 1u << r.stage;
                     issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
@@ -666,7 +666,8 @@ struct Roles {
                 const uint32_t fb = a_full(r.stage);
                 mbar_arrive_expect_tx(fb, (uint32_t)t.mtu * kATileBytes);
                 if (first) {
-                    griddep_wait();  // A may be written by the previous kernel
+                    // A may be written by the previous kernel, unless the caller says otherwise
+                    if (!(p.early & kEarlyA)) griddep_wait();
                     NVFP4_TRACE_AT(kTrDepWait);
                 }
                 tma_load_2d(a_stage(r.stage), map, kt * (kTileK / 2), t.mt0 * kTileM, fb, pol);
@@ -729,20 +730,23 @@ struct Roles {
                     break;
                 }
                 mbar_arrive_expect_tx(fb, bytes);
-                // the scales may be written by the previous kernel; B's scales are
-                // loaded before waiting for it when the caller says they are not
-                const bool sfb_early = first && p.b_static == 2;
+                // the scales may be written by the previous kernel: on the first
+                // stage, part 0 loads those the caller declared it does not write,
+                // then part 1 waits for it and loads the rest
+                const bool sfa_early = !first || (p.early & kEarlySfa);
+                const bool sfb_early = !first || (p.early & kEarlySfb);
                 for (int part = 0; part < 2; ++part) {
+                    const bool sfa_now = part == 0 ? sfa_early : !sfa_early;
                     const bool sfb_now = part == 0 ? sfb_early : !sfb_early;
-                    if (part == 1 && first) griddep_wait();
+                    if (part == 1 && !(sfa_early && sfb_early)) griddep_wait();
                     if (RAW) {
                         // scale bytes [16 * kt0, 16 * (kt0 + kKS)) of each row: k tiles kt0 .. kt0 + kKS - 1;
                         // the unit's row tiles in one box, the tile's columns in the fewest boxes
                         const int x = ks * C::kSfRow;
-                        if (part == 1) tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
+                        if (sfa_now) tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
                         if (sfb_now) tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
                     } else {
-                        if (part == 1) {
+                        if (sfa_now) {
 #pragma unroll
                             for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
                                 if (mt < t.mtu)

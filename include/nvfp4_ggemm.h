@@ -123,12 +123,18 @@ typedef struct {
                                  CTAs finish (programmatic dependent launch); its loads and
                                  stores still wait until that kernel has completed. 1: plain
                                  launches, every kernel starts after the previous one ends */
-    int32_t b_static;         /* 0 (default), or 1: the caller guarantees that no kernel that may
-                                 still run when this GEMM starts (the kernel before it on its
-                                 stream) writes B or SFB, e.g. model weights in inference. The
-                                 GEMM then starts streaming B and SFB before that kernel has
-                                 completed, during its last CTAs; A, SFA and the C stores still
-                                 wait for it. With serial_launch the flag has no effect */
+    int32_t b_static;         /* 0 (default): every load waits for the kernel before the GEMM on
+                                 its stream to complete. 1: the caller guarantees that this
+                                 kernel (the only one that may still run when the GEMM starts)
+                                 writes neither B nor SFB, e.g. model weights in inference; the
+                                 GEMM then starts streaming B and SFB during that kernel's last
+                                 CTAs, while A, SFA and the C stores still wait for it. 2: the
+                                 same guarantee for all four inputs (A, SFA, B, SFB), e.g. inputs
+                                 produced two or more kernels earlier: every load may start
+                                 early and only the C stores wait. On the re-layout path the
+                                 scales always wait (the re-layout kernel just before the GEMM
+                                 writes them). With serial_launch, and in nvfp4_ggemm_run_host,
+                                 the option has no effect */
     int32_t debug_check_fail; /* test only, and only in the debug build of the library (compiled
                                  with -DNVFP4_DEBUG, whose kernel checks every shared-memory and
                                  TMEM range, TMA coordinate and alignment before the operation it

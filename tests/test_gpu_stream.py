@@ -144,3 +144,48 @@ def test_relayout_reads_scales_the_previous_kernel_wrote(cached):
     finally:
         g1.close()
         g2.close()
+
+
+def test_all_inputs_static_still_orders_the_c_stores():
+    """b_static = 2: the caller declares that the kernel before the GEMM
+    writes none of its inputs, so every load may start during that kernel's
+    last CTAs, but the C stores must still wait for it. Here the kernel
+    before the second GEMM (the first GEMM) reads, as its A operand, the
+    buffer the second GEMM writes as C; a store issued too early would change
+    what the first GEMM read. The second GEMM's inputs are written once, long
+    before, so the declaration holds."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    p2 = synth.make_problem("custom", seed=45, M=[256], N=4096, K=7168)
+    A2, B2, SFA2, SFB2 = to_device(p2.A), to_device(p2.B), to_device(p2.SFA), to_device(p2.SFB)
+    C2 = [torch.zeros((256, 4096), dtype=torch.float16, device="cuda")]
+    # the first GEMM reads the first 256 x 4096 bytes of C2 as its A (K1 = 8192)
+    p1 = synth.make_problem("custom", seed=46, M=[256], N=512, K=8192)
+    A1 = [C2[0].view(torch.uint8).reshape(-1)[: 256 * 4096].view(256, 4096)]
+    B1, SFA1, SFB1 = to_device(p1.B), to_device(p1.SFA), to_device(p1.SFB)
+    C1 = [torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")]
+    g1 = nb.GroupedGemm(p1.M, p1.N, p1.K)
+    g2 = nb.GroupedGemm(p2.M, p2.N, p2.K, b_static=2)
+    O = oracle.get()
+    try:
+        call1 = g1.bind(A1, B1, SFA1, SFB1, C1)
+        call2 = g2.bind(A2, B2, SFA2, SFB2, C2)
+        call2()
+        call1()
+        torch.cuda.synchronize()
+        want2, _, _ = O.group_gemm(p2.A[0], p2.B[0], p2.SFA[0], p2.SFB[0], p2.K)
+        for rnd in range(3):
+            # C2 is zeroed so that its next write changes the bytes the first GEMM reads
+            C2[0].zero_()
+            a1_before = A1[0].cpu().numpy().copy()
+            call1()  # reads C2's bytes (zeros)
+            call2()  # overwrites C2; its loads may start early, its stores may not
+            for gg in (g1, g2):
+                st, word = gg.sync_status()
+                assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
+            want1, _, _ = O.group_gemm(a1_before, p1.B[0], p1.SFA[0], p1.SFB[0], p1.K)
+            assert_close(C1[0].cpu().numpy(), want1, f"round {rnd}: the first GEMM read C2 before it was written")
+            assert_close(C2[0].cpu().numpy(), want2, f"round {rnd}: the second GEMM with every input static")
+    finally:
+        g1.close()
+        g2.close()
