@@ -248,6 +248,37 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
     }
 }
 
+void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t *chunk_prefix, const GroupShape *shapes,
+                int cap_single, int cap_pair)
+{
+    double cost[kMaxCtas];
+    int wg = 0;  // ranges ascend, so the group walk only moves forward
+    for (int c = 0; c < grid; ++c) {
+        cost[c] = 0.0;
+        int pos = ranges[c].begin;
+        while (pos < ranges[c].end) {
+            while (pos >= chunk_prefix[wg] + ((shapes[wg].m_tiles + 1) / 2) * shapes[wg].n_chunks) ++wg;
+            const int n = shapes[wg].n_chunks;
+            const int local = pos - chunk_prefix[wg];
+            const int mp = local / n;
+            const int ch0 = local - mp * n;
+            const int mtu = std::min(kRowTilesPerUnit, shapes[wg].m_tiles - mp * kRowTilesPerUnit);
+            const int plen = std::min(n - ch0, ranges[c].end - pos);
+            const int pt = ceil_div(plen, mtu == 2 ? cap_pair : cap_single);
+            const double b_bytes = (double)plen * kChunkN * shapes[wg].k_tiles * (kTileK / 2) * 9.0 / 8.0;
+            const int rows = std::max(0, std::min(shapes[wg].M - mp * kRowTilesPerUnit * kTileM, mtu * kTileM));
+            const double c_bytes = (double)rows * plen * kChunkN * 2.0;
+            const double wait = (mtu == 2 && pt >= 2) ? 4.0 * c_bytes * (pt - 1) / pt : 0.0;
+            cost[c] += b_bytes + c_bytes + wait;
+            pos += plen;
+        }
+    }
+    int idx[kMaxCtas];
+    for (int c = 0; c < grid; ++c) idx[c] = c;
+    std::stable_sort(idx, idx + grid, [&](int a, int b) { return cost[a] > cost[b]; });
+    for (int c = 0; c < grid; ++c) order[c] = (uint8_t)idx[c];
+}
+
 void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes)
 {
     for (int c = 0; c < grid; ++c) {
@@ -524,6 +555,8 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
         gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
         pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks, p->shapes.data());
+        order_ctas(gp.order, p->ctas.data(), p->grid, p->chunk_prefix.data(), p->shapes.data(), p->cap_single,
+                   p->cap_pair);
         const GroupDesc *hg = reinterpret_cast<const GroupDesc *>(s.h_table);
         for (int g = 0; g < std::min(p->G, kParamGroups); ++g) gp.pmaps[g] = hg[g].maps;
         gp.err = p->d_err;

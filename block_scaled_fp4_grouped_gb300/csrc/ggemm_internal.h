@@ -197,6 +197,7 @@ struct GemmParams {
     const GroupDesc *groups;       // [G]
     const int32_t *chunk_prefix;   // [G+1]
     CtaStart cta[kMaxCtas + 1];    // [grid + 1]
+    uint8_t order[kMaxCtas];       // block b walks range order[b] (a permutation of 0 .. grid - 1)
     uint32_t *err;                 // device error word
     uint64_t timeout_ns;
     int32_t G;
@@ -216,6 +217,19 @@ struct GemmParams {
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
                      const GroupShape *shapes, int G, int cap_single, int cap_pair);
 void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes);
+
+// Which block walks which range: the ranges sorted by an estimate of their
+// work, heaviest first. Blocks are placed on SMs in index order as the
+// previous kernel's CTAs leave them, so the lowest indices start first and
+// the heaviest ranges get the most time. The estimate counts the bytes a
+// range moves through HBM (its B strip with SFB, its C) and, for each tile of
+// two row tiles that another tile of the CTA follows, four times that tile's
+// C: such a tile fills both accumulator halves, so the next tile's MMAs wait
+// for its whole epilogue (timed on the GPU: the heaviest-first order matches
+// or beats every input group order tried, by up to 1.2 us on the skinny
+// 8-group shape).
+void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t *chunk_prefix, const GroupShape *shapes,
+                int cap_single, int cap_pair);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {

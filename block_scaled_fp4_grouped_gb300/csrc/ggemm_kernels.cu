@@ -189,9 +189,10 @@ struct Walker {
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
-        const CtaStart &r = p.cta[blockIdx.x];
+        const int c = p.order[blockIdx.x];  // the range this block walks
+        const CtaStart &r = p.cta[c];
         pos = r.begin;
-        end = p.cta[blockIdx.x + 1].begin;
+        end = p.cta[c + 1].begin;
         g = cta_group(r.packed);
         g_base = r.g_base;
         g_rows = cta_rows_m(r.rows);
@@ -500,7 +501,7 @@ struct Roles {
     // Size the ring slots from this CTA's widest tile and most row tiles.
     __device__ void size_rings()
     {
-        const uint32_t packed = p.cta[blockIdx.x].packed;
+        const uint32_t packed = p.cta[p.order[blockIdx.x]].packed;
         max_chunks = min(max(cta_max_chunks(packed), 1), MAXN / kChunkN);
         max_rows = min(max(cta_max_rows(packed), 1), kRowTilesPerUnit);
         b_slot = (uint32_t)max_chunks * kBRowBoxBytes;

@@ -168,6 +168,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
     pack_cta_starts(gp.cta, ranges, grid, (int)total, shapes);
+    order_ctas(gp.order, ranges, grid, prefix, shapes, cap_single, cap_pair);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
