@@ -39,7 +39,9 @@
 // a pair share every B stage, so each B strip is read from HBM once, by one
 // SM. The host keeps every range inside one pair when it can and picks the
 // smallest per-CTA budget of k-stages that fits the grid, so a CTA streams
-// its B strip in as few passes over K as possible.
+// its B strip in as few passes over K as possible. Block b walks range
+// order[b]: the host hands the ranges out heaviest first, as blocks with low
+// indices reach their SMs first.
 //
 // Every mbarrier wait is bounded by the plan's timeout: on expiry the waiter
 // records (status, site, block) in the error word, raises a CTA-wide abort
