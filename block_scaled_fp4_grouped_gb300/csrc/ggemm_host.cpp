@@ -100,6 +100,22 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
     return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over an atom-layout scale matrix: [blocks][katoms] atoms of
+// 512 bytes (a 128-row block's atoms of successive 64-k slices contiguous),
+// read as 8-byte elements; a box is the four atoms of one k tile of
+// `box_blocks` consecutive 128-row blocks (2 KB each, one after another).
+bool encode_atoms(CUtensorMap *map, const void *base, uint64_t katoms, uint64_t blocks, uint32_t box_blocks)
+{
+    cuuint64_t dims[3] = {kSfAtomBytes / 8, katoms, blocks};
+    cuuint64_t strides[2] = {kSfAtomBytes, katoms * kSfAtomBytes};
+    cuuint32_t box[3] = {kSfAtomBytes / 8, kTileK / 64, box_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Smallest kernel tile width (128 or 256) that holds `tile_n` columns.
 int variant_width(int tile_n) { return tile_n <= 128 ? 128 : 256; }
 
@@ -324,8 +340,13 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
             ok = encode_2d(&d.maps.tmSFB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N, K / 16, sf_box, kChunkN << i,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
     } else {
-        d.sfa_atoms = static_cast<const uint8_t *>(SFA);
-        d.sfb_atoms = static_cast<const uint8_t *>(SFB);
+        // atom layout: SFA boxes of the unit's 1 or 2 row tiles, SFB boxes of
+        // 1, 2 or 3 (and, unused by the kernel variants, 4) 128-row blocks
+        const uint64_t katoms = (uint64_t)K / 64;
+        for (int i = 0; i < 2 && ok; ++i)
+            ok = encode_atoms(&d.maps.tmSFA[i], SFA, katoms, (uint64_t)ceil_div(M, kTileM), (uint32_t)(i + 1));
+        for (int i = 0; i < kNumRowBoxes && ok; ++i)
+            ok = encode_atoms(&d.maps.tmSFB[i], SFB, katoms, (uint64_t)ceil_div(N, kTileM), (uint32_t)(i + 1));
     }
     return ok;
 }

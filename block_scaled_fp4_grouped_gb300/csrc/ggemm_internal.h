@@ -90,16 +90,17 @@ enum TraceSlot : int {
 struct alignas(128) GroupMaps {
     CUtensorMap tmA[2];    // A_g bytes [M_g][K_g/2];  boxes 128 B x 128 / 256 rows; 128-byte swizzle
     CUtensorMap tmB[kNumRowBoxes];    // B_g bytes [N_g][K_g/2]; boxes 128 B x (32 << i) rows; 128-byte swizzle
-    CUtensorMap tmSFA[2];  // raw SFA_g [M_g][K_g/16]; boxes 32 B x 128 / 256 rows (raw-scale path)
-    CUtensorMap tmSFB[kNumRowBoxes];  // raw SFB_g [N_g][K_g/16]; boxes 32 B x (32 << i) rows (raw-scale path)
+    // raw scales: SFA_g [M_g][K_g/16], boxes 32 B x 128 / 256 rows; SFB_g
+    // [N_g][K_g/16], boxes 32 B x (32 << i) rows. Atom layout: the atoms of one
+    // k tile (4 x 512 B) of i + 1 consecutive 128-row blocks.
+    CUtensorMap tmSFA[2];
+    CUtensorMap tmSFB[kNumRowBoxes];
 };
 constexpr int kNumMaps = 2 + kNumRowBoxes + 2 + kNumRowBoxes;
 static_assert(sizeof(GroupMaps) == kNumMaps * sizeof(CUtensorMap), "the maps are consecutive");
 
 struct alignas(128) GroupDesc {
     GroupMaps maps;
-    const uint8_t *sfa_atoms;  // atom-layout SFA_g (atom path)
-    const uint8_t *sfb_atoms;  // atom-layout SFB_g (atom path)
     uint16_t *C;               // C_g fp16 [M_g][ldc], columns [0, N_g) written
     int32_t M;
     int32_t m_tiles;      // ceil(M / 128)

@@ -698,22 +698,19 @@ struct Roles {
         bool ok = true;
 
         for (bool more = have; ok && more; more = wk.next(p, t)) {
-            const GroupDesc *gd = p.groups + t.g;
             const GroupMaps *gm = maps_of(p, t.g);
             const int chunks = t.ncols / kChunkN;
-            if (RAW) {
-                maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
-                maps.use_rows(gm, t.g, gm->tmSFB, chunks);
-            }
             int b0 = 0, nblk = 0;
             sfb_blocks(t.n0, t.ncols, t.N, b0, nblk);
-            const size_t katoms = (size_t)(t.k_tiles - 1) * 4 + t.k_last;  // 64-k atoms per 128-row block
-            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;          // scale stages of this tile
+            maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
+            if (RAW) maps.use_rows(gm, t.g, gm->tmSFB, chunks);
+            else if (nblk >= 1 && nblk <= 3) maps.use(gm, t.g, &gm->tmSFB[nblk - 1]);
+            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;  // scale stages of this tile
             for (int ks = 0; ks < s_tiles; ++ks) {
-                // atom layout: the atoms of k tile ks (fewer in a partial last one)
-                const uint32_t piece = ks + 1 == s_tiles ? (uint32_t)t.k_last * kSfAtomBytes : kSfTileBytes;
+                // atom layout: whole boxes of four atoms per 128-row block, the
+                // atoms past K_g of a partial last k tile filled with zeros
                 const uint32_t bytes = RAW ? (uint32_t)(t.mtu * kTileM + t.ncols) * C::kSfRow
-                                           : (uint32_t)(t.mtu + nblk) * piece;
+                                           : (uint32_t)(t.mtu + nblk) * kSfTileBytes;
                 if (!wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
                     ok = false;
                     break;
@@ -724,10 +721,7 @@ struct Roles {
                                      (RAW ? (uint32_t)t.mtu * kTileM * C::kSfRow <= (uint32_t)C::kSfaBytes &&
                                                 (uint32_t)t.ncols * C::kSfRow <= (uint32_t)C::kSfbRegion &&
                                                 ((ks * C::kSfRow) & 15) == 0
-                                          : nblk >= 1 && nblk * kSfTileBytes <= C::kSfbRegion &&
-                                                (piece & 15u) == 0 &&
-                                                ((reinterpret_cast<uintptr_t>(gd->sfa_atoms) |
-                                                  reinterpret_cast<uintptr_t>(gd->sfb_atoms)) & 15u) == 0),
+                                          : nblk >= 1 && nblk <= 3 && nblk * kSfTileBytes <= C::kSfbRegion),
                                  kSiteCheckLoadSf)) {
                     ok = false;
                     break;
@@ -749,20 +743,11 @@ struct Roles {
                         if (sfa_now) tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
                         if (sfb_now) tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
                     } else {
-                        if (sfa_now) {
-#pragma unroll
-                            for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                                if (mt < t.mtu)
-                                    bulk_load(st + mt * kSfTileBytes,
-                                              gd->sfa_atoms +
-                                                  ((size_t)(t.mt0 + mt) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                              piece, fb, pol);
-                        }
-                        if (sfb_now)
-                            for (int b = 0; b < nblk; ++b)
-                                bulk_load(st + C::kSfaBytes + b * kSfTileBytes,
-                                          gd->sfb_atoms + ((size_t)(b0 + b) * katoms + (size_t)ks * 4) * kSfAtomBytes,
-                                          piece, fb, pol);
+                        // the four atoms of k tile ks for the unit's row tiles
+                        // and for the 128-row blocks under the tile's columns,
+                        // one box each: 2 KB per 128-row block, block after block
+                        if (sfa_now) tma_load_3d(st, &gm->tmSFA[t.mtu - 1], 0, ks * 4, t.mt0, fb, pol);
+                        if (sfb_now) tma_load_3d(st + C::kSfaBytes, &gm->tmSFB[nblk - 1], 0, ks * 4, b0, fb, pol);
                     }
                 }
                 if (first) {
