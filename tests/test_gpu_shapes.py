@@ -214,6 +214,27 @@ def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
         assert_close(got[g], ref, f"group {g} (M={p.M[0]}, N={p.N}, K={p.K})")
 
 
+@pytest.mark.parametrize("layout,path,cached", [("raw", "relayout", False), ("raw", "relayout", True),
+                                                ("atom", "fused", False)])
+def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached):
+    """The K % 64 workload that is timed: the 8-group N = 4096 M list at
+    K = 7104 (27 whole 256-k tiles and a last tile of three 64-k slices),
+    through each path a caller can take (raw scales re-laid out every call,
+    with the B scales cached by the plan, and atom-layout scales read by
+    3-D tensor-map boxes whose atoms past K are zero-filled); sampled
+    entries and the output's tile edges against the oracle."""
+    from gpu_util import run_gpu, sample_indices
+    M = synth.make_problem("c4", seed=0).M
+    prob = synth.make_problem("custom", seed=1200, M=M, N=4096, K=7104)
+    got = run_gpu(prob, sf_layout=layout, sf_path=path, cache_b_scales=cached)
+    rng = np.random.default_rng(1200)
+    for g in range(prob.G):
+        rows, cols = sample_indices(prob.M[g], prob.N, 400, rng)
+        ref16, _ = O.group_entries(prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], prob.K, rows, cols)
+        assert_close(got[g][rows, cols], ref16, f"K=7104 {layout}/{path} group {g}")
+        assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
+
+
 def test_k_multiple_of_64_uniform_and_exact(O):
     """One K for every group (nvfp4_ggemm_plan), K = 704 = 2 x 256 + 192,
     with power-of-two scales of span 4 so that every fp32 partial sum is
