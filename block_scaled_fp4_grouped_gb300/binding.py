@@ -51,6 +51,7 @@ EXPORTED = (
     "nvfp4_ggemm_version",
     "nvfp4_ggemm_run_noalloc",
     "nvfp4_ggemm_schedule",
+    "nvfp4_ggemm_schedule_units",
     "nvfp4_ggemm_plan_shapes",
     "nvfp4_ggemm_run_strided",
     "nvfp4_ggemm_plan_batched",
@@ -73,6 +74,7 @@ class nvfp4_ggemm_options_t(ctypes.Structure):
         ("serial_launch", ctypes.c_int32),
         ("b_static", ctypes.c_int32),
         ("debug_check_fail", ctypes.c_int32),
+        ("row_units", ctypes.c_int32),
     ]
 
 
@@ -87,6 +89,8 @@ class nvfp4_ggemm_plan_info_t(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("kernels_per_run", ctypes.c_int32),
         ("sf_path", ctypes.c_int32),
+        ("row_units", ctypes.c_int32),
+        ("split_acc", ctypes.c_int32),
     ]
 
 
@@ -149,6 +153,12 @@ def lib() -> ctypes.CDLL:
     L.nvfp4_ggemm_schedule.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    L.nvfp4_ggemm_schedule_units.restype = ctypes.c_int
+    L.nvfp4_ggemm_schedule_units.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     L.nvfp4_ggemm_run_strided.restype = ctypes.c_int
     L.nvfp4_ggemm_run_strided.argtypes = [_VP, _VPP, _VPP, _VPP, _VPP, _VPP, ctypes.POINTER(ctypes.c_int32), _VP]
     L.nvfp4_ggemm_plan_shapes.restype = ctypes.c_int
@@ -338,13 +348,30 @@ def nvfp4_ggemm_schedule(M: Sequence[int], N, tile_n: int = 0, max_ctas: int = 1
     return st, [int(out[i]) for i in range(grid.value + 1)] if grid.value > 0 else [0]
 
 
+def nvfp4_ggemm_schedule_units(M: Sequence[int], N, tile_n: int = 0, max_ctas: int = 148, K=256,
+                               row_units: int = 0) -> Tuple[int, List[int], int, int]:
+    """Per-CTA chunk ranges for units of row_units 128-row tiles (0: the
+    plan's own choice). Returns (status, cta_begin[0..grid], units, split_acc)."""
+    Ns = list(N) if isinstance(N, (list, tuple)) else [int(N)] * len(M)
+    Ks = list(K) if isinstance(K, (list, tuple)) else [int(K)] * len(M)
+    out = (ctypes.c_int32 * (max(1, int(max_ctas)) + 1))()
+    grid, units, split = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    st = lib().nvfp4_ggemm_schedule_units(len(M), _i32_array(M), _i32_array(Ns), _i32_array(Ks), int(tile_n),
+                                          int(max_ctas), int(row_units), out, ctypes.byref(grid),
+                                          ctypes.byref(units), ctypes.byref(split))
+    if st != NVFP4_OK:
+        return st, [], 0, 0
+    cb = [int(out[i]) for i in range(grid.value + 1)] if grid.value > 0 else [0]
+    return st, cb, int(units.value), int(split.value)
+
+
 # -------------------------------------------------------------- convenience
 
 def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales: bool = False,
                  wait_timeout_ns: int = 0, tile_n: int = 0, max_ctas: int = 0,
                  debug_skip_load: int = 0, b_stages: int = 0, a_stages: int = 0,
                  serial_launch: bool = False, b_static: int = 0,
-                 debug_check_fail: int = 0) -> nvfp4_ggemm_options_t:
+                 debug_check_fail: int = 0, row_units: int = 0) -> nvfp4_ggemm_options_t:
     opt = nvfp4_ggemm_default_options()
     opt.sf_layout = {"raw": NVFP4_SF_RAW, "atom": NVFP4_SF_ATOM}[sf_layout]
     opt.sf_path = {"fused": NVFP4_SF_FUSED, "relayout": NVFP4_SF_RELAYOUT}[sf_path]
@@ -359,6 +386,7 @@ def make_options(sf_layout: str = "raw", sf_path: str = "fused", cache_b_scales:
     opt.serial_launch = 1 if serial_launch else 0
     opt.b_static = int(b_static)  # False/True = 0/1; 2 = every input static
     opt.debug_check_fail = int(debug_check_fail)
+    opt.row_units = int(row_units)
     return opt
 
 

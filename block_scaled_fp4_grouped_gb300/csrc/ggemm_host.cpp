@@ -139,16 +139,16 @@ TensorMapEncodeFn tensor_map_encoder()
 
 int pair_cap_chunks(int max_n) { return (max_n >= 192 ? 192 : max_n) / kChunkN; }
 
-int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int32_t *cta_begin,
-                  int32_t *counts)
+int schedule_ctas(const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair, int max_ctas,
+                  int32_t *cta_begin, int32_t *counts)
 {
     max_ctas = std::max(1, std::min(max_ctas, kMaxCtas));
-    // segments: pairs of row tiles; the last pair of a group with an odd tile count has one
+    // segments: units of `unit` row tiles; the last unit of a group may have fewer
     long nseg = 0, total = 0;
     for (int g = 0; g < G; ++g) {
-        const long pairs = (shapes[g].m_tiles + 1) / 2;
-        nseg += pairs;
-        total += pairs * shapes[g].n_chunks;
+        const long units = ceil_div(shapes[g].m_tiles, unit);
+        nseg += units;
+        total += units * shapes[g].n_chunks;
     }
     if (total == 0) {
         cta_begin[0] = 0;
@@ -160,7 +160,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
         for (int c = 0; c <= grid; ++c) cta_begin[c] = (int32_t)((long)c * total / grid);
         return grid;
     }
-    auto seg_cap = [&](int g, int t) { return (shapes[g].m_tiles - t) >= 2 ? cap_pair : cap_single; };
+    auto seg_cap = [&](int g, int t) { return unit == 2 && (shapes[g].m_tiles - t) >= 2 ? cap_pair : cap_single; };
     // CTAs a segment needs when a CTA may spend `budget` k-stages on it (at
     // least one pass). A CTA that walks two or more tiles of two row tiles
     // takes them one chunk narrower: such tiles fill both accumulator halves,
@@ -168,7 +168,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
     // tiles shorten that wait and spread the pair over more CTAs.
     auto ctas_for = [&](int g, int t, long budget) {
         const long passes = std::max<long>(1, budget / shapes[g].k_tiles);
-        const bool pair = (shapes[g].m_tiles - t) >= 2;
+        const bool pair = unit == 2 && (shapes[g].m_tiles - t) >= 2;
         const long cap = seg_cap(g, t);
         const long per_cta = passes * (pair && passes > 1 && cap > 2 ? cap - 1 : cap);
         return (shapes[g].n_chunks + per_cta - 1) / per_cta;
@@ -176,7 +176,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
     auto need = [&](long budget) {
         long n = 0;
         for (int g = 0; g < G; ++g)
-            for (int t = 0; t < shapes[g].m_tiles; t += 2) n += ctas_for(g, t, budget);
+            for (int t = 0; t < shapes[g].m_tiles; t += unit) n += ctas_for(g, t, budget);
         return n;
     };
     // the smallest budget that fits (need() does not grow with the budget; a
@@ -193,7 +193,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
     {
         long s = 0;
         for (int g = 0; g < G; ++g)
-            for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) counts[s] = (int32_t)ctas_for(g, t, lo);
+            for (int t = 0; t < shapes[g].m_tiles; t += unit, ++s) counts[s] = (int32_t)ctas_for(g, t, lo);
         for (long i = 0; i < nseg; ++i) grid += counts[i];
     }
     // spare CTAs shorten the longest ranges, measured in k-stages, then in chunks
@@ -201,7 +201,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
         long best = -1, best_stages = 0, best_len = 0;
         long s = 0;
         for (int g = 0; g < G; ++g)
-            for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) {
+            for (int t = 0; t < shapes[g].m_tiles; t += unit, ++s) {
                 const int n = shapes[g].n_chunks;
                 if (counts[s] >= n) continue;
                 const long len = (n + counts[s] - 1) / counts[s];  // longest range of this segment
@@ -219,7 +219,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
     int c = 0;
     long s = 0, base = 0;
     for (int g = 0; g < G; ++g)
-        for (int t = 0; t < shapes[g].m_tiles; t += 2, ++s) {
+        for (int t = 0; t < shapes[g].m_tiles; t += unit, ++s) {
             const long n = shapes[g].n_chunks;
             for (int j = 0; j < counts[s]; ++j) cta_begin[c++] = (int32_t)(base + (long)j * n / counts[s]);
             base += n;
@@ -229,7 +229,7 @@ int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair,
 }
 
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const GroupShape *shapes, int G, int cap_single, int cap_pair)
+                     const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair)
 {
     int g = 0;
     for (int c = 0; c < grid; ++c) {
@@ -242,18 +242,18 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
         r.g_base = chunk_prefix[g];
         r.g_tiles = shapes[g].m_tiles;
         r.g_rows = shapes[g].M;
-        // the kernel's walk: the part of the range in each pair is cut into
+        // the kernel's walk: the part of the range in each unit is cut into
         // ceil(len / cap) tiles of equal width (to within one chunk)
         int pos = r.begin, wg = g;
         r.max_chunks = 1;
         r.max_rows = 1;
         while (pos < r.end) {
-            while (pos >= chunk_prefix[wg] + ((shapes[wg].m_tiles + 1) / 2) * shapes[wg].n_chunks) ++wg;
+            while (pos >= chunk_prefix[wg] + ceil_div(shapes[wg].m_tiles, unit) * shapes[wg].n_chunks) ++wg;
             const int n = shapes[wg].n_chunks;
             const int local = pos - chunk_prefix[wg];
             const int mp = local / n;
             const int ch0 = local - mp * n;
-            const int mtu = std::min(kRowTilesPerUnit, shapes[wg].m_tiles - mp * kRowTilesPerUnit);
+            const int mtu = std::min(unit, shapes[wg].m_tiles - mp * unit);
             const int plen = std::min(n - ch0, r.end - pos);
             const int cap = mtu == 2 ? cap_pair : cap_single;
             const int pt = ceil_div(plen, cap);
@@ -265,7 +265,7 @@ void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const
 }
 
 void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t *chunk_prefix, const GroupShape *shapes,
-                int cap_single, int cap_pair)
+                int unit, int cap_single, int cap_pair)
 {
     double cost[kMaxCtas];
     int wg = 0;  // ranges ascend, so the group walk only moves forward
@@ -273,16 +273,16 @@ void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t 
         cost[c] = 0.0;
         int pos = ranges[c].begin;
         while (pos < ranges[c].end) {
-            while (pos >= chunk_prefix[wg] + ((shapes[wg].m_tiles + 1) / 2) * shapes[wg].n_chunks) ++wg;
+            while (pos >= chunk_prefix[wg] + ceil_div(shapes[wg].m_tiles, unit) * shapes[wg].n_chunks) ++wg;
             const int n = shapes[wg].n_chunks;
             const int local = pos - chunk_prefix[wg];
             const int mp = local / n;
             const int ch0 = local - mp * n;
-            const int mtu = std::min(kRowTilesPerUnit, shapes[wg].m_tiles - mp * kRowTilesPerUnit);
+            const int mtu = std::min(unit, shapes[wg].m_tiles - mp * unit);
             const int plen = std::min(n - ch0, ranges[c].end - pos);
             const int pt = ceil_div(plen, mtu == 2 ? cap_pair : cap_single);
             const double b_bytes = (double)plen * kChunkN * shapes[wg].k_tiles * (kTileK / 2) * 9.0 / 8.0;
-            const int rows = std::max(0, std::min(shapes[wg].M - mp * kRowTilesPerUnit * kTileM, mtu * kTileM));
+            const int rows = std::max(0, std::min(shapes[wg].M - mp * unit * kTileM, mtu * kTileM));
             const double c_bytes = (double)rows * plen * kChunkN * 2.0;
             const double wait = (mtu == 2 && pt >= 2) ? 4.0 * c_bytes * (pt - 1) / pt : 0.0;
             cost[c] += b_bytes + c_bytes + wait;
@@ -293,6 +293,73 @@ void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t 
     for (int c = 0; c < grid; ++c) idx[c] = c;
     std::stable_sort(idx, idx + grid, [&](int a, int b) { return cost[a] > cost[b]; });
     for (int c = 0; c < grid; ++c) order[c] = (uint8_t)idx[c];
+}
+
+namespace {
+
+// The kernel's walk of a schedule: the most tiles and k-stages any CTA
+// walks, and the widest tile (chunks) of two row tiles and of one.
+struct WalkStats {
+    int max_tiles = 0;
+    long max_stages = 0;
+    int max_pair_chunks = 0;
+    int max_single_chunks = 0;
+};
+
+WalkStats walk_stats(const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair,
+                     const int32_t *cta_begin, int grid)
+{
+    WalkStats w;
+    int g = 0;
+    long base = 0;  // first chunk of group g; ranges ascend, so g only moves forward
+    for (int c = 0; c < grid; ++c) {
+        long pos = cta_begin[c];
+        int tiles = 0;
+        long stages = 0;
+        while (pos < cta_begin[c + 1]) {
+            while (g < G && pos >= base + (long)ceil_div(shapes[g].m_tiles, unit) * shapes[g].n_chunks) {
+                base += (long)ceil_div(shapes[g].m_tiles, unit) * shapes[g].n_chunks;
+                ++g;
+            }
+            if (g >= G) break;
+            const long n = shapes[g].n_chunks;
+            const long mp = (pos - base) / n;
+            const long len = std::min<long>(base + (mp + 1) * n, cta_begin[c + 1]) - pos;
+            const int mtu = std::min<int>(unit, shapes[g].m_tiles - (int)mp * unit);
+            const long cap = mtu == 2 ? cap_pair : cap_single;
+            const long pt = (len + cap - 1) / cap;
+            const int width = (int)((len + pt - 1) / pt);
+            tiles += (int)pt;
+            stages += pt * shapes[g].k_tiles;
+            if (mtu == 2) w.max_pair_chunks = std::max(w.max_pair_chunks, width);
+            else w.max_single_chunks = std::max(w.max_single_chunks, width);
+            pos += len;
+        }
+        w.max_tiles = std::max(w.max_tiles, tiles);
+        w.max_stages = std::max(w.max_stages, stages);
+    }
+    return w;
+}
+
+}  // namespace
+
+UnitChoice choose_units(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int forced)
+{
+    if (forced == 2) return UnitChoice{2, false};
+    int32_t begin[kMaxCtas + 1];
+    int32_t counts[kMaxCtas];
+    const int grid1 = schedule_ctas(shapes, G, 1, cap_single, cap_pair, max_ctas, begin, counts);
+    const WalkStats w1 = walk_stats(shapes, G, 1, cap_single, cap_pair, begin, grid1);
+    // every CTA walks one tile: splitting a tile's accumulator over both
+    // halves never stalls a next tile (the kernel splits those of at most
+    // half the accumulator columns)
+    const bool split = grid1 > 0 && w1.max_tiles == 1;
+    if (forced == 1) return UnitChoice{1, split};
+    const int grid2 = schedule_ctas(shapes, G, 2, cap_single, cap_pair, max_ctas, begin, counts);
+    const WalkStats w2 = walk_stats(shapes, G, 2, cap_single, cap_pair, begin, grid2);
+    if (w2.max_pair_chunks > 0 && w2.max_pair_chunks <= 4 && split && w1.max_stages <= w2.max_stages)
+        return UnitChoice{1, true};
+    return UnitChoice{2, false};
 }
 
 void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes)
@@ -309,14 +376,14 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
 }
 
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw)
+                     const void *SFB, void *C, bool sf_raw, int unit)
 {
     if (!load_encode()) return false;
     const uint64_t Mg = (uint64_t)M;
     d.M = M;
     d.m_tiles = ceil_div(M, kTileM);
-    d.m_pairs = ceil_div(d.m_tiles, kRowTilesPerUnit);
-    d.b_keep = d.m_pairs > 1 ? 1 : 0;
+    d.m_units = ceil_div(d.m_tiles, unit);
+    d.b_keep = d.m_units > 1 ? 1 : 0;
     d.N = N;
     d.k_tiles = k_tiles_of(K);
     d.k_last = k_last_of(K);
@@ -364,7 +431,9 @@ struct nvfp4_ggemm_plan_s {
     int grid = 0;
     int total_chunks = 0;
     int cap_single = 8, cap_pair = 6;
-    std::vector<int32_t> m_tiles, m_pairs, chunk_prefix, cta_begin;
+    int unit = 2;        // 128-row tiles per unit of work
+    bool split = false;  // one-row-tile tiles accumulate in two halves
+    std::vector<int32_t> m_tiles, m_units, chunk_prefix, cta_begin;
     std::vector<GroupShape> shapes;
     std::vector<CtaRange> ctas;
     size_t off_prefix = 0, off_jobs = 0, table_bytes = 0;
@@ -439,6 +508,7 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
     if (out->b_static < 0 || out->b_static > 2) return NVFP4_ERR_INVALID_ARG;
+    if (out->row_units < 0 || out->row_units > 2) return NVFP4_ERR_INVALID_ARG;
     if (out->debug_check_fail != 0 && (out->debug_check_fail < kSiteCheckLoadB || out->debug_check_fail > kSiteCheckEpi))
         return NVFP4_ERR_INVALID_ARG;
     if (out->wait_timeout_ns == 0) out->wait_timeout_ns = kDefaultTimeoutNs;
@@ -459,7 +529,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         GroupDesc &d = groups[g];
         d.M = p->M[g];
         d.m_tiles = p->m_tiles[g];
-        d.m_pairs = p->m_pairs[g];
+        d.m_units = p->m_units[g];
         d.chunk_begin = p->chunk_prefix[g];
         if (p->M[g] == 0) continue;
         const int N = p->N[g], K = p->K[g], pieces = k_tiles_of(K);
@@ -472,7 +542,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
             items += ceil_div(p->M[g], 128) * pieces;
             ++njobs;
         }
-        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused())) return false;
+        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->unit)) return false;
         d.chunk_begin = p->chunk_prefix[g];
         if (ldc) d.ldc = ldc[g];
     }
@@ -576,8 +646,8 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         gp.groups = reinterpret_cast<const GroupDesc *>(s.d_table);
         gp.chunk_prefix = reinterpret_cast<const int32_t *>(s.d_table + p->off_prefix);
         pack_cta_starts(gp.cta, p->ctas.data(), p->grid, p->total_chunks, p->shapes.data());
-        order_ctas(gp.order, p->ctas.data(), p->grid, p->chunk_prefix.data(), p->shapes.data(), p->cap_single,
-                   p->cap_pair);
+        order_ctas(gp.order, p->ctas.data(), p->grid, p->chunk_prefix.data(), p->shapes.data(), p->unit,
+                   p->cap_single, p->cap_pair);
         const GroupDesc *hg = reinterpret_cast<const GroupDesc *>(s.h_table);
         for (int g = 0; g < std::min(p->G, kParamGroups); ++g) gp.pmaps[g] = hg[g].maps;
         gp.err = p->d_err;
@@ -587,6 +657,8 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         gp.cap_pair = p->cap_pair;
         gp.debug_skip_load = p->opt.debug_skip_load;
         gp.debug_check_fail = p->opt.debug_check_fail;
+        gp.unit_tiles = p->unit;
+        gp.split_acc = p->split ? 1 : 0;
     }
     Slot &s = p->slots[slot];
 
@@ -645,12 +717,13 @@ void nvfp4_ggemm_default_options(nvfp4_ggemm_options_t *opt)
     opt->b_static = 0;
 }
 
-nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,
-                                    int32_t tile_n, int32_t max_ctas, int32_t *cta_begin, int32_t *grid)
+nvfp4_status_t nvfp4_ggemm_schedule_units(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,
+                                          int32_t tile_n, int32_t max_ctas, int32_t row_units, int32_t *cta_begin,
+                                          int32_t *grid, int32_t *units, int32_t *split_acc)
 {
     if (!M || !N || !K || !cta_begin || !grid || num_groups < 1 || num_groups > kMaxGroups)
         return NVFP4_ERR_INVALID_ARG;
-    if (max_ctas < 1 || max_ctas > kMaxCtas) return NVFP4_ERR_INVALID_ARG;
+    if (max_ctas < 1 || max_ctas > kMaxCtas || row_units < 0 || row_units > 2) return NVFP4_ERR_INVALID_ARG;
     if (tile_n == 0) tile_n = kDefaultTileN;
     if (tile_n < kChunkN || tile_n > kMaxTileN || tile_n % kChunkN != 0) return NVFP4_ERR_INVALID_ARG;
     std::vector<GroupShape> shapes(num_groups);
@@ -660,13 +733,23 @@ nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int3
         if (M[g] < 0 || M[g] > kMaxM) return NVFP4_ERR_INVALID_ARG;
         if (!shape_ok(N[g], K[g])) return NVFP4_ERR_UNSUPPORTED_SHAPE;
         shapes[g] = group_shape(M[g], N[g], K[g]);
-        total += (long)ceil_div(shapes[g].m_tiles, kRowTilesPerUnit) * shapes[g].n_chunks;
+        total += (long)shapes[g].m_tiles * shapes[g].n_chunks;
     }
     if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     const int cap_single = tile_n / kChunkN;
     const int cap_pair = std::min(cap_single, pair_cap_chunks(variant_width(tile_n)));
-    *grid = schedule_ctas(shapes.data(), num_groups, cap_single, cap_pair, max_ctas, cta_begin, counts.data());
+    const UnitChoice uc = choose_units(shapes.data(), num_groups, cap_single, cap_pair, max_ctas, row_units);
+    *grid = schedule_ctas(shapes.data(), num_groups, uc.unit, cap_single, cap_pair, max_ctas, cta_begin,
+                          counts.data());
+    if (units) *units = uc.unit;
+    if (split_acc) *split_acc = uc.split ? 1 : 0;
     return NVFP4_OK;
+}
+
+nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, const int32_t *N, const int32_t *K,
+                                    int32_t tile_n, int32_t max_ctas, int32_t *cta_begin, int32_t *grid)
+{
+    return nvfp4_ggemm_schedule_units(num_groups, M, N, K, tile_n, max_ctas, 2, cta_begin, grid, nullptr, nullptr);
 }
 
 nvfp4_status_t nvfp4_ggemm_plan(nvfp4_ggemm_plan_t *out, int device, int num_groups, const int32_t *M, int32_t N,
@@ -743,40 +826,47 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
         return NVFP4_ERR_CUDA;
     }
 
-    // Work decomposition: m_pairs_g x ceil(N_g/32) chunks per group, prefix-summed.
+    // Work decomposition: m_units_g x ceil(N_g/32) chunks per group, prefix-summed.
     p->cap_single = opt.tile_n / kChunkN;
     p->cap_pair = std::min(p->cap_single, pair_cap_chunks(p->var.max_n));
     p->chunk_prefix.assign(num_groups + 1, 0);
     p->m_tiles.assign(num_groups, 0);
-    p->m_pairs.assign(num_groups, 0);
+    p->m_units.assign(num_groups, 0);
     p->shapes.assign(num_groups, GroupShape{});
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         p->m_tiles[g] = ceil_div(M[g], kTileM);
-        p->m_pairs[g] = ceil_div(p->m_tiles[g], kRowTilesPerUnit);
         p->shapes[g] = group_shape(M[g], N[g], K[g]);
-        p->chunk_prefix[g] = (int32_t)total;
-        total += (long)p->m_pairs[g] * p->shapes[g].n_chunks;
+        total += (long)p->m_tiles[g] * p->shapes[g].n_chunks;  // the most chunks either unit gives
     }
     if (total > 0x7FFFFFFF) {
         release(p);
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     }
+    const int cap = std::min(opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms, kMaxCtas);
+    const UnitChoice uc = choose_units(p->shapes.data(), num_groups, p->cap_single, p->cap_pair, cap, opt.row_units);
+    p->unit = uc.unit;
+    p->split = uc.split;
+    total = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        p->m_units[g] = ceil_div(p->m_tiles[g], p->unit);
+        p->chunk_prefix[g] = (int32_t)total;
+        total += (long)p->m_units[g] * p->shapes[g].n_chunks;
+    }
     p->chunk_prefix[num_groups] = (int32_t)total;
     p->total_chunks = (int)total;
-    const int cap = std::min(opt.max_ctas > 0 ? std::min(opt.max_ctas, sms) : sms, kMaxCtas);
     p->cta_begin.assign(cap + 1, 0);
     {
         std::vector<int32_t> counts(kMaxCtas, 0);
-        p->grid = schedule_ctas(p->shapes.data(), num_groups, p->cap_single, p->cap_pair, cap, p->cta_begin.data(),
-                                counts.data());
+        p->grid = schedule_ctas(p->shapes.data(), num_groups, p->unit, p->cap_single, p->cap_pair, cap,
+                                p->cta_begin.data(), counts.data());
     }
     p->cta_begin.resize(p->grid + 1);
 
     p->off_prefix = align_up(sizeof(GroupDesc) * (size_t)num_groups, 64);
     p->ctas.assign(std::max(p->grid, 1), CtaRange{});
     fill_cta_ranges(p->ctas.data(), p->cta_begin.data(), p->grid, p->chunk_prefix.data(), p->shapes.data(),
-                    num_groups, p->cap_single, p->cap_pair);
+                    num_groups, p->unit, p->cap_single, p->cap_pair);
     p->off_jobs = align_up(p->off_prefix + sizeof(int32_t) * (size_t)(num_groups + 1), 64);
     p->table_bytes = align_up(p->off_jobs + sizeof(RelayoutJob) * 2 * (size_t)num_groups, 128);
 
@@ -1145,6 +1235,8 @@ nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_i
     info->smem_bytes = ggemm_smem_bytes(plan->variant);
     info->kernels_per_run = plan->total_chunks == 0 ? 0 : (plan->relayout() ? 2 : 1);
     info->sf_path = plan->relayout() ? NVFP4_SF_RELAYOUT : NVFP4_SF_FUSED;
+    info->row_units = plan->unit;
+    info->split_acc = plan->split ? 1 : 0;
     return NVFP4_OK;
 }
 

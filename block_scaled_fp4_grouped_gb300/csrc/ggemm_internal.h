@@ -104,9 +104,9 @@ struct alignas(128) GroupDesc {
     uint16_t *C;               // C_g fp16 [M_g][ldc], columns [0, N_g) written
     int32_t M;
     int32_t m_tiles;      // ceil(M / 128)
-    int32_t m_pairs;      // ceil(m_tiles / 2): passes over B
+    int32_t m_units;      // ceil(m_tiles / row tiles per unit): passes over B
     int32_t chunk_begin;  // first scheduling chunk of this group (prefix sum)
-    int32_t b_keep;       // 1: B is read by more than one pair of row tiles (keep it in L2)
+    int32_t b_keep;       // 1: B is read by more than one unit of row tiles (keep it in L2)
     int32_t N;            // N_g
     int32_t k_tiles;      // ceil(K_g / 256)
     int32_t n_chunks;     // ceil(N_g / 32)
@@ -179,10 +179,11 @@ NVFP4_HD int cta_max_rows(uint32_t packed) { return (int)((packed >> 13) & 0x1u)
 NVFP4_HD int cta_k_last(uint32_t packed) { return (int)((packed >> 14) & 0x3u) + 1; }
 NVFP4_HD int cta_n_chunks(uint32_t packed) { return (int)(packed >> 16); }
 
-// Work decomposition: group g owns m_pairs_g * ceil(N_g/32) chunks (32
-// columns of one pair of 128-row tiles), numbered after the chunks of groups
-// 0..g-1 (chunk_prefix), pair by pair; a pair is a "segment" of ceil(N_g/32)
-// chunks.
+// Work decomposition: a plan's units of work are pairs of 128-row tiles
+// (unit 2; the last unit of a group with an odd tile count has one) or
+// single row tiles (unit 1). Group g owns m_units_g * ceil(N_g/32) chunks (32
+// columns of one unit), numbered after the chunks of groups 0..g-1
+// (chunk_prefix), unit by unit; a unit is a "segment" of ceil(N_g/32) chunks.
 // CTA c takes the chunk range [cta_begin[c], cta_begin[c+1]) and walks it as
 // tiles inside one segment of up to cap_pair chunks (segments with two row
 // tiles, whose accumulators share TMEM) or cap_single chunks (one row tile).
@@ -207,6 +208,10 @@ struct GemmParams {
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
     int32_t early;                 // kEarly* bits: operands loaded before the previous kernel completes
     int32_t debug_check_fail;      // debug build, test only: the check site forced to fail (0 = none)
+    int32_t unit_tiles;            // row tiles per unit of work: 2 (pairs) or 1
+    int32_t split_acc;             // 1: a one-row-tile tile of at most half the accumulator columns
+                                   // adds its even and odd 64-k slices into the two halves, which
+                                   // the epilogue sums (two MMA chains instead of one)
 #ifdef NVFP4_TRACE
     unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null
 #endif
@@ -216,7 +221,7 @@ struct GemmParams {
 // each range exactly as the kernel does to bound its tiles; pack_cta_starts
 // turns them into the kernel's start records (grid + 1 entries).
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
-                     const GroupShape *shapes, int G, int cap_single, int cap_pair);
+                     const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair);
 void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes);
 
 // Which block walks which range: the ranges sorted by an estimate of their
@@ -230,7 +235,7 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
 // or beats every input group order tried, by up to 1.2 us on the skinny
 // 8-group shape).
 void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t *chunk_prefix, const GroupShape *shapes,
-                int cap_single, int cap_pair);
+                int unit, int cap_single, int cap_pair);
 
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {
@@ -277,15 +282,31 @@ cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t 
 // widest tile is max_n columns (their accumulators share TMEM).
 int pair_cap_chunks(int max_n);
 
-// Splits the chunks of all segments (pairs of row tiles, group by group)
-// into per-CTA ranges, written to cta_begin[0..grid], and returns grid
+// Splits the chunks of all segments (units of `unit` row tiles, group by
+// group) into per-CTA ranges, written to cta_begin[0..grid], and returns grid
 // (<= max_ctas <= kMaxCtas). With no more segments than max_ctas, every range
 // lies inside one segment: the split takes the smallest per-CTA budget of
 // k-stages (passes over K_g times ceil(K_g / 256)) that fits max_ctas CTAs, and
 // spare CTAs then shorten the longest ranges; otherwise the chunks are split
 // into equal contiguous ranges. counts is scratch for kMaxCtas ints.
-int schedule_ctas(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int32_t *cta_begin,
-                  int32_t *counts);
+int schedule_ctas(const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair, int max_ctas,
+                  int32_t *cta_begin, int32_t *counts);
+
+// Row tiles per unit of work, and whether one-row-tile tiles split their
+// accumulator, for a plan over these shapes. forced 2: pairs; forced 1:
+// single row tiles; 0: pairs, unless their tiles would be at most four
+// chunks wide (narrow tiles: the stage's MMA chains, not the bytes, set the
+// pace) while single row tiles give every CTA one tile in no more k-stages
+// than pairs do. split: single row tiles and every CTA walks one tile; the
+// kernel then adds the even and odd 64-k slices of each such tile of at most
+// half the accumulator columns into the two halves (one MMA waits for the
+// previous one into the same accumulator, so two chains per stage take
+// about half as long).
+struct UnitChoice {
+    int unit;
+    bool split;
+};
+UnitChoice choose_units(const GroupShape *shapes, int G, int cap_single, int cap_pair, int max_ctas, int forced);
 using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                        const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                        CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -293,8 +314,8 @@ using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuin
 TensorMapEncodeFn tensor_map_encoder();  // nullptr when the driver has none
 
 // Fills one table entry (tensor maps, pointers, counts) for group g with
-// M_g > 0. sf_raw: encode the raw-scale maps; else store the atom pointers.
+// M_g > 0. sf_raw: encode the raw-scale maps; else the atom-layout maps.
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw);
+                     const void *SFB, void *C, bool sf_raw, int unit);
 
 }  // namespace nvfp4

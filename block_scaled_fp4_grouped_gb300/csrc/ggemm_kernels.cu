@@ -30,14 +30,18 @@
 //               blocks), RN to fp16, 32- or 16-byte stores of each row
 //               straight to C.
 // The producer lanes walk to their first tile before the prologue barrier.
-// Work: group g owns m_pairs_g x ceil(N_g/32) chunks (32 columns of one pair
-// of 128-row tiles); the chunks of all groups are numbered through prefix
+// Work: group g owns m_units_g x ceil(N_g/32) chunks (32 columns of one unit
+// of work: a pair of 128-row tiles, or one row tile when the plan chooses
+// single row tiles); the chunks of all groups are numbered through prefix
 // sums, and the host gives every CTA a contiguous chunk range (its start
 // record travels in the kernel parameters). A CTA walks its range as tiles
-// inside one pair: up to 192 columns when the pair has two row tiles (their
+// inside one unit: up to 192 columns when the unit has two row tiles (their
 // accumulators share TMEM) and up to MAXN when it has one. Both row tiles of
 // a pair share every B stage, so each B strip is read from HBM once, by one
-// SM. The host keeps every range inside one pair when it can and picks the
+// SM. With single row tiles and one tile of at most 192 columns per CTA
+// (split_acc), the tile adds its even and odd 64-k slices into the two
+// accumulator halves, and the epilogue sums them: an MMA waits for the
+// previous one into the same accumulator, so two chains halve that wait. The host keeps every range inside one pair when it can and picks the
 // smallest per-CTA budget of k-stages that fits the grid, so a CTA streams
 // its B strip in as few passes over K as possible. Block b walks range
 // order[b]: the host hands the ranges out heaviest first, as blocks with low
@@ -174,7 +178,7 @@ struct Unit {
     int mtu;     // row tiles in the unit (1 or 2)
     int n0;      // first column
     int ncols;   // tile width: a multiple of 32
-    bool keep;   // the group has more pairs of row tiles, which read B again
+    bool keep;   // the group has more units of row tiles, which read B again
     int M;       // rows of the group
     int N;       // columns of the group
     int k_tiles; // ceil(K of the group / 256)
@@ -188,9 +192,11 @@ struct Walker {
     // is cut into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
     int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_klast, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
+    int unit;  // row tiles per unit of work (1 or 2)
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
+        unit = p.unit_tiles == 1 ? 1 : 2;
         const int c = p.order[blockIdx.x];  // the range this block walks
         const CtaStart &r = p.cta[c];
         pos = r.begin;
@@ -209,7 +215,7 @@ struct Walker {
         if (pi == pt) {
             if (pos >= end) return false;
             // groups past the one holding `pos` (only ranges that span groups get here)
-            while (pos >= g_base + ((g_tiles + 1) >> 1) * g_chunks) {
+            while (pos >= g_base + (unit == 1 ? g_tiles : (g_tiles + 1) >> 1) * g_chunks) {
                 ++g;
                 const GroupDesc &gd = p.groups[g];
                 g_base = __ldg(p.chunk_prefix + g);
@@ -223,8 +229,8 @@ struct Walker {
             const int local = pos - g_base;
             const int mp = local / g_chunks;
             ch0 = local - mp * g_chunks;
-            mt0 = mp * kRowTilesPerUnit;
-            mtu = min(kRowTilesPerUnit, g_tiles - mt0);
+            mt0 = mp * unit;
+            mtu = min(unit, g_tiles - mt0);
             plen = min(g_chunks - ch0, end - pos);
             const int cap = mtu == 2 ? p.cap_pair : p.cap_single;
             pt = (plen + cap - 1) / cap;
@@ -239,7 +245,7 @@ struct Walker {
         t.mtu = mtu;
         t.n0 = (ch0 + c0) * kChunkN;
         t.ncols = (c1 - c0) * kChunkN;
-        t.keep = g_tiles > kRowTilesPerUnit;
+        t.keep = g_tiles > unit;
         t.M = g_rows;
         t.k_tiles = g_ktiles;
         t.k_last = g_klast;
@@ -520,6 +526,13 @@ struct Roles {
         record_error(p.err, kStatusFault, kSiteTileCheck);
         *abort_flag = 1;
         return false;
+    }
+
+    // A tile that adds its even and odd 64-k slices into the two accumulator
+    // halves (the plan's split_acc: one row tile, at most half the columns)
+    __device__ __forceinline__ bool split_tile(const Unit &t) const
+    {
+        return p.split_acc != 0 && t.mtu == 1 && t.ncols <= C::kPairN;
     }
 
 #ifdef NVFP4_DEBUG
@@ -890,7 +903,8 @@ struct Roles {
         Walker wk(p);
         Unit t;
         while (ok && wk.next(p, t)) {
-            const bool both = t.mtu > 1 || t.ncols > C::kPairN;
+            const bool split = split_tile(t);
+            const bool both = t.mtu > 1 || t.ncols > C::kPairN || split;
             const int h0 = both ? 0 : acc.next;
             if (!wait_phase(acc_empty(h0), acc.par(h0) ^ 1u, abort_flag, p, kSiteAccEmpty) ||
                 (both && !wait_phase(acc_empty(1), acc.par(1) ^ 1u, abort_flag, p, kSiteAccEmpty)))
@@ -917,7 +931,7 @@ struct Roles {
                 // regions, operands inside their rings; a failed check skips
                 // the stage's MMAs, and the commit below still frees the stage
                 const bool issue = NVFP4_CHECK(
-                    (h0 + t.mtu - 1) * C::kPairN + t.ncols <= C::kAccCols &&
+                    (split ? C::kPairN : (h0 + t.mtu - 1) * C::kPairN) + t.ncols <= C::kAccCols &&
                         C::kSfBase + rt.stage * kSfCols + kSfCols <= (int)kTmemCols &&
                         smem_in(sa, (uint32_t)t.mtu * kATileBytes, C::kOffARing, C::kOffARing + C::kARing) &&
                         smem_in(sb, (uint32_t)t.ncols * (kTileK / 2), C::kOffBRing, C::kOffBRing + C::kBRing),
@@ -925,6 +939,13 @@ struct Roles {
 #pragma unroll
                 for (int kk = 0; kk < 4 && issue; ++kk) {
                     const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
+                    if (split) {
+                        // slice kk into half kk & 1; each half starts from its first slice
+                        if (kk < slices)
+                            tc_mma_nvf4(d + (uint32_t)((kk & 1) * C::kPairN), desc_sw128_kmajor(sa + kk * 32), bdesc,
+                                        idesc, sf + kk * 4, sf + 32 + kk * 8, (kt | (kk >> 1)) != 0 ? 1u : 0u);
+                        continue;
+                    }
 #pragma unroll
                     for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
                         if (mt < t.mtu && kk < slices)
@@ -972,8 +993,11 @@ struct Roles {
             const int N = gd->N;
             const int ldc = gd->ldc;
             uint16_t *const cbase = gd->C;
-            const bool both = t.mtu > 1 || t.ncols > C::kPairN;
+            const bool split = split_tile(t);
+            const bool both = t.mtu > 1 || t.ncols > C::kPairN || split;
             const int h0 = both ? 0 : acc.next;
+            // a split tile's odd 64-k slices (none when K_g is one slice)
+            const bool odd = split && (t.k_tiles > 1 || t.k_last > 1);
             if (!warp_wait_phase(acc_full(h0), acc.par(h0), abort_flag, p, kSiteAccFull) ||
                 (both && !warp_wait_phase(acc_full(1), acc.par(1), abort_flag, p, kSiteAccFull)))
                 break;
@@ -996,7 +1020,8 @@ struct Roles {
                 uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
                 // (debug build) the accumulator columns this warp reads, and the
                 // 32-byte alignment of its rows' wide stores
-                if (!NVFP4_CHECK_WARP((h0 + mt) * C::kPairN + 32 * (h + 2 * (mine - 1) + 1) <= C::kAccCols &&
+                if (!NVFP4_CHECK_WARP((split ? C::kPairN : (h0 + mt) * C::kPairN) + 32 * (h + 2 * (mine - 1) + 1) <=
+                                              C::kAccCols &&
                                           (!wide_st || !live ||
                                            (reinterpret_cast<uintptr_t>(crow + t.n0 + 32 * h) & 31u) == 0),
                                       kSiteCheckEpi)) {
@@ -1006,6 +1031,24 @@ struct Roles {
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
                                        (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
                 uint32_t v0[32], v1[32];
+                if (split) {
+                    // the two halves' partial sums of each block, added in fp32
+#pragma unroll 1
+                    for (int j = 0; j < mine; ++j) {
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * j), v0);
+                        if (odd) tmem_ld_32x32b_x32(tbase + (uint32_t)(C::kPairN + 64 * j), v1);
+                        tmem_ld_wait();
+                        pin_registers(v0);
+                        if (odd) {
+                            pin_registers(v1);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(v1[i]));
+                        }
+                        if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), N, v0, wide_st, pol_c);
+                    }
+                    continue;
+                }
                 tmem_ld_32x32b_x32(tbase, v0);
 #pragma unroll 1
                 for (int j = 0; j < mine; j += 2) {

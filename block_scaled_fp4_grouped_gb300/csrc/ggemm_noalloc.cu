@@ -124,33 +124,39 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     auto *prefix = reinterpret_cast<int32_t *>(table + kPrefixOffset);
     const int n_chunks = ceil_div_i(N, kChunkN);
     GroupShape shapes[kNoAllocMaxGroups];
+    long most = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        shapes[g] = group_shape(M[g], N, K);
+        most += (long)shapes[g].m_tiles * n_chunks;
+    }
+    if (most > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the same units of work a plan with default options would use
+    const int cap_single = kMaxTileN / kChunkN;
+    const int cap_pair = pair_cap_chunks(kMaxTileN);
+    const int max_ctas = std::min(g_sm_count[dev], kMaxCtas);
+    const UnitChoice uc = choose_units(shapes, num_groups, cap_single, cap_pair, max_ctas, 0);
     long total = 0;
     for (int g = 0; g < num_groups; ++g) {
         GroupDesc &d = groups[g];
         d.M = M[g];
         d.m_tiles = ceil_div_i(M[g], kTileM);
-        d.m_pairs = ceil_div_i(d.m_tiles, kRowTilesPerUnit);
-        shapes[g] = group_shape(M[g], N, K);
+        d.m_units = ceil_div_i(d.m_tiles, uc.unit);
         d.chunk_begin = (int32_t)total;
         prefix[g] = (int32_t)total;
-        total += (long)d.m_pairs * n_chunks;
+        total += (long)d.m_units * n_chunks;
         if (M[g] == 0) continue;
-        if (!fill_group_desc(d, M[g], N, K, A[g], B[g], SFA[g], SFB[g], C[g], true))
+        if (!fill_group_desc(d, M[g], N, K, A[g], B[g], SFA[g], SFB[g], C[g], true, uc.unit))
             return NVFP4_ERR_CUDA;
         d.chunk_begin = prefix[g];
     }
     prefix[num_groups] = (int32_t)total;
     if (total == 0) return NVFP4_OK;
-    if (total > 0x7FFFFFFF) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    const int cap_single = kMaxTileN / kChunkN;
-    const int cap_pair = pair_cap_chunks(kMaxTileN);
     int32_t cta_begin[kMaxCtas + 1];
     int32_t counts[kMaxCtas];
-    const int grid = schedule_ctas(shapes, num_groups, cap_single, cap_pair, std::min(g_sm_count[dev], kMaxCtas),
-                                   cta_begin, counts);
+    const int grid = schedule_ctas(shapes, num_groups, uc.unit, cap_single, cap_pair, max_ctas, cta_begin, counts);
     if (grid < 1) return NVFP4_OK;
     CtaRange ranges[kMaxCtas];
-    fill_cta_ranges(ranges, cta_begin, grid, prefix, shapes, num_groups, cap_single, cap_pair);
+    fill_cta_ranges(ranges, cta_begin, grid, prefix, shapes, num_groups, uc.unit, cap_single, cap_pair);
 
     // --- upload (pageable source: the copy call returns once the bytes are
     //     staged, so the buffer may be rewritten by the next call), clear the
@@ -168,13 +174,15 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.groups = reinterpret_cast<const GroupDesc *>(scratch);
     gp.chunk_prefix = reinterpret_cast<const int32_t *>(scratch + kPrefixOffset);
     pack_cta_starts(gp.cta, ranges, grid, (int)total, shapes);
-    order_ctas(gp.order, ranges, grid, prefix, shapes, cap_single, cap_pair);
+    order_ctas(gp.order, ranges, grid, prefix, shapes, uc.unit, cap_single, cap_pair);
     gp.err = reinterpret_cast<uint32_t *>(scratch + kErrOffset);
     gp.timeout_ns = 2000000000ull;
     gp.G = num_groups;
     gp.cap_single = cap_single;
     gp.cap_pair = cap_pair;
     gp.debug_skip_load = 0;
+    gp.unit_tiles = uc.unit;
+    gp.split_acc = uc.split ? 1 : 0;
     if (ggemm_launch(variant, gp, grid, s, false) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;

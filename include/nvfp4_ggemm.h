@@ -144,6 +144,18 @@ typedef struct {
                                  detail word, the operation skipped, the kernel ending through
                                  its abort flag) runs without any invalid operation. The
                                  release build ignores it */
+    int32_t row_units;        /* 128-row tiles per unit of work: 0 (default) = the plan chooses,
+                                 1 = one row tile, 2 = pairs of row tiles. A pair shares every
+                                 B stage between its two row tiles, so each B strip is streamed
+                                 from memory once. The plan keeps pairs unless their tiles
+                                 would be at most 128 columns wide while single row tiles give
+                                 every CTA one tile of at most 192 columns in no more 256-k
+                                 stages (few tall groups and a narrow N, such as the two
+                                 2-group workloads of the pages). Such tiles then add their
+                                 even and odd 64-k slices into two accumulators, summed by the
+                                 epilogue: each MMA into an accumulator waits for the one
+                                 before it, so two chains take about half as long. Results
+                                 agree with pairs within the rounding of that one fp32 sum */
 } nvfp4_ggemm_options_t;
 
 typedef struct nvfp4_ggemm_plan_s *nvfp4_ggemm_plan_t;
@@ -283,8 +295,9 @@ NVFP4_API nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t ro
 NVFP4_API uint64_t nvfp4_sf_atom_bytes(int32_t rows, int32_t K);
 
 /*
- * The work split a plan would use, computed on the host alone (no device,
- * no allocation). M, N and K are host arrays of the G per-group sizes (the
+ * The work split of a plan whose units of work are pairs of row tiles
+ * (row_units 2), computed on the host alone (no device, no allocation).
+ * M, N and K are host arrays of the G per-group sizes (the
  * limits of nvfp4_ggemm_plan_shapes). Every group with M_g > 0 has
  * ceil(ceil(M_g/128)/2) pairs of 128-row tiles; each pair owns ceil(N_g/32)
  * consecutive 32-column chunks, numbered group by group. CTA c of the
@@ -304,6 +317,21 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_schedule(int num_groups, const int32_t *M, 
                                     const int32_t *K, int32_t tile_n, int32_t max_ctas,
                                     int32_t *cta_begin, int32_t *grid);
 
+/*
+ * The same split for units of row_units 128-row tiles (1 or 2; 0 = the
+ * choice a plan with default options makes, see row_units in
+ * nvfp4_ggemm_options_t). Units of one row tile own ceil(N_g/32) chunks each
+ * and their tiles are at most tile_n wide. *units (if not NULL) receives the
+ * row tiles per unit used, *split_acc (if not NULL) 1 when such a plan adds
+ * the even and odd 64-k slices of its one-row-tile tiles into two
+ * accumulators. nvfp4_ggemm_schedule is this call with row_units = 2. Host
+ * only; for inspection and testing.
+ */
+NVFP4_API nvfp4_status_t nvfp4_ggemm_schedule_units(int num_groups, const int32_t *M, const int32_t *N,
+                                          const int32_t *K, int32_t tile_n, int32_t max_ctas,
+                                          int32_t row_units, int32_t *cta_begin, int32_t *grid,
+                                          int32_t *units, int32_t *split_acc);
+
 /* Plan introspection (for tests and benchmarks). */
 typedef struct {
     int32_t tile_n;        /* widest output tile (columns) */
@@ -316,6 +344,8 @@ typedef struct {
     int32_t kernels_per_run; /* kernel launches enqueued by one run */
     int32_t sf_path;       /* the scale path runs take: NVFP4_SF_FUSED, or NVFP4_SF_RELAYOUT (asked for,
                               or forced by a raw-scale plan with some K_g % 256 != 0) */
+    int32_t row_units;     /* 128-row tiles per unit of work: 1 or 2 (see nvfp4_ggemm_options_t) */
+    int32_t split_acc;     /* 1: one-row-tile tiles accumulate in two accumulators */
 } nvfp4_ggemm_plan_info_t;
 
 NVFP4_API nvfp4_status_t nvfp4_ggemm_plan_info(nvfp4_ggemm_plan_t plan, nvfp4_ggemm_plan_info_t *info);

@@ -34,7 +34,7 @@ def atom_copy(sf_dev, rows: int, K: int):
 
 
 def run_gpu(prob, sf_layout="raw", sf_path="fused", tile_n=0, cache_b_scales=False, sentinel=None,
-            max_ctas=0, use_host=False, b_stages=0, a_stages=0):
+            max_ctas=0, use_host=False, b_stages=0, a_stages=0, row_units=0):
     """Returns the list of C_g as numpy float16 arrays."""
     torch = torch_mod()
     from block_scaled_fp4_grouped_gb300 import binding as nb
@@ -62,7 +62,7 @@ def run_gpu(prob, sf_layout="raw", sf_path="fused", tile_n=0, cache_b_scales=Fal
     C = [torch.full((m, N), fill, dtype=torch.float16, device="cuda") for m in prob.M]
     with nb.GroupedGemm(prob.M, N, K, sf_layout=sf_layout, sf_path=sf_path, tile_n=tile_n,
                         cache_b_scales=cache_b_scales, max_ctas=max_ctas, b_stages=b_stages,
-                        a_stages=a_stages) as gg:
+                        a_stages=a_stages, row_units=row_units) as gg:
         if cache_b_scales:
             gg.prepare_b_scales(SFB)
             gg.run(A, B, SFA, [None] * len(SFB), C)

@@ -83,7 +83,8 @@ def test_plan_rejects_bad_options(L):
     for field, val in [("sf_layout", 2), ("sf_path", 5), ("cache_b_scales", 3), ("tile_n", 80),
                        ("tile_n", 288), ("max_ctas", -1), ("debug_skip_load", -2), ("struct_size", 8),
                        ("b_stages", 3), ("a_stages", 9), ("debug_check_fail", 0x20), ("debug_check_fail", 0x27),
-                       ("debug_check_fail", -1), ("b_static", 3), ("b_static", -1)]:
+                       ("debug_check_fail", -1), ("b_static", 3), ("b_static", -1), ("row_units", 3),
+                       ("row_units", -1)]:
         opt = nb.nvfp4_ggemm_default_options()
         setattr(opt, field, val)
         st, h = nb.nvfp4_ggemm_plan(0, [64], 256, 256, opt)

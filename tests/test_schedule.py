@@ -185,3 +185,107 @@ def test_per_group_bad_shapes():
     for N, K in (([256, 12], [256, 256]), ([256, 256], [256, 300])):
         st, _ = nb.nvfp4_ggemm_schedule([64, 64], N, 0, 152, K=K)
         assert st == nb.NVFP4_ERR_UNSUPPORTED_SHAPE
+
+
+# ------------------------------------------------- units of one row tile
+
+def check_single(M, N, tile_n, max_ctas):
+    """row_units = 1: every group's ceil(M_g/128) row tiles own ceil(N/32)
+    chunks each; the same properties as for pairs, with every segment one
+    row tile wide (tiles of at most tile_n). Returns (cta_begin, split)."""
+    st, cb, units, split = nb.nvfp4_ggemm_schedule_units(M, N, tile_n, max_ctas, 256, 1)
+    assert st == nb.NVFP4_OK and units == 1
+    n = -(-N // 32)
+    segs = sum(-(-m // 128) for m in M)
+    total = segs * n
+    grid = len(cb) - 1
+    if total == 0:
+        assert grid == 0
+        return cb, split
+    assert 1 <= grid <= max_ctas
+    assert cb[0] == 0 and cb[-1] == total
+    assert all(b > a for a, b in zip(cb, cb[1:]))
+    single, _ = caps(tile_n)
+    tiles = [-(-(b - a) // single) for a, b in zip(cb, cb[1:])]
+    if segs <= max_ctas:
+        fewest = next(P for P in range(1, 10 ** 6) if segs * -(-n // (P * single)) <= max_ctas)
+        for a, b in zip(cb, cb[1:]):
+            assert (b - 1) // n == a // n, f"range [{a},{b}) crosses a row tile boundary"
+        assert max(tiles) <= fewest
+        # split accumulators exactly when every CTA walks one tile
+        assert split == (1 if max(tiles) == 1 else 0)
+    return cb, split
+
+
+@pytest.mark.parametrize("tile_n", [0, 256, 192, 128, 64])
+def test_single_row_units_random_shapes(tile_n):
+    rng = random.Random(4321 + tile_n)
+    for _ in range(150):
+        G = rng.randint(1, 10)
+        M = [rng.choice([0, rng.randint(1, 700)]) for _ in range(G)]
+        N = 8 * rng.randint(1, 1200)
+        check_single(M, N, tile_n, rng.choice([1, 5, 37, 152, 192]))
+
+
+def test_pairs_through_the_units_entry_match_the_pair_schedule():
+    rng = random.Random(99)
+    for _ in range(100):
+        M = [rng.randint(0, 700) for _ in range(rng.randint(1, 8))]
+        N = 8 * rng.randint(1, 900)
+        st, cb, units, split = nb.nvfp4_ggemm_schedule_units(M, N, 0, 152, 256, 2)
+        assert st == nb.NVFP4_OK and units == 2 and split == 0
+        assert cb == nb.nvfp4_ggemm_schedule(M, N, 0, 152)[1]
+
+
+@pytest.mark.parametrize("cfg,want", [("c0", 2), ("c1", 1), ("c2", 1), ("c3", 2), ("c4", 2),
+                                      ("c1_page", 1), ("c2_page", 1), ("c3_page", 2), ("c4_page", 2)])
+def test_automatic_units_on_the_workloads(cfg, want):
+    """Pairs stay unless their tiles would be at most four chunks wide while
+    one-row-tile units give every CTA a single tile: the two 2-group
+    workloads (tall groups, narrow N) take single row tiles with split
+    accumulators; the 8-group ones and the small case keep pairs."""
+    import numpy as np
+    from block_scaled_fp4_grouped_gb300 import synth
+    if cfg.endswith("_page"):
+        d = synth.PAGE_SHAPES[cfg]
+        M, N, K = d["M"], d["N"], d["K"]
+    else:
+        spec = synth.CONFIGS[cfg]
+        M, N, K = synth.draw_m_list(spec, np.random.default_rng(0)), spec.N, spec.K
+    st, cb, units, split = nb.nvfp4_ggemm_schedule_units(M, N, 0, 152, K, 0)
+    assert st == nb.NVFP4_OK and units == want
+    assert split == (1 if want == 1 else 0)
+    if want == 1:
+        assert cb == nb.nvfp4_ggemm_schedule_units(M, N, 0, 152, K, 1)[1]
+    else:
+        assert cb == nb.nvfp4_ggemm_schedule(M, N, 0, 152, K)[1]
+
+
+def test_automatic_units_rule_on_random_shapes():
+    """Whenever the choice is single row tiles, every CTA walks one tile and
+    the pair split's two-row-tile tiles would be at most four chunks wide."""
+    rng = random.Random(7)
+    for _ in range(200):
+        M = [rng.randint(0, 600) for _ in range(rng.randint(1, 6))]
+        N = 8 * rng.randint(1, 700)
+        st, cb, units, split = nb.nvfp4_ggemm_schedule_units(M, N, 0, 152, 256, 0)
+        assert st == nb.NVFP4_OK and units in (1, 2)
+        if units == 1:
+            assert split == 1
+            assert max(b - a for a, b in zip(cb, cb[1:])) <= 8
+            n = -(-N // 32)
+            _, cb2 = nb.nvfp4_ggemm_schedule(M, N, 0, 152)
+            segs = pairs_of(M)
+            widest = 0
+            for a, b in zip(cb2, cb2[1:]):
+                if segs[a // n] == 2:
+                    cap = 6
+                    pt = -(-(b - a) // cap)
+                    widest = max(widest, -(-(b - a) // pt))
+            assert 0 < widest <= 4
+
+
+@pytest.mark.parametrize("row_units", [-1, 3])
+def test_units_entry_rejects_bad_unit_counts(row_units):
+    st, cb, units, split = nb.nvfp4_ggemm_schedule_units([64], 256, 0, 152, 256, row_units)
+    assert st == nb.NVFP4_ERR_INVALID_ARG
