@@ -503,7 +503,7 @@ nvfp4_status_t validate_options(const nvfp4_ggemm_options_t *in, nvfp4_ggemm_opt
     if (out->b_stages < 0 || out->a_stages < 0 || (out->b_stages == 0) != (out->a_stages == 0))
         return NVFP4_ERR_INVALID_ARG;
     const bool raw_fused = out->sf_layout == NVFP4_SF_RAW && out->sf_path == NVFP4_SF_FUSED;
-    if (ggemm_variant_index(variant_width(out->tile_n), out->b_stages, out->a_stages, raw_fused) < 0)
+    if (ggemm_variant_index(variant_width(out->tile_n), out->b_stages, out->a_stages, raw_fused, 2) < 0)
         return NVFP4_ERR_INVALID_ARG;
     if (out->max_ctas < 0 || out->debug_skip_load < 0) return NVFP4_ERR_INVALID_ARG;
     if (out->serial_launch != 0 && out->serial_launch != 1) return NVFP4_ERR_INVALID_ARG;
@@ -657,7 +657,6 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
         gp.cap_pair = p->cap_pair;
         gp.debug_skip_load = p->opt.debug_skip_load;
         gp.debug_check_fail = p->opt.debug_check_fail;
-        gp.unit_tiles = p->unit;
         gp.split_acc = p->split ? 1 : 0;
     }
     Slot &s = p->slots[slot];
@@ -784,7 +783,7 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
         for (int g = 0; g < num_groups; ++g) {
             if (raw_tma_ok(K[g])) continue;
             opt.sf_path = NVFP4_SF_RELAYOUT;
-            if (ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, false) < 0)
+            if (ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, false, 2) < 0)
                 opt.b_stages = opt.a_stages = 0;
             break;
         }
@@ -815,7 +814,7 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     p->K.assign(K, K + num_groups);
     p->opt = opt;
 
-    p->variant = ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused());
+    p->variant = ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused(), 2);
     if (p->variant < 0) {
         release(p);
         return NVFP4_ERR_INVALID_ARG;
@@ -847,6 +846,18 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     const UnitChoice uc = choose_units(p->shapes.data(), num_groups, p->cap_single, p->cap_pair, cap, opt.row_units);
     p->unit = uc.unit;
     p->split = uc.split;
+    if (p->unit != 2) {  // the same ring configuration, built for single row tiles
+        p->variant = ggemm_variant_index(p->var.max_n, p->var.b_stages, p->var.a_stages, p->var.sf_raw, p->unit);
+        if (p->variant < 0) {
+            release(p);
+            return NVFP4_ERR_INVALID_ARG;
+        }
+        p->var = ggemm_variant(p->variant);
+        if (ggemm_configure(p->variant) != cudaSuccess) {
+            release(p);
+            return NVFP4_ERR_CUDA;
+        }
+    }
     total = 0;
     for (int g = 0; g < num_groups; ++g) {
         p->m_units[g] = ceil_div(p->m_tiles[g], p->unit);

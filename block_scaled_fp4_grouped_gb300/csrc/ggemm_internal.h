@@ -208,10 +208,9 @@ struct GemmParams {
     int32_t debug_skip_load;       // test-only fault injection (0 = off)
     int32_t early;                 // kEarly* bits: operands loaded before the previous kernel completes
     int32_t debug_check_fail;      // debug build, test only: the check site forced to fail (0 = none)
-    int32_t unit_tiles;            // row tiles per unit of work: 2 (pairs) or 1
-    int32_t split_acc;             // 1: a one-row-tile tile of at most half the accumulator columns
-                                   // adds its even and odd 64-k slices into the two halves, which
-                                   // the epilogue sums (two MMA chains instead of one)
+    int32_t split_acc;             // kernels for single row tiles: 1 = a tile of at most half the
+                                   // accumulator columns adds its even and odd 64-k slices into the
+                                   // two halves, which the epilogue sums (two MMA chains, not one)
 #ifdef NVFP4_TRACE
     unsigned long long *trace;     // [grid][kTraceSlots] timeline of this launch, or null
 #endif
@@ -254,17 +253,19 @@ struct RelayoutParams {
     int32_t total_items;
 };
 
-// GEMM kernel variants: widest tile, B ring depth, A ring depth, scale path.
+// GEMM kernel variants: widest tile, B ring depth, A ring depth, scale path,
+// 128-row tiles per unit of work (each configuration is built for 2 and 1).
 struct GemmVariant {
     int max_n;
     int b_stages;
     int a_stages;
     bool sf_raw;
+    int unit;
 };
 
 // Returns the variant index, or -1. b_stages / a_stages 0 pick the default
-// depths for (max_n, sf_raw).
-int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw);
+// depths for (max_n, sf_raw, unit).
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit);
 GemmVariant ggemm_variant(int index);
 int ggemm_smem_bytes(int index);
 int ggemm_threads();

@@ -185,18 +185,19 @@ struct Unit {
     int k_last;  // 64-k slices in the last k tile (1..4)
 };
 
-// Walks this CTA's contiguous range of chunks as tiles.
+// Walks this CTA's contiguous range of chunks as tiles, for units of UNIT
+// 128-row tiles (the plan's row tiles per unit, 1 or 2).
+template <int UNIT>
 struct Walker {
+    static_assert(UNIT == 1 || UNIT == 2, "row tiles per unit");
     int pos, end;
-    // the part of the range inside the current pair (plen chunks from ch0)
+    // the part of the range inside the current unit (plen chunks from ch0)
     // is cut into pt tiles of equal width (to within one chunk); pi = next tile
     int plen = 0, pt = 0, pi = 0;
     int g, g_base, g_tiles, g_rows, g_chunks, g_ktiles, g_klast, g_cols = -1, mt0 = 0, mtu = 0, ch0 = 0;
-    int unit;  // row tiles per unit of work (1 or 2)
 
     __device__ __forceinline__ explicit Walker(const GemmParams &p)
     {
-        unit = p.unit_tiles == 1 ? 1 : 2;
         const int c = p.order[blockIdx.x];  // the range this block walks
         const CtaStart &r = p.cta[c];
         pos = r.begin;
@@ -215,7 +216,7 @@ struct Walker {
         if (pi == pt) {
             if (pos >= end) return false;
             // groups past the one holding `pos` (only ranges that span groups get here)
-            while (pos >= g_base + (unit == 1 ? g_tiles : (g_tiles + 1) >> 1) * g_chunks) {
+            while (pos >= g_base + (UNIT == 1 ? g_tiles : (g_tiles + 1) >> 1) * g_chunks) {
                 ++g;
                 const GroupDesc &gd = p.groups[g];
                 g_base = __ldg(p.chunk_prefix + g);
@@ -229,8 +230,8 @@ struct Walker {
             const int local = pos - g_base;
             const int mp = local / g_chunks;
             ch0 = local - mp * g_chunks;
-            mt0 = mp * unit;
-            mtu = min(unit, g_tiles - mt0);
+            mt0 = mp * UNIT;
+            mtu = min(UNIT, g_tiles - mt0);
             plen = min(g_chunks - ch0, end - pos);
             const int cap = mtu == 2 ? p.cap_pair : p.cap_single;
             pt = (plen + cap - 1) / cap;
@@ -245,7 +246,7 @@ struct Walker {
         t.mtu = mtu;
         t.n0 = (ch0 + c0) * kChunkN;
         t.ncols = (c1 - c0) * kChunkN;
-        t.keep = g_tiles > unit;
+        t.keep = g_tiles > UNIT;
         t.M = g_rows;
         t.k_tiles = g_ktiles;
         t.k_last = g_klast;
@@ -487,9 +488,10 @@ struct MapUse {
     }
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
 struct Roles {
     using C = Cfg<MAXN, NB, NA, NS, RAW>;
+    using Walker = nvfp4::Walker<UNIT>;
     static constexpr int NT = C::kNT;
 
     uint8_t *smem;
@@ -532,7 +534,8 @@ struct Roles {
     // halves (the plan's split_acc: one row tile, at most half the columns)
     __device__ __forceinline__ bool split_tile(const Unit &t) const
     {
-        return p.split_acc != 0 && t.mtu == 1 && t.ncols <= C::kPairN;
+        if constexpr (UNIT == 2) return false;  // pairs: never (the code below compiles away)
+        return p.split_acc != 0 && t.ncols <= C::kPairN;
     }
 
 #ifdef NVFP4_DEBUG
@@ -936,22 +939,25 @@ struct Roles {
                         smem_in(sa, (uint32_t)t.mtu * kATileBytes, C::kOffARing, C::kOffARing + C::kARing) &&
                         smem_in(sb, (uint32_t)t.ncols * (kTileK / 2), C::kOffBRing, C::kOffBRing + C::kBRing),
                     kSiteCheckMma);
+                if (split) {
+                    // slice kk into half kk & 1; each half starts from its first slice
 #pragma unroll
-                for (int kk = 0; kk < 4 && issue; ++kk) {
-                    const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
-                    if (split) {
-                        // slice kk into half kk & 1; each half starts from its first slice
+                    for (int kk = 0; kk < 4 && issue; ++kk)
                         if (kk < slices)
-                            tc_mma_nvf4(d + (uint32_t)((kk & 1) * C::kPairN), desc_sw128_kmajor(sa + kk * 32), bdesc,
-                                        idesc, sf + kk * 4, sf + 32 + kk * 8, (kt | (kk >> 1)) != 0 ? 1u : 0u);
-                        continue;
-                    }
+                            tc_mma_nvf4(d + (uint32_t)((kk & 1) * C::kPairN), desc_sw128_kmajor(sa + kk * 32),
+                                        desc_sw128_kmajor(sb + kk * 32), idesc, sf + kk * 4, sf + 32 + kk * 8,
+                                        (kt | (kk >> 1)) != 0 ? 1u : 0u);
+                } else {
 #pragma unroll
-                    for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
-                        if (mt < t.mtu && kk < slices)
-                            tc_mma_nvf4(d + (uint32_t)(mt * C::kPairN), desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32),
-                                        bdesc, idesc, sf + mt * 16 + kk * 4, sf + 32 + kk * 8,
-                                        (kt | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4 && issue; ++kk) {
+                        const uint64_t bdesc = desc_sw128_kmajor(sb + kk * 32);
+#pragma unroll
+                        for (int mt = 0; mt < kRowTilesPerUnit; ++mt)
+                            if (mt < t.mtu && kk < slices)
+                                tc_mma_nvf4(d + (uint32_t)(mt * C::kPairN),
+                                            desc_sw128_kmajor(sa + mt * kATileBytes + kk * 32), bdesc, idesc,
+                                            sf + mt * 16 + kk * 4, sf + 32 + kk * 8, (kt | kk) != 0 ? 1u : 0u);
+                    }
                 }
                 // the stages and the scale buffer are free once these MMAs have read them
                 tc_commit(done(seq % kDoneRing));
@@ -1011,28 +1017,21 @@ struct Roles {
             const int mine = (nblk - h + 1) / 2;
             const bool wide_st = ((reinterpret_cast<uintptr_t>(cbase) & 31u) == 0) && (N % 16 == 0) && (ldc % 16 == 0);
             bool failed = false;
-#pragma unroll
-            for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
-                const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
-                if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
-                const int row = row0 + lane;
-                const bool live = row < t.M;
-                uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
-                // (debug build) the accumulator columns this warp reads, and the
-                // 32-byte alignment of its rows' wide stores
-                if (!NVFP4_CHECK_WARP((split ? C::kPairN : (h0 + mt) * C::kPairN) + 32 * (h + 2 * (mine - 1) + 1) <=
-                                              C::kAccCols &&
-                                          (!wide_st || !live ||
-                                           (reinterpret_cast<uintptr_t>(crow + t.n0 + 32 * h) & 31u) == 0),
-                                      kSiteCheckEpi)) {
-                    failed = true;
-                    break;
-                }
-                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
-                                       (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
-                uint32_t v0[32], v1[32];
-                if (split) {
-                    // the two halves' partial sums of each block, added in fp32
+            uint32_t v0[32], v1[32];
+            if (split) {
+                // one row tile, its accumulator in the two halves: each block's
+                // two partial sums are added in fp32, then stored
+                const int row0 = t.mt0 * kTileM + 32 * q;  // warp-uniform
+                if (row0 < t.M && mine > 0) {
+                    const int row = row0 + lane;
+                    const bool live = row < t.M;
+                    uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
+                    if (!NVFP4_CHECK_WARP(C::kPairN + 32 * (h + 2 * (mine - 1) + 1) <= C::kAccCols &&
+                                              (!wide_st || !live ||
+                                               (reinterpret_cast<uintptr_t>(crow + t.n0 + 32 * h) & 31u) == 0),
+                                          kSiteCheckEpi))
+                        break;
+                    const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * h);
 #pragma unroll 1
                     for (int j = 0; j < mine; ++j) {
                         tmem_ld_32x32b_x32(tbase + (uint32_t)(64 * j), v0);
@@ -1047,8 +1046,26 @@ struct Roles {
                         }
                         if (live) store_row_block(crow, t.n0 + 32 * (h + 2 * j), N, v0, wide_st, pol_c);
                     }
-                    continue;
                 }
+            } else
+#pragma unroll
+            for (int mt = 0; mt < kRowTilesPerUnit; ++mt) {
+                const int row0 = (t.mt0 + mt) * kTileM + 32 * q;  // warp-uniform
+                if (mt >= t.mtu || row0 >= t.M || mine <= 0) continue;
+                const int row = row0 + lane;
+                const bool live = row < t.M;
+                uint16_t *crow = cbase + (size_t)(live ? row : 0) * (size_t)ldc;
+                // (debug build) the accumulator columns this warp reads, and the
+                // 32-byte alignment of its rows' wide stores
+                if (!NVFP4_CHECK_WARP((h0 + mt) * C::kPairN + 32 * (h + 2 * (mine - 1) + 1) <= C::kAccCols &&
+                                          (!wide_st || !live ||
+                                           (reinterpret_cast<uintptr_t>(crow + t.n0 + 32 * h) & 31u) == 0),
+                                      kSiteCheckEpi)) {
+                    failed = true;
+                    break;
+                }
+                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) +
+                                       (uint32_t)((h0 + mt) * C::kPairN + 32 * h);
                 tmem_ld_32x32b_x32(tbase, v0);
 #pragma unroll 1
                 for (int j = 0; j < mine; j += 2) {
@@ -1081,13 +1098,14 @@ struct Roles {
     }
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ GemmParams p)
 {
     using C = Cfg<MAXN, NB, NA, NS, RAW>;
+    using Walker = nvfp4::Walker<UNIT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Roles<MAXN, NB, NA, NS, RAW> r(smem, p);
+    Roles<MAXN, NB, NA, NS, RAW, UNIT> r(smem, p);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
@@ -1226,28 +1244,31 @@ struct VariantEntry {
     int smem;
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
 constexpr VariantEntry make_entry(bool is_default)
 {
-    return VariantEntry{GemmVariant{MAXN, NB, NA, RAW}, is_default, &ggemm_kernel<MAXN, NB, NA, NS, RAW>,
-                        Cfg<MAXN, NB, NA, NS, RAW>::kSmemBytes};
+    return VariantEntry{GemmVariant{MAXN, NB, NA, RAW, UNIT}, is_default,
+                        &ggemm_kernel<MAXN, NB, NA, NS, RAW, UNIT>, Cfg<MAXN, NB, NA, NS, RAW>::kSmemBytes};
 }
 
-// (MAXN, B stages, A stages, scale stages, raw scales)
+// (MAXN, B stages, A stages, scale stages, raw scales, row tiles per unit):
+// each ring configuration for pairs of row tiles and for single row tiles
 const VariantEntry kVariants[] = {
-    make_entry<256, 3, 3, 2, true>(true),  make_entry<256, 3, 3, 3, false>(true),
-    make_entry<256, 4, 2, 2, true>(false), make_entry<128, 8, 2, 2, true>(true),
-    make_entry<128, 8, 2, 3, false>(true),
+    make_entry<256, 3, 3, 2, true, 2>(true),  make_entry<256, 3, 3, 3, false, 2>(true),
+    make_entry<256, 4, 2, 2, true, 2>(false), make_entry<128, 8, 2, 2, true, 2>(true),
+    make_entry<128, 8, 2, 3, false, 2>(true), make_entry<256, 3, 3, 2, true, 1>(true),
+    make_entry<256, 3, 3, 3, false, 1>(true), make_entry<256, 4, 2, 2, true, 1>(false),
+    make_entry<128, 8, 2, 2, true, 1>(true),  make_entry<128, 8, 2, 3, false, 1>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 }  // namespace
 
-int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw)
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit)
 {
     for (int i = 0; i < kNumVariants; ++i) {
         const GemmVariant &v = kVariants[i].v;
-        if (v.max_n != max_n || v.sf_raw != sf_raw) continue;
+        if (v.max_n != max_n || v.sf_raw != sf_raw || v.unit != unit) continue;
         if (b_stages == 0 && a_stages == 0 && kVariants[i].is_default) return i;
         if (v.b_stages == b_stages && v.a_stages == a_stages) return i;
     }

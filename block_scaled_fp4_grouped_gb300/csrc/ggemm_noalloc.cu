@@ -43,9 +43,9 @@ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 bool aligned16_p(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // First call on a device (that device current): look up the scratch array's
-// device address, raise the kernel's shared-memory limit, fetch the
-// tensor-map encoder.
-nvfp4_status_t setup_device(int dev, int variant)
+// device address, raise the shared-memory limit of the kernels for pairs and
+// for single row tiles, fetch the tensor-map encoder.
+nvfp4_status_t setup_device(int dev, int variant2, int variant1)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_scratch_addr[dev]) return NVFP4_OK;
@@ -54,7 +54,7 @@ nvfp4_status_t setup_device(int dev, int variant)
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (ggemm_configure(variant) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (ggemm_configure(variant2) != cudaSuccess || ggemm_configure(variant1) != cudaSuccess) return NVFP4_ERR_CUDA;
     g_sm_count[dev] = sms;
     g_scratch_addr[dev] = static_cast<uint8_t *>(ptr);
     return NVFP4_OK;
@@ -84,8 +84,9 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
             !aligned16_p(C[g]))
             return NVFP4_ERR_ALIGNMENT;
     }
-    const int variant = ggemm_variant_index(kMaxTileN, 0, 0, true);
-    if (variant < 0) return NVFP4_ERR_CUDA;
+    const int variant2 = ggemm_variant_index(kMaxTileN, 0, 0, true, 2);
+    const int variant1 = ggemm_variant_index(kMaxTileN, 0, 0, true, 1);
+    if (variant2 < 0 || variant1 < 0) return NVFP4_ERR_CUDA;
 
     // --- a call made while `stream` is being captured into a graph is refused
     //     before anything is enqueued: the copy below reads a host buffer
@@ -110,7 +111,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
         return NVFP4_ERR_UNSUPPORTED_DEVICE;
     }
     if (major != 10 || minor != 3) return NVFP4_ERR_UNSUPPORTED_DEVICE;
-    nvfp4_status_t st = setup_device(dev, variant);
+    nvfp4_status_t st = setup_device(dev, variant2, variant1);
     if (st != NVFP4_OK) {
         cudaGetLastError();
         return st;
@@ -181,9 +182,8 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     gp.cap_single = cap_single;
     gp.cap_pair = cap_pair;
     gp.debug_skip_load = 0;
-    gp.unit_tiles = uc.unit;
     gp.split_acc = uc.split ? 1 : 0;
-    if (ggemm_launch(variant, gp, grid, s, false) != cudaSuccess) {
+    if (ggemm_launch(uc.unit == 1 ? variant1 : variant2, gp, grid, s, false) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
     }

@@ -348,7 +348,6 @@ def test_run_host_pinned_buffers_through_the_sms_bitwise():
     buffer and must give the same result."""
     import torch
     from block_scaled_fp4_grouped_gb300 import binding as nb
-    from gpu_util import run_gpu
     parts = [synth.make_problem("custom", seed=960 + g, M=[m], N=n, K=k)
              for g, (m, n, k) in enumerate([(200, 328, 768), (0, 512, 512), (64, 4096, 256), (17, 8, 320)])]
     M = [p.M[0] for p in parts]
@@ -357,9 +356,7 @@ def test_run_host_pinned_buffers_through_the_sms_bitwise():
     pin = lambda arrs: [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in arrs]
     A, B = pin([p.A[0] for p in parts]), pin([p.B[0] for p in parts])
     SFA, SFB = pin([p.SFA[0] for p in parts]), pin([p.SFB[0] for p in parts])
-    dense = []
-    for p in parts:
-        dense += run_gpu(p)
+    dense = _run(parts)  # the same plan shapes on device buffers
     C = [torch.full((m, n), float("nan"), dtype=torch.float16).pin_memory() for m, n in zip(M, N)]
     with nb.GroupedGemm(M, N, K) as gg:
         call = gg.bind_host(A, B, SFA, SFB, C)
