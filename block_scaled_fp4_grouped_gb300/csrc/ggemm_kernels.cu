@@ -38,12 +38,13 @@
 // inside one unit: up to 192 columns when the unit has two row tiles (their
 // accumulators share TMEM) and up to MAXN when it has one. Both row tiles of
 // a pair share every B stage, so each B strip is read from HBM once, by one
-// SM. With single row tiles and one tile of at most 192 columns per CTA
-// (split_acc), the tile adds its even and odd 64-k slices into the two
-// accumulator halves, and the epilogue sums them: an MMA waits for the
-// previous one into the same accumulator, so two chains halve that wait. The host keeps every range inside one pair when it can and picks the
-// smallest per-CTA budget of k-stages that fits the grid, so a CTA streams
-// its B strip in as few passes over K as possible. Block b walks range
+// SM. With single row tiles (the UNIT = 1 instances) and one tile per CTA
+// (split_acc), a tile of at most 192 columns adds its even and odd 64-k
+// slices into the two accumulator halves, and the epilogue sums them: an
+// MMA waits for the previous one into the same accumulator, so two chains
+// halve that wait. The host keeps every range inside one unit when it can
+// and picks the smallest per-CTA budget of k-stages that fits the grid, so a
+// CTA streams its B strip in as few passes over K as possible. Block b walks range
 // order[b]: the host hands the ranges out heaviest first, as blocks with low
 // indices reach their SMs first.
 //
