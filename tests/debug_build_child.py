@@ -38,7 +38,10 @@ def main():
     O = oracle.get()
     problems = [
         ("c0", synth.make_problem("c0", seed=0), {}),
-        ("pairs_ragged", synth.make_problem("custom", seed=71, M=[1, 130, 257, 0, 64], N=328, K=768), {}),
+        ("pairs_ragged", synth.make_problem("custom", seed=71, M=[1, 130, 257, 0, 64], N=328, K=768),
+         {"row_units": 2}),
+        ("single_rows_split", synth.make_problem("custom", seed=76, M=[1, 130, 257, 0, 64], N=328, K=832),
+         {"row_units": 1}),
         ("k_mod_64_relayout", synth.make_problem("custom", seed=72, M=[100, 200], N=256, K=448), {}),
         ("atom_layout", synth.make_problem("custom", seed=73, M=[96, 300], N=512, K=1024), {"sf_layout": "atom"}),
         ("tile_128", synth.make_problem("custom", seed=74, M=[129, 64], N=384, K=512), {"tile_n": 128}),
@@ -48,15 +51,19 @@ def main():
         ref, _ = O.grouped(prob)
         out["parity"][name] = worst_ratio(got, ref)
     prob = synth.make_problem("custom", seed=75, M=[200, 64], N=512, K=1024)
-    for site in range(0x21, 0x27):
-        A, B, SFA, SFB = to_device(prob.A), to_device(prob.B), to_device(prob.SFA), to_device(prob.SFB)
-        C = [torch.zeros((m, prob.N), dtype=torch.float16, device="cuda") for m in prob.M]
-        with nb.GroupedGemm(prob.M, prob.N, prob.K, debug_check_fail=site, wait_timeout_ns=100_000_000) as gg:
-            gg.run(A, B, SFA, SFB, C)
-            st, word = gg.sync_status()
-        got = run_gpu(prob)
-        ref, _ = O.grouped(prob)
-        out["checks"][hex(site)] = {"status": st, "word": word, "after": worst_ratio(got, ref)}
+    ref, _ = O.grouped(prob)
+    for units in (1, 2):  # the kernels for single row tiles (split accumulators) and for pairs
+        for site in range(0x21, 0x27):
+            A, B, SFA, SFB = to_device(prob.A), to_device(prob.B), to_device(prob.SFA), to_device(prob.SFB)
+            C = [torch.zeros((m, prob.N), dtype=torch.float16, device="cuda") for m in prob.M]
+            with nb.GroupedGemm(prob.M, prob.N, prob.K, debug_check_fail=site, wait_timeout_ns=100_000_000,
+                                row_units=units) as gg:
+                info = gg.info()
+                gg.run(A, B, SFA, SFB, C)
+                st, word = gg.sync_status()
+            got = run_gpu(prob, row_units=units)
+            out["checks"][f"{units}/{hex(site)}"] = {"status": st, "word": word, "after": worst_ratio(got, ref),
+                                                     "units": int(info.row_units), "split": int(info.split_acc)}
     print(json.dumps(out))
 
 

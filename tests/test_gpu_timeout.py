@@ -36,13 +36,18 @@ def _inputs(prob):
     return A, B, SFA, SFB, C
 
 
+@pytest.mark.parametrize("row_units", [1, 2])
 @pytest.mark.parametrize("skip", [1, 3])
-def test_a_wait_that_runs_out_is_reported_and_the_context_survives(O, skip):
+def test_a_wait_that_runs_out_is_reported_and_the_context_survives(O, skip, row_units):
+    """Both kernel families: single row tiles with split accumulators (the
+    plan's own choice for this shape) and pairs of row tiles."""
     import torch
     from block_scaled_fp4_grouped_gb300 import binding as nb
     prob = synth.make_problem("custom", seed=41, M=[200, 64, 0, 130], N=512, K=1024)
     A, B, SFA, SFB, C = _inputs(prob)
-    with nb.GroupedGemm(prob.M, prob.N, prob.K, debug_skip_load=skip, wait_timeout_ns=20_000_000) as gg:
+    with nb.GroupedGemm(prob.M, prob.N, prob.K, debug_skip_load=skip, wait_timeout_ns=20_000_000,
+                        row_units=row_units) as gg:
+        assert gg.info().row_units == row_units
         gg.run(A, B, SFA, SFB, C)
         st, word = gg.sync_status()
         assert st == nb.NVFP4_ERR_TIMEOUT, (nb.nvfp4_status_string(st), hex(word))
@@ -54,7 +59,7 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_survives(O, skip):
     torch.cuda.synchronize()
     # the same problem through a plain plan
     A, B, SFA, SFB, C = _inputs(prob)
-    with nb.GroupedGemm(prob.M, prob.N, prob.K) as gg:
+    with nb.GroupedGemm(prob.M, prob.N, prob.K, row_units=row_units) as gg:
         gg.run(A, B, SFA, SFB, C)
         st, word = gg.sync_status()
         assert st == nb.NVFP4_OK, (nb.nvfp4_status_string(st), hex(word))
