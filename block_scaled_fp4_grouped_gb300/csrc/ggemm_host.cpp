@@ -18,7 +18,7 @@ using namespace nvfp4;
 
 namespace {
 
-constexpr int kVersion = 10100;  // 1.1.0: K % 64, batched groups, plan_info.sf_path
+constexpr int kVersion = 10200;  // 1.2.0: row_units, nvfp4_ggemm_schedule_units, plan_info.row_units/split_acc
 constexpr int kMaxGroups = 1024;
 constexpr int32_t kMaxM = 1 << 20;
 constexpr int32_t kMaxN = 1 << 20;
