@@ -289,3 +289,29 @@ def test_automatic_units_rule_on_random_shapes():
 def test_units_entry_rejects_bad_unit_counts(row_units):
     st, cb, units, split = nb.nvfp4_ggemm_schedule_units([64], 256, 0, 152, 256, row_units)
     assert st == nb.NVFP4_ERR_INVALID_ARG
+
+
+def test_units_entry_random_per_group_shapes():
+    """Per-group N_g and K_g, every unit count: the ranges partition the
+    chunks of the units the call reports (ceil(M_g/128/units) units of
+    ceil(N_g/32) chunks per group), and split accumulators only come with
+    single row tiles."""
+    rng = random.Random(2024)
+    for _ in range(150):
+        G = rng.randint(1, 9)
+        M = [rng.choice([0, rng.randint(1, 900)]) for _ in range(G)]
+        N = [8 * rng.randint(1, 600) for _ in range(G)]
+        K = [64 * rng.randint(1, 120) for _ in range(G)]
+        row_units = rng.choice([0, 1, 2])
+        max_ctas = rng.choice([1, 9, 64, 152, 192])
+        st, cb, units, split = nb.nvfp4_ggemm_schedule_units(M, N, rng.choice([0, 128, 256]), max_ctas, K,
+                                                             row_units)
+        assert st == nb.NVFP4_OK
+        assert units in (1, 2) and (row_units == 0 or units == row_units)
+        assert split in (0, 1) and (units == 1 or split == 0)
+        total = sum(-(-(-(-m // 128)) // units) * -(-n // 32) for m, n in zip(M, N))
+        if total == 0:
+            assert cb == [0]
+            continue
+        assert cb[0] == 0 and cb[-1] == total and 1 <= len(cb) - 1 <= max_ctas
+        assert all(b > a for a, b in zip(cb, cb[1:]))
