@@ -489,7 +489,8 @@ def config_summary(q, fp4_peak_tflops, hbm):
             "roofline_fraction_nominal": round(t_nom / us, 3),
             "algorithmic_bytes": q["bytes"], "flops": q["flops"],
             "host_us": {k: round(v, 2) for k, v in q["host"].items()},
-            "grid": q["info"].grid, "chunks": q["info"].chunks, "M": list(q["prob"].M)}
+            "grid": q["info"].grid, "chunks": q["info"].chunks, "M": list(q["prob"].M),
+            "row_units": q["info"].row_units, "split_acc": q["info"].split_acc}
 
 
 def main():
