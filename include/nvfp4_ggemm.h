@@ -359,8 +359,9 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  * (code under a fixed memory budget or its own device allocator, code in a
  * region where an allocation would synchronise the device, plugins that must
  * not grow the process's device footprint). It computes what
- * nvfp4_ggemm_run computes for raw row-major scales, with the same kernel,
- * but needs no plan: the per-group tensor maps and the device error word it
+ * nvfp4_ggemm_run computes for raw row-major scales, with the same kernels
+ * and the units of work a plan with default options would choose, but
+ * needs no plan: the per-group tensor maps and the device error word it
  * needs live in a static device array of under 112 KB that every GPU loading
  * the library holds until the process exits.
  *
