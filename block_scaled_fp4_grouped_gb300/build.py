@@ -29,7 +29,7 @@ LIB = os.path.join(PKG, "libnvfp4_ggemm.so")
 BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libnvfp4_ggemm_debug.so")
 
-SOURCES = ["ggemm_kernels.cu", "ggemm_host.cpp", "ggemm_noalloc.cu", "io_copy.cu"]
+SOURCES = ["ggemm_kernels.cu", "sf_relayout.cu", "ggemm_host.cpp", "ggemm_noalloc.cu", "io_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           f"-I{INCLUDE}", f"-I{CSRC}"]

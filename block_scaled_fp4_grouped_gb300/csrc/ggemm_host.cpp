@@ -73,7 +73,7 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Per-group N and K limits: 16-byte C rows; whole 64-k MMA slices (a last
 // 256-k stage may be partial). Raw scale rows are 16-byte TMA rows only when
-// K % 256 == 0; plans with other K re-lay the scales out first.
+// K % 256 == 0; the kernel copies other raw rows with cp.async.
 inline bool shape_ok(int32_t N, int32_t K)
 {
     return N >= 8 && N <= kMaxN && N % 8 == 0 && K >= 64 && K <= kMaxK && K % 64 == 0;
@@ -398,7 +398,15 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
         ok = encode_2d(&d.maps.tmB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kTileK / 2, kChunkN << i,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return false;
-    if (sf_raw) {
+    d.sf_row_bytes = 0;
+    d.sfa_rows = d.sfb_rows = nullptr;
+    if (sf_raw && !raw_tma_ok(K)) {
+        // rows of K/16 bytes, not whole 16-byte units: no scale maps, the
+        // kernel's scale producer copies the rows with its lanes
+        d.sf_row_bytes = K / 16;
+        d.sfa_rows = static_cast<const uint8_t *>(SFA);
+        d.sfb_rows = static_cast<const uint8_t *>(SFB);
+    } else if (sf_raw) {
         const uint32_t sf_box = kSfKTiles * (kTileK / 16);  // bytes of one scale row per box
         for (int i = 0; i < 2 && ok; ++i)
             ok = encode_2d(&d.maps.tmSFA[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, K / 16, Mg, K / 16, sf_box, kTileM << i,
@@ -433,6 +441,7 @@ struct nvfp4_ggemm_plan_s {
     int cap_single = 8, cap_pair = 6;
     int unit = 2;        // 128-row tiles per unit of work
     bool split = false;  // one-row-tile tiles accumulate in two halves
+    bool sf_lanes = false;  // FUSED path with some K_g % 256 != 0: the scale producer copies those raw rows
     std::vector<int32_t> m_tiles, m_units, chunk_prefix, cta_begin;
     std::vector<GroupShape> shapes;
     std::vector<CtaRange> ctas;
@@ -532,14 +541,14 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         d.m_units = p->m_units[g];
         d.chunk_begin = p->chunk_prefix[g];
         if (p->M[g] == 0) continue;
-        const int N = p->N[g], K = p->K[g], pieces = k_tiles_of(K);
+        const int N = p->N[g], K = p->K[g];
         const void *sfa = SFA[g];
         const void *sfb = SFB ? SFB[g] : nullptr;
         if (p->relayout()) {
             sfa = p->d_ws + p->ws_sfa[g];
             sfb = p->d_ws + p->ws_sfb[g];
             jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFA[g]), p->d_ws + p->ws_sfa[g], p->M[g], K, items, 0};
-            items += ceil_div(p->M[g], 128) * pieces;
+            items += relayout_items_of(p->M[g], K);
             ++njobs;
         }
         if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->unit)) return false;
@@ -551,7 +560,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
             if (p->M[g] == 0) continue;
             const int N = p->N[g], K = p->K[g];
             jobs[njobs] = RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], N, K, items, 0};
-            items += ceil_div(N, 128) * k_tiles_of(K);
+            items += relayout_items_of(N, K);
             ++njobs;
         }
     }
@@ -578,9 +587,8 @@ int relayout_items(nvfp4_ggemm_plan_s *p, bool with_sfb)
     int items = 0;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
-        const int pieces = k_tiles_of(p->K[g]);
-        items += ceil_div(p->M[g], 128) * pieces;
-        if (with_sfb) items += ceil_div(p->N[g], 128) * pieces;
+        items += relayout_items_of(p->M[g], p->K[g]);
+        if (with_sfb) items += relayout_items_of(p->N[g], p->K[g]);
     }
     return items;
 }
@@ -775,19 +783,6 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     nvfp4_ggemm_options_t opt;
     nvfp4_status_t st = validate_options(opt_in, &opt);
     if (st != NVFP4_OK) return st;
-    // Raw scale rows of K_g / 16 bytes are TMA rows only when K_g % 256 == 0;
-    // otherwise the plan re-lays the scales out (its own kernel) and runs the
-    // atom-layout GEMM. Explicit ring depths without an atom-layout kernel
-    // fall back to that kernel's defaults.
-    if (opt.sf_layout == NVFP4_SF_RAW && opt.sf_path == NVFP4_SF_FUSED) {
-        for (int g = 0; g < num_groups; ++g) {
-            if (raw_tma_ok(K[g])) continue;
-            opt.sf_path = NVFP4_SF_RELAYOUT;
-            if (ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, false, 2) < 0)
-                opt.b_stages = opt.a_stages = 0;
-            break;
-        }
-    }
 
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
@@ -813,8 +808,14 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     p->N.assign(N, N + num_groups);
     p->K.assign(K, K + num_groups);
     p->opt = opt;
+    for (int g = 0; g < num_groups; ++g)
+        if (!raw_tma_ok(K[g])) p->sf_lanes = p->fused();
 
-    p->variant = ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused(), 2);
+    // raw scale rows the scale producer's lanes copy: the kernels built for
+    // that (the widest tiles, default ring depths; the tile caps still follow
+    // tile_n)
+    p->variant = p->sf_lanes ? ggemm_variant_index(kMaxTileN, 0, 0, true, 2, true)
+                             : ggemm_variant_index(variant_width(opt.tile_n), opt.b_stages, opt.a_stages, p->fused(), 2);
     if (p->variant < 0) {
         release(p);
         return NVFP4_ERR_INVALID_ARG;
@@ -847,7 +848,8 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
     p->unit = uc.unit;
     p->split = uc.split;
     if (p->unit != 2) {  // the same ring configuration, built for single row tiles
-        p->variant = ggemm_variant_index(p->var.max_n, p->var.b_stages, p->var.a_stages, p->var.sf_raw, p->unit);
+        p->variant =
+            ggemm_variant_index(p->var.max_n, p->var.b_stages, p->var.a_stages, p->var.sf_raw, p->unit, p->var.lanes);
         if (p->variant < 0) {
             release(p);
             return NVFP4_ERR_INVALID_ARG;
@@ -1151,7 +1153,7 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
         if (p->M[g] == 0) continue;
         p->h_prep_jobs[nj++] =
             RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N[g], p->K[g], items, 0};
-        items += ceil_div(p->N[g], 128) * k_tiles_of(p->K[g]);
+        items += relayout_items_of(p->N[g], p->K[g]);
     }
     if (nj > 0) {
         if (cudaMemcpyAsync(p->d_prep_jobs, p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)nj, cudaMemcpyHostToDevice,
@@ -1220,7 +1222,7 @@ nvfp4_status_t nvfp4_sf_relayout(const void *in, void *out, int32_t rows, int32_
     rp.jobs = nullptr;
     rp.single = RelayoutJob{static_cast<const uint8_t *>(in), static_cast<uint8_t *>(out), rows, K, 0, 0};
     rp.njobs = 1;
-    rp.total_items = ceil_div(rows, 128) * k_tiles_of(K);
+    rp.total_items = relayout_items_of(rows, K);
     if (relayout_launch(rp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
@@ -1258,7 +1260,7 @@ const char *nvfp4_status_string(nvfp4_status_t status)
     case NVFP4_ERR_INVALID_ARG: return "invalid argument";
     case NVFP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case NVFP4_ERR_UNSUPPORTED_SHAPE:
-        return "unsupported shape (need K % 64 == 0 (K % 256 == 0 without allocation), N % 8 == 0, sizes in range)";
+        return "unsupported shape (need K % 64 == 0, N % 8 == 0, sizes in range; at most 64 groups without allocation)";
     case NVFP4_ERR_UNSUPPORTED_DEVICE: return "no usable device (needs compute capability 10.3, GB300)";
     case NVFP4_ERR_CUDA: return "CUDA call failed";
     case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";

@@ -112,7 +112,12 @@ struct alignas(128) GroupDesc {
     int32_t n_chunks;     // ceil(N_g / 32)
     int32_t ldc;          // row stride of C_g in elements (>= N_g, a multiple of 8)
     int32_t k_last;       // 64-k slices in the last k tile (1..4; 4 when K_g % 256 == 0)
-    int32_t pad[2];
+    // raw scales whose rows (K_g/16 bytes) are not whole 16-byte units
+    // (K_g % 256 != 0): no scale tensor maps; the scale producer's lanes copy
+    // the rows from these pointers. sf_row_bytes = K_g/16 then, else 0.
+    int32_t sf_row_bytes;
+    const uint8_t *sfa_rows;  // SFA_g [M_g][K_g/16]
+    const uint8_t *sfb_rows;  // SFB_g [N_g][K_g/16]
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
@@ -236,13 +241,19 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
 void order_ctas(uint8_t *order, const CtaRange *ranges, int grid, const int32_t *chunk_prefix, const GroupShape *shapes,
                 int unit, int cap_single, int cap_pair);
 
+// The scale re-layout kernel's unit of work: 128 rows of a matrix by 16
+// 32-bit words of each row (16 atoms, 1024 k).
+constexpr int kRelayoutWords = 16;
+constexpr int kRelayoutThreads = 128;
+inline int relayout_items_of(int rows, int K) { return ((rows + 127) / 128) * ((K / 64 + kRelayoutWords - 1) / kRelayoutWords); }
+
 // One matrix for the scale re-layout kernel.
 struct RelayoutJob {
     const uint8_t *src;  // raw [rows][K/16]
     uint8_t *dst;        // atoms
     int32_t rows;
     int32_t K;           // a multiple of 64
-    int32_t item_begin;  // prefix over jobs of ceil(rows/128) * ceil(K/256)
+    int32_t item_begin;  // prefix over jobs of relayout_items_of(rows, K)
     int32_t pad;
 };
 
@@ -254,18 +265,21 @@ struct RelayoutParams {
 };
 
 // GEMM kernel variants: widest tile, B ring depth, A ring depth, scale path,
-// 128-row tiles per unit of work (each configuration is built for 2 and 1).
+// 128-row tiles per unit of work (each configuration is built for 2 and 1),
+// and whether the scale producer's lanes copy raw scale rows the TMA cannot
+// load (built for the default raw-scale configuration only).
 struct GemmVariant {
     int max_n;
     int b_stages;
     int a_stages;
     bool sf_raw;
     int unit;
+    bool lanes;
 };
 
 // Returns the variant index, or -1. b_stages / a_stages 0 pick the default
-// depths for (max_n, sf_raw, unit).
-int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit);
+// depths for (max_n, sf_raw, unit, lanes).
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit, bool lanes = false);
 GemmVariant ggemm_variant(int index);
 int ggemm_smem_bytes(int index);
 int ggemm_threads();

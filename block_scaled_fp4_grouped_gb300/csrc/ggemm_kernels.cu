@@ -1,5 +1,5 @@
-// Device code: the persistent warp-specialised NVFP4 grouped GEMM and the
-// scale re-layout kernel, for sm_103a.
+// Device code: the persistent warp-specialised NVFP4 grouped GEMM, for
+// sm_103a (the scale re-layout kernel is in sf_relayout.cu).
 //
 // GEMM structure (one CTA per SM, persistent, 16 warps):
 //   warp 0      B producer: per 256-k stage, TMA loads of the tile's B rows
@@ -337,11 +337,6 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint32_t word_at(const uint4 &v, int c)
-{
-    return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
-}
-
 // Orders every later use of v after the preceding tcgen05.wait::ld (the
 // registers of a tcgen05.ld are written asynchronously).
 __device__ __forceinline__ void pin_registers(uint32_t (&v)[32])
@@ -489,7 +484,7 @@ struct MapUse {
     }
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT, bool LANES>
 struct Roles {
     using C = Cfg<MAXN, NB, NA, NS, RAW>;
     using Walker = nvfp4::Walker<UNIT>;
@@ -584,7 +579,7 @@ struct Roles {
         }
         for (int d = 0; d < kDoneRing; ++d) mbar_init(done(d), 1);
         for (int s = 0; s < NS; ++s) {
-            mbar_init(s_full(s), 1);
+            mbar_init(s_full(s), LANES ? 32 : 1);  // 32: a warp-wide scale producer
             mbar_init(s_empty(s), kNumSfWarps);
         }
         for (int b = 0; b < NT; ++b) mbar_init(sf_ready(b), kNumSfWarps);
@@ -778,6 +773,134 @@ struct Roles {
         }
         for (int s = 0; s < NS; ++s)
             if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+    }
+
+    // Bytes [x, x + kSfRow) of `rows` raw scale rows of row_bytes bytes each,
+    // from row row0 of src on, into consecutive kSfRow-byte rows of shared
+    // memory at dst (the layout a TMA box gives), by the warp's 32 lanes:
+    // cp.async pieces of 8 bytes when row_bytes % 8 == 0, else 4. A lane
+    // keeps one piece position of the row and steps through every
+    // (32 / pieces per row)-th row. Pieces past a row's end (64-k slices past
+    // K_g, which are never issued) are not copied, nor are rows past the
+    // matrix (rows counts only rows inside it).
+    template <int PIECE>
+    __device__ __forceinline__ void copy_sf_pieces(uint32_t dst, const uint8_t *src, int row0, int rows,
+                                                   int row_bytes, int x, int lane)
+    {
+        constexpr int P = C::kSfRow / PIECE;  // pieces per row
+        constexpr int R = 32 / P;             // rows per pass of the warp
+        const int c = lane % P;
+        const int off = x + PIECE * c;
+        if (off >= row_bytes) return;
+        int r = lane / P;
+        if (r >= rows) return;
+        const uint8_t *sp = src + (size_t)(row0 + r) * row_bytes + off;
+        uint32_t dp = dst + (uint32_t)(r * C::kSfRow + PIECE * c);
+        const size_t s_step = (size_t)R * row_bytes;
+#pragma unroll 4
+        for (; r < rows; r += R) {
+            if (PIECE == 8) cp_async_8(dp, sp);
+            else cp_async_4(dp, sp);
+            sp += s_step;
+            dp += R * C::kSfRow;
+        }
+    }
+
+    __device__ __forceinline__ void copy_sf_rows(uint32_t dst, const uint8_t *src, int row0, int rows, int row_bytes,
+                                                 int x, int lane)
+    {
+        if (row_bytes % 8 == 0) copy_sf_pieces<8>(dst, src, row0, rows, row_bytes, x, lane);
+        else copy_sf_pieces<4>(dst, src, row0, rows, row_bytes, x, lane);
+    }
+
+    // The scale producer of the raw-scale kernels built for groups whose raw
+    // scale rows are not whole 16-byte units (LANES): the whole warp runs this
+    // loop and the stage barriers count 32 arrivals. For such a group's tiles
+    // every lane copies its share of the stage's rows with cp.async and arms
+    // an arrive that fires once its copies have landed; for the other groups
+    // lane 0 loads by TMA as s_producer does and arrives with the byte count,
+    // and the other lanes arrive at once. (Kernels of their own, so that the
+    // kernels every other plan runs carry none of this code.)
+    __device__ void s_producer_lanes(Walker wk, Unit t, bool have, int lane)
+    {
+        static_assert(RAW && LANES, "raw-scale kernels built with the lane copies only");
+        const uint64_t pol = policy_evict_normal();
+        RingPos r;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        MapUse maps;
+        bool first = true;
+        bool ok = true;
+
+        for (bool more = have; ok && more; more = wk.next(p, t)) {
+            const GroupMaps *gm = maps_of(p, t.g);
+            const int chunks = t.ncols / kChunkN;
+            // raw rows the lanes copy (read once per tile): this group's row
+            // bytes, else 0 (TMA)
+            const GroupDesc *gd = &p.groups[t.g];
+            const int row_bytes = gd->sf_row_bytes;
+            const uint8_t *sfa_rows = gd->sfa_rows;
+            const uint8_t *sfb_rows = gd->sfb_rows;
+            const int a_rows = min(t.mtu * kTileM, t.M - t.mt0 * kTileM);  // rows inside the matrices
+            const int b_rows = min(t.ncols, t.N - t.n0);
+            if (lane == 0 && row_bytes == 0) {
+                maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
+                maps.use_rows(gm, t.g, gm->tmSFB, chunks);
+            }
+            const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;  // scale stages of this tile
+            for (int ks = 0; ks < s_tiles; ++ks) {
+                if (!warp_wait_phase(s_empty(r.stage), r.phase ^ 1u, abort_flag, p, kSiteSEmpty)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = s_full(r.stage);
+                const uint32_t st = s_stage(r.stage);
+                if (!NVFP4_CHECK(st >= sbase + C::kOffSRing && st + C::kSStage <= sbase + C::kOffSRing + NS * C::kSStage &&
+                                     (uint32_t)t.mtu * kTileM * C::kSfRow <= (uint32_t)C::kSfaBytes &&
+                                     (uint32_t)t.ncols * C::kSfRow <= (uint32_t)C::kSfbRegion &&
+                                     ((ks * C::kSfRow) & 15) == 0,
+                                 kSiteCheckLoadSf)) {
+                    ok = false;
+                    break;
+                }
+                // the scales may be written by the previous kernel: on the first
+                // stage, part 0 loads those the caller declared it does not write,
+                // then part 1 waits for it and loads the rest
+                const bool sfa_early = !first || (p.early & kEarlySfa);
+                const bool sfb_early = !first || (p.early & kEarlySfb);
+                const int x = ks * C::kSfRow;  // scale bytes [x, x + kSfRow) of each row
+                if (row_bytes != 0) {
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !(sfa_early && sfb_early)) griddep_wait();
+                        if (part == 0 ? sfa_early : !sfa_early)
+                            copy_sf_rows(st, sfa_rows, t.mt0 * kTileM, a_rows, row_bytes, x, lane);
+                        if (part == 0 ? sfb_early : !sfb_early)
+                            copy_sf_rows(st + C::kSfaBytes, sfb_rows, t.n0, b_rows, row_bytes, x, lane);
+                    }
+                    cp_async_mbar_arrive_noinc(fb);
+                } else if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)(t.mtu * kTileM + t.ncols) * C::kSfRow);
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !(sfa_early && sfb_early)) griddep_wait();
+                        if (part == 0 ? sfa_early : !sfa_early)
+                            tma_load_2d(st, &gm->tmSFA[t.mtu - 1], x, t.mt0 * kTileM, fb, pol);
+                        if (part == 0 ? sfb_early : !sfb_early)
+                            tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
+                    }
+                } else {
+                    mbar_arrive(fb);
+                }
+                if (first) {
+                    first = false;
+                    if (lane == 0) NVFP4_TRACE_AT(kTrSFirst);
+                }
+                issued_mask |= 1u << r.stage;
+                issued_parity = (issued_parity & ~(1u << r.stage)) | (r.phase << r.stage);
+                r.advance<NS>();
+            }
+        }
+        for (int s = 0; s < NS; ++s)
+            if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
+        cp_async_wait_all();  // this thread's copies, whatever became of the stages
     }
 
     // ------------------------------------------------------------ scale writers
@@ -1099,14 +1222,14 @@ struct Roles {
     }
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT, bool LANES>
 __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constant__ GemmParams p)
 {
     using C = Cfg<MAXN, NB, NA, NS, RAW>;
     using Walker = nvfp4::Walker<UNIT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Roles<MAXN, NB, NA, NS, RAW, UNIT> r(smem, p);
+    Roles<MAXN, NB, NA, NS, RAW, UNIT, LANES> r(smem, p);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
@@ -1131,7 +1254,9 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     Walker wk0(p);
     Unit t0{};
     bool have0 = false;
-    if (lane == 0 && (warp == kWarpBProducer || warp == kWarpAProducer || warp == kWarpSProducer))
+    // (every lane of the scale producer's warp when that warp runs as one)
+    if ((lane == 0 && (warp == kWarpBProducer || warp == kWarpAProducer || warp == kWarpSProducer)) ||
+        (LANES && warp == kWarpSProducer))
     {
         have0 = wk0.next(p, t0);
         NVFP4_TRACE_MAX(kTrWalked);
@@ -1159,7 +1284,8 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     } else if (warp == kWarpAProducer) {
         if (lane == 0) r.a_producer(wk0, t0, have0);
     } else if (warp == kWarpSProducer) {
-        if (lane == 0) r.s_producer(wk0, t0, have0);
+        if constexpr (LANES) r.s_producer_lanes(wk0, t0, have0, lane);
+        else if (lane == 0) r.s_producer(wk0, t0, have0);
     } else if (warp == kWarpMma) {
         if (lane == 0) r.mma_issuer(tmem);
     } else if ((warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) || warp >= kWarpEpi1) {
@@ -1177,62 +1303,6 @@ __global__ void __launch_bounds__(kThreads, 1) ggemm_kernel(const __grid_constan
     if (threadIdx.x == 0) NVFP4_TRACE_AT(kTrEnd);
 }
 
-// ------------------------------------------------------------ scale re-layout
-
-// One warp per item = (matrix, 128-row block, 16-byte column piece of the
-// raw rows, i.e. 4 x 64 k). Lane i reads rows i, i+32, i+64, i+96 of the
-// block (16 bytes each) and writes 16 contiguous bytes into each of the four
-// atoms, so every atom is written as one 512-byte coalesced store.
-__global__ void __launch_bounds__(256) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
-{
-    const int lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    for (int item = blockIdx.x * wpb + (threadIdx.x >> 5); item < p.total_items; item += gridDim.x * wpb) {
-        RelayoutJob job;
-        if (p.jobs == nullptr) {
-            job = p.single;
-        } else {
-            int lo = 0, hi = p.njobs;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (p.jobs[mid].item_begin <= item) lo = mid;
-                else hi = mid;
-            }
-            job = p.jobs[lo];
-        }
-        const int pieces = (job.K + 255) / 256;
-        const int katoms = job.K / 64;  // K is a multiple of 64
-        const size_t row_bytes = (size_t)(job.K / 16);
-        const int l = item - job.item_begin;
-        const int rb = l / pieces;
-        const int pc = l % pieces;
-        const int live = min(4, katoms - 4 * pc);  // atoms (4-byte words of a row) in this piece
-        uint4 w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = rb * 128 + 32 * j + lane;
-            const uint8_t *src = job.src + (size_t)r * row_bytes + pc * 16;
-            if (r >= job.rows) {
-                w[j] = make_uint4(0u, 0u, 0u, 0u);
-            } else if (row_bytes % 16 == 0) {
-                w[j] = __ldg(reinterpret_cast<const uint4 *>(src));
-            } else {
-                // rows of K/16 bytes, a multiple of 4: 4-byte aligned words only
-                const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
-                w[j].x = __ldg(s32);
-                w[j].y = live > 1 ? __ldg(s32 + 1) : 0u;
-                w[j].z = live > 2 ? __ldg(s32 + 2) : 0u;
-                w[j].w = live > 3 ? __ldg(s32 + 3) : 0u;
-            }
-        }
-        uint8_t *dst = job.dst + ((size_t)rb * katoms + (size_t)pc * 4) * kSfAtomBytes + 16 * lane;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (c < live)
-                *reinterpret_cast<uint4 *>(dst + c * kSfAtomBytes) =
-                    make_uint4(word_at(w[0], c), word_at(w[1], c), word_at(w[2], c), word_at(w[3], c));
-    }
-}
 
 // ------------------------------------------------------------------- variants
 
@@ -1245,31 +1315,33 @@ struct VariantEntry {
     int smem;
 };
 
-template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT>
+template <int MAXN, int NB, int NA, int NS, bool RAW, int UNIT, bool LANES = false>
 constexpr VariantEntry make_entry(bool is_default)
 {
-    return VariantEntry{GemmVariant{MAXN, NB, NA, RAW, UNIT}, is_default,
-                        &ggemm_kernel<MAXN, NB, NA, NS, RAW, UNIT>, Cfg<MAXN, NB, NA, NS, RAW>::kSmemBytes};
+    return VariantEntry{GemmVariant{MAXN, NB, NA, RAW, UNIT, LANES}, is_default,
+                        &ggemm_kernel<MAXN, NB, NA, NS, RAW, UNIT, LANES>, Cfg<MAXN, NB, NA, NS, RAW>::kSmemBytes};
 }
 
-// (MAXN, B stages, A stages, scale stages, raw scales, row tiles per unit):
-// each ring configuration for pairs of row tiles and for single row tiles
+// (MAXN, B stages, A stages, scale stages, raw scales, row tiles per unit
+// [, lane copies of raw scale rows]): each ring configuration for pairs of
+// row tiles and for single row tiles
 const VariantEntry kVariants[] = {
     make_entry<256, 3, 3, 2, true, 2>(true),  make_entry<256, 3, 3, 3, false, 2>(true),
     make_entry<256, 4, 2, 2, true, 2>(false), make_entry<128, 8, 2, 2, true, 2>(true),
     make_entry<128, 8, 2, 3, false, 2>(true), make_entry<256, 3, 3, 2, true, 1>(true),
     make_entry<256, 3, 3, 3, false, 1>(true), make_entry<256, 4, 2, 2, true, 1>(false),
     make_entry<128, 8, 2, 2, true, 1>(true),  make_entry<128, 8, 2, 3, false, 1>(true),
+    make_entry<256, 3, 3, 2, true, 2, true>(true), make_entry<256, 3, 3, 2, true, 1, true>(true),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 }  // namespace
 
-int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit)
+int ggemm_variant_index(int max_n, int b_stages, int a_stages, bool sf_raw, int unit, bool lanes)
 {
     for (int i = 0; i < kNumVariants; ++i) {
         const GemmVariant &v = kVariants[i].v;
-        if (v.max_n != max_n || v.sf_raw != sf_raw || v.unit != unit) continue;
+        if (v.max_n != max_n || v.sf_raw != sf_raw || v.unit != unit || v.lanes != lanes) continue;
         if (b_stages == 0 && a_stages == 0 && kVariants[i].is_default) return i;
         if (v.b_stages == b_stages && v.a_stages == a_stages) return i;
     }
@@ -1301,17 +1373,6 @@ cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t 
     cfg.attrs = attr;
     cfg.numAttrs = overlap_prev ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kVariants[index].fn, p);
-}
-
-cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream)
-{
-    if (p.total_items <= 0) return cudaSuccess;
-    const int warps_per_block = 8;
-    int blocks = (p.total_items + warps_per_block - 1) / warps_per_block;
-    const int cap = sm_count * 8;
-    if (blocks > cap) blocks = cap;
-    sf_relayout_kernel<<<blocks, warps_per_block * 32, 0, stream>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

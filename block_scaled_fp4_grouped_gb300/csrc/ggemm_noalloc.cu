@@ -42,10 +42,14 @@ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
 bool aligned16_p(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The default raw-scale kernels: pairs of row tiles and single row tiles,
+// each without and with the lane copies of raw scale rows (K % 256 != 0).
+int noalloc_variant(int unit, bool lanes) { return ggemm_variant_index(kMaxTileN, 0, 0, true, unit, lanes); }
+
 // First call on a device (that device current): look up the scratch array's
-// device address, raise the shared-memory limit of the kernels for pairs and
-// for single row tiles, fetch the tensor-map encoder.
-nvfp4_status_t setup_device(int dev, int variant2, int variant1)
+// device address, raise the shared-memory limit of the four kernels, fetch
+// the tensor-map encoder.
+nvfp4_status_t setup_device(int dev)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_scratch_addr[dev]) return NVFP4_OK;
@@ -54,7 +58,9 @@ nvfp4_status_t setup_device(int dev, int variant2, int variant1)
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (ggemm_configure(variant2) != cudaSuccess || ggemm_configure(variant1) != cudaSuccess) return NVFP4_ERR_CUDA;
+    for (int unit = 1; unit <= 2; ++unit)
+        for (int lanes = 0; lanes < 2; ++lanes)
+            if (ggemm_configure(noalloc_variant(unit, lanes != 0)) != cudaSuccess) return NVFP4_ERR_CUDA;
     g_sm_count[dev] = sms;
     g_scratch_addr[dev] = static_cast<uint8_t *>(ptr);
     return NVFP4_OK;
@@ -74,7 +80,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
     // --- arguments (nothing is enqueued before these pass)
     if (num_groups < 1 || !M || !A || !B || !SFA || !SFB || !C) return NVFP4_ERR_INVALID_ARG;
     if (num_groups > kNoAllocMaxGroups) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (N < 8 || N > (1 << 20) || N % 8 != 0 || K < 256 || K > (1 << 18) || K % 256 != 0)
+    if (N < 8 || N > (1 << 20) || N % 8 != 0 || K < 64 || K > (1 << 18) || K % 64 != 0)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     for (int g = 0; g < num_groups; ++g) {
         if (M[g] < 0 || M[g] > (1 << 20)) return NVFP4_ERR_INVALID_ARG;
@@ -84,9 +90,11 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
             !aligned16_p(C[g]))
             return NVFP4_ERR_ALIGNMENT;
     }
-    const int variant2 = ggemm_variant_index(kMaxTileN, 0, 0, true, 2);
-    const int variant1 = ggemm_variant_index(kMaxTileN, 0, 0, true, 1);
-    if (variant2 < 0 || variant1 < 0) return NVFP4_ERR_CUDA;
+    const bool lanes = K % 256 != 0;  // scale rows the TMA cannot load: the scale producer copies them
+    const int variant2 = noalloc_variant(2, lanes);
+    const int variant1 = noalloc_variant(1, lanes);
+    if (variant2 < 0 || variant1 < 0 || noalloc_variant(2, !lanes) < 0 || noalloc_variant(1, !lanes) < 0)
+        return NVFP4_ERR_CUDA;
 
     // --- a call made while `stream` is being captured into a graph is refused
     //     before anything is enqueued: the copy below reads a host buffer
@@ -111,7 +119,7 @@ extern "C" NVFP4_API nvfp4_status_t nvfp4_ggemm_run_noalloc(int num_groups, cons
         return NVFP4_ERR_UNSUPPORTED_DEVICE;
     }
     if (major != 10 || minor != 3) return NVFP4_ERR_UNSUPPORTED_DEVICE;
-    nvfp4_status_t st = setup_device(dev, variant2, variant1);
+    nvfp4_status_t st = setup_device(dev);
     if (st != NVFP4_OK) {
         cudaGetLastError();
         return st;

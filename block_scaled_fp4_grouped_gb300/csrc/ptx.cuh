@@ -65,6 +65,33 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Copies of 4 or 8 bytes from global to shared memory that complete
+// asynchronously (cp.async): for data whose rows are not whole 16-byte
+// units, which the TMA cannot address. Both addresses aligned to the size.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// An arrive on `bar` that fires once every cp.async this thread issued
+// before it has landed. It counts toward the phase (.noinc: the barrier's
+// arrival count must include it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // True once the phase with parity `parity` has completed. Returns false after
 // a hardware-defined time slice when it has not.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)

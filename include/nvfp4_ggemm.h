@@ -34,9 +34,10 @@
  * a group with M_g > 0 non-null and 16-byte aligned (the TMA rule). A group
  * with M_g == 0 is skipped and its pointers are not read. Raw scale rows (K/16 bytes) are rows
  * the TMA can load only when K % 256 == 0 (the rule the TMA helper of
- * submission 498317 enforces on K); a raw-scale plan with some K_g % 256 != 0
- * therefore runs the NVFP4_SF_RELAYOUT path whatever sf_path asks
- * (nvfp4_ggemm_plan_info reports it).
+ * submission 498317 enforces on K); on the NVFP4_SF_FUSED path the kernel's
+ * scale producer copies the rows of a group with K_g % 256 != 0 itself
+ * (cp.async pieces of 8 bytes when K_g % 128 == 0, else 4), so every
+ * K_g % 64 == 0 runs as one kernel on either path the caller picks.
  *
  * Ownership: the caller owns every tensor and the host arrays of pointers;
  * the arrays are read during the call only. A plan owns its device problem
@@ -93,8 +94,7 @@ enum {
 typedef struct {
     uint32_t struct_size;     /* sizeof(nvfp4_ggemm_options_t) */
     int32_t sf_layout;        /* NVFP4_SF_RAW (default) or NVFP4_SF_ATOM */
-    int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only
-                                 (FUSED needs every K_g % 256 == 0, else RELAYOUT is used) */
+    int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only */
     int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
                                  nvfp4_ggemm_prepare_b_scales and run skips it */
     uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
@@ -115,7 +115,10 @@ typedef struct {
                                  defaults (256,3,3), (128,8,2) with atom-layout scales. The
                                  stage counts size the A and B regions for the widest tile;
                                  each CTA cuts them into more slots when its tiles are
-                                 narrower or have one row tile */
+                                 narrower or have one row tile. A raw-scale FUSED plan with
+                                 some K_g % 256 != 0 runs (256,3,3), built with the scale
+                                 producer's row copies, whatever these ask (tile_n still
+                                 caps its tiles) */
     int32_t a_stages;         /* shared-memory stages of the A ring (see b_stages) */
     int32_t serial_launch;    /* 0 (default): a GEMM launch that follows another kernel on its
                                  stream may start its set-up (barriers, TMEM, tensor-map
@@ -342,8 +345,7 @@ typedef struct {
     int32_t sm_count;
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t kernels_per_run; /* kernel launches enqueued by one run */
-    int32_t sf_path;       /* the scale path runs take: NVFP4_SF_FUSED, or NVFP4_SF_RELAYOUT (asked for,
-                              or forced by a raw-scale plan with some K_g % 256 != 0) */
+    int32_t sf_path;       /* the scale path runs take: NVFP4_SF_FUSED or NVFP4_SF_RELAYOUT (as asked) */
     int32_t row_units;     /* 128-row tiles per unit of work: 1 or 2 (see nvfp4_ggemm_options_t) */
     int32_t split_acc;     /* 1: one-row-tile tiles accumulate in two accumulators */
 } nvfp4_ggemm_plan_info_t;
@@ -367,11 +369,11 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status_t status);
  *
  * Arguments: as nvfp4_ggemm_plan + nvfp4_ggemm_run (M host array of G row
  * counts, A/B/SFA/SFB/C host arrays of G device pointers, raw scales), on
- * the current device. Limits: 1 <= num_groups <= 64 and K % 256 == 0
- * (raw scale rows are loaded by the TMA, which needs 16-byte rows; there is
- * no re-layout workspace to fall back on), otherwise
- * NVFP4_ERR_UNSUPPORTED_SHAPE before anything is enqueued; the other checks
- * and status codes are those of plan/run.
+ * the current device. Limits: 1 <= num_groups <= 64, otherwise
+ * NVFP4_ERR_UNSUPPORTED_SHAPE before anything is enqueued; the shape rules,
+ * other checks and status codes are those of plan/run (K % 64 == 0: raw
+ * scale rows that are not 16-byte units are copied by the kernel's scale
+ * producer, as on the plan's FUSED path).
  *
  * The first call on a device looks up the array's device address and
  * configures the kernel; make that first call before any stream capture.

@@ -155,8 +155,8 @@ def test_batched_plan_and_run_argument_checks(L):
     assert nb.nvfp4_ggemm_run_batched(None, [], [], [], [], [], [0] * 5) == nb.NVFP4_ERR_INVALID_ARG
 
 
-def test_noalloc_needs_k_multiple_of_256(L):
-    # raw scale rows are TMA rows only when K % 256 == 0; checked before any device work
-    for K in (320, 192, 64):
+def test_noalloc_needs_k_multiple_of_64(L):
+    # whole 64-k MMA slices, as plan/run; checked before any device work
+    for K in (96, 32, 200, 0, -64):
         st, _ = nb.nvfp4_ggemm_run_noalloc([64], 256, K, [16], [16], [16], [16], [16])
         assert st == nb.NVFP4_ERR_UNSUPPORTED_SHAPE, K

@@ -29,7 +29,7 @@ def _draw(rng, k256):
     G = int(rng.integers(1, 13))
     M = [int(rng.choice([0, 1, rng.integers(1, 129), rng.integers(129, 700)])) for _ in range(G)]
     N = [8 * int(rng.integers(1, 300)) for _ in range(G)]
-    # every third case keeps all K_g % 256 == 0 and takes the fused raw-scale path
+    # every third case keeps all K_g % 256 == 0 (raw scale rows loaded by the TMA)
     K = [int(256 * rng.integers(1, 12) if k256 else rng.choice([256 * rng.integers(1, 12), 64 * rng.integers(1, 48)]))
          for _ in range(G)]
     layout = "raw" if k256 else str(rng.choice(["raw", "atom"]))

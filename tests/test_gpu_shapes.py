@@ -194,16 +194,18 @@ SHAPES_K64 = [  # (M_g, N_g, K_g): most K_g are not multiples of 256
 def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
     """K_g % 64 == 0 with a partial last 256-k tile: A and B past K_g come
     from the TMA's zero fill, the last tile issues only its live 64-k MMA
-    slices and loads only its live scale atoms. A raw-scale plan runs the
-    re-layout path (raw scale rows are not 16-byte TMA rows) and says so."""
+    slices and loads only its live scale atoms. Raw scale rows are not
+    16-byte TMA rows here: on the FUSED path the scale producer's lanes copy
+    them (one kernel), on the RELAYOUT path the re-layout kernel runs first;
+    the plan says which."""
     from block_scaled_fp4_grouped_gb300 import binding as nb
     parts = [synth.make_problem("custom", seed=1000 + g, M=[m], N=n, K=k)
              for g, (m, n, k) in enumerate(SHAPES_K64)]
     with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts],
                         sf_layout=layout, sf_path=path) as gg:
         info = gg.info()
-        assert info.sf_path == (nb.NVFP4_SF_RELAYOUT if layout == "raw" else nb.NVFP4_SF_FUSED)
-        assert info.kernels_per_run == (2 if layout == "raw" else 1)
+        assert info.sf_path == (nb.NVFP4_SF_RELAYOUT if path == "relayout" else nb.NVFP4_SF_FUSED)
+        assert info.kernels_per_run == (2 if path == "relayout" else 1)
     got = _run(parts, sf_layout=layout, sf_path=path, cache_b_scales=cached)
     for g, p in enumerate(parts):
         assert got[g].shape == (p.M[0], p.N)
@@ -214,12 +216,13 @@ def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
         assert_close(got[g], ref, f"group {g} (M={p.M[0]}, N={p.N}, K={p.K})")
 
 
-@pytest.mark.parametrize("layout,path,cached", [("raw", "relayout", False), ("raw", "relayout", True),
-                                                ("atom", "fused", False)])
+@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "relayout", False),
+                                                ("raw", "relayout", True), ("atom", "fused", False)])
 def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached):
     """The K % 64 workload that is timed: the 8-group N = 4096 M list at
     K = 7104 (27 whole 256-k tiles and a last tile of three 64-k slices),
-    through each path a caller can take (raw scales re-laid out every call,
+    through each path a caller can take (raw scale rows copied by the scale
+    producer's lanes, raw scales re-laid out every call,
     with the B scales cached by the plan, and atom-layout scales read by
     3-D tensor-map boxes whose atoms past K are zero-filled); sampled
     entries and the output's tile edges against the oracle."""
@@ -252,9 +255,12 @@ def test_k_multiple_of_64_uniform_and_exact(O):
         assert np.array_equal(got[g].view(np.uint16), ref[g].view(np.uint16)), f"group {g}"
 
 
-def test_k_multiple_of_64_mixed_with_256_bit_exact(O):
-    """One plan whose groups mix K_g % 256 == 0 and K_g % 256 != 0 (so raw
-    scales take the re-layout path for all of them), M_g % 4 != 0 and
+@pytest.mark.parametrize("path", ["fused", "relayout"])
+def test_k_multiple_of_64_mixed_with_256_bit_exact(O, path):
+    """One plan whose groups mix K_g % 256 == 0 and K_g % 256 != 0 (on the
+    FUSED path the scale producer loads the first kind by TMA and copies the
+    second with its lanes, K_g % 128 == 0 in 8-byte pieces and the rest in
+    4-byte ones; on the RELAYOUT path all are re-laid out), M_g % 4 != 0 and
     M_g < 4, with power-of-two scales of span 4 so that every fp32 partial
     sum is exact: the GPU must equal the oracle bit for bit, every row of
     every group."""
@@ -265,9 +271,10 @@ def test_k_multiple_of_64_mixed_with_256_bit_exact(O):
     for p in parts:
         p.SFA[0] = (((rng.integers(-2, 2, p.SFA[0].shape) + 7) << 3)).astype(np.uint8)
         p.SFB[0] = (((rng.integers(-2, 2, p.SFB[0].shape) + 7) << 3)).astype(np.uint8)
-    with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts]) as gg:
-        assert gg.info().sf_path == nb.NVFP4_SF_RELAYOUT and gg.info().kernels_per_run == 2
-    got = _run(parts)
+    with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts], sf_path=path) as gg:
+        want = (nb.NVFP4_SF_RELAYOUT, 2) if path == "relayout" else (nb.NVFP4_SF_FUSED, 1)
+        assert (gg.info().sf_path, gg.info().kernels_per_run) == want
+    got = _run(parts, sf_path=path)
     for g, p in enumerate(parts):
         ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
         assert np.array_equal(got[g].view(np.uint16), ref.view(np.uint16)), f"group {g} {shapes[g]}"
@@ -278,8 +285,8 @@ def test_batched_groups_match_the_oracle(O, layout):
     """nvfp4_ggemm_plan_batched / run_batched: every group is `batch`
     independent problems laid out [batch][rows][cols], one pointer per group
     and a byte stride per operand. C's batches are padded apart; the padding
-    must keep its sentinel. K_g % 256 != 0 in one group (re-layout path for
-    raw scales)."""
+    must keep its sentinel. K_g % 256 != 0 in one group (its raw scale rows
+    copied by the scale producer's lanes)."""
     import torch
     from block_scaled_fp4_grouped_gb300 import binding as nb
     shapes = [(100, 256, 512), (0, 128, 256), (200, 520, 320), (33, 64, 1024)]

@@ -10,9 +10,10 @@ of calls; the checked round changes the first GEMM's inputs with a torch
 kernel and then enqueues both GEMMs with nothing between them, so both
 launches overlap their predecessor. The expected values are the oracle's on
 the bytes read back after the stream has drained. A second test does the same
-for the scale re-layout kernel that K % 256 != 0 puts ahead of the GEMM: it
-must read scales a kernel wrote just before it only after that kernel has
-completed."""
+for raw scales whose rows are not 16-byte units (K % 256 != 0), copied by the
+GEMM's scale producer on the FUSED path and by the re-layout kernel ahead of
+the GEMM on the RELAYOUT path: either must read scales a kernel wrote just
+before it only after that kernel has completed."""
 import numpy as np
 import pytest
 
@@ -92,19 +93,22 @@ def test_second_gemm_reads_what_the_first_wrote(serial, b_static):
         g2.close()
 
 
-@pytest.mark.parametrize("cached", [False, True], ids=["relayout", "relayout_cached_b_scales"])
-def test_relayout_reads_scales_the_previous_kernel_wrote(cached):
-    """K % 256 != 0 runs the scale re-layout kernel ahead of the GEMM, both
-    launched to overlap their predecessor. Here a torch kernel writes the
+@pytest.mark.parametrize("path,cached", [("fused", False), ("relayout", False), ("relayout", True)],
+                         ids=["fused_lanes", "relayout", "relayout_cached_b_scales"])
+def test_relayout_reads_scales_the_previous_kernel_wrote(path, cached):
+    """K % 256 != 0: on the FUSED path the GEMM's scale producer copies the
+    raw scale rows with its lanes; on the RELAYOUT path the re-layout kernel
+    runs ahead of the GEMM. Each kernel is launched to overlap its
+    predecessor. Here a torch kernel writes the
     second GEMM's A scales (from the first GEMM's output, masked to finite
-    E4M3 codes) right before the call, so a re-layout kernel that read its
+    E4M3 codes) right before the call, so a scale copy that read its
     input before that kernel completed would see the previous contents."""
     import torch
     from block_scaled_fp4_grouped_gb300 import binding as nb
     p1 = synth.make_problem("custom", seed=43, M=[256], N=4096, K=7168)
     A1, B1, SFA1, SFB1 = to_device(p1.A), to_device(p1.B), to_device(p1.SFA), to_device(p1.SFB)
     C1 = [torch.zeros((256, 4096), dtype=torch.float16, device="cuda")]
-    K2 = 8128  # K % 256 == 192: the re-layout path
+    K2 = 8128  # K % 256 == 192: raw scale rows of 508 bytes
     p2 = synth.make_problem("custom", seed=44, M=[256], N=512, K=K2)
     c1_bytes = C1[0].view(torch.uint8).reshape(-1)
     A2 = [c1_bytes[: 256 * K2 // 2].view(256, K2 // 2)]
@@ -113,9 +117,12 @@ def test_relayout_reads_scales_the_previous_kernel_wrote(cached):
     B2, SFB2 = to_device(p2.B), to_device(p2.SFB)
     C2 = [torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")]
     g1 = nb.GroupedGemm(p1.M, p1.N, p1.K)
-    g2 = nb.GroupedGemm(p2.M, p2.N, K2, cache_b_scales=cached)
+    g2 = nb.GroupedGemm(p2.M, p2.N, K2, sf_path=path, cache_b_scales=cached)
     try:
-        assert g2.info().sf_path == nb.NVFP4_SF_RELAYOUT and g2.info().kernels_per_run == 2
+        if path == "relayout":
+            assert g2.info().sf_path == nb.NVFP4_SF_RELAYOUT and g2.info().kernels_per_run == 2
+        else:
+            assert g2.info().sf_path == nb.NVFP4_SF_FUSED and g2.info().kernels_per_run == 1
         if cached:
             g2.prepare_b_scales(SFB2)
         call1 = g1.bind(A1, B1, SFA1, SFB1, C1)

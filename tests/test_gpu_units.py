@@ -101,7 +101,7 @@ def test_single_row_units_with_several_tiles_per_cta(O):
         assert_close(got[g], ref[g], f"group {g}")
 
 
-@pytest.mark.parametrize("layout,path", [("raw", "relayout"), ("atom", "fused")])
+@pytest.mark.parametrize("layout,path", [("raw", "fused"), ("raw", "relayout"), ("atom", "fused")])
 def test_split_accumulators_on_the_other_scale_paths(O, layout, path):
     prob = synth.make_problem("custom", seed=60, M=[448, 320], N=3072, K=1088)
     ref, _ = O.grouped(prob)

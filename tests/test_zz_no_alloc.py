@@ -8,8 +8,9 @@ them: it keeps its tensor maps and error word in a static device array
 instead of a plan. Here it is called through the C ABI two times in a row
 on different problems, and each result is compared with the CPU oracle and
 with the plan-based nvfp4_ggemm_run, within the tolerance the other GPU
-tests use; a call of the size of the largest workload (8 groups, K = 7168)
-is checked on sampled entries; the device's free memory must not change
+tests use; two calls with K % 256 != 0 are checked against the oracle; a
+call of the size of the largest workload (8 groups, K = 7168) is checked on
+sampled entries; the device's free memory must not change
 over several calls; and a call made while the stream is being captured into
 a graph must be refused without enqueuing anything. This file is collected
 last so that a run stopping at the first failure has already run every
@@ -62,6 +63,18 @@ def test_noalloc_matches_oracle_and_plan_entry_on_two_calls_in_a_row():
             assert not np.isnan(got[g]).any(), "an output element was never written"
             assert_close(got[g], ref[g], f"{prob.name} group {g} against the oracle")
             assert_close(got[g], want[g], f"{prob.name} group {g} against nvfp4_ggemm_run")
+
+
+@pytest.mark.parametrize("K", [704, 1152])
+def test_noalloc_k_multiple_of_64_against_oracle(K):
+    """K % 256 != 0: scale rows of 44 bytes (copied in 4-byte pieces) and of
+    72 bytes (8-byte pieces), every element against the oracle."""
+    prob = synth.make_problem("custom", seed=33, M=[130, 1, 0, 256, 77], N=200, K=K)
+    got = _run_noalloc(prob)
+    ref, _ = oracle.get().grouped(prob)
+    for g in range(prob.G):
+        assert not np.isnan(got[g]).any(), "an output element was never written"
+        assert_close(got[g], ref[g], f"K={K} group {g}")
 
 
 def test_noalloc_largest_workload_sampled_against_oracle():
