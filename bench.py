@@ -430,7 +430,7 @@ def run_reference(args, world, rank):
     group (they only load the oracle and warm the caches)."""
     if rank != 0:
         return
-    prob = synth.make_problem(args.config, seed=0)
+    prob = headline_problem(args)
     g_small = int(np.argmin([m if m > 0 else 1 << 30 for m in prob.M]))
     for _ in range(args.warmup):
         oracle_time(prob, groups=[g_small])
@@ -455,6 +455,15 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def headline_problem(args):
+    """The timed workload: the config's problem, or with --k its M list and N
+    at another K (values drawn afresh, seed 0)."""
+    prob = synth.make_problem(args.config, seed=0)
+    if args.k:
+        prob = synth.make_problem("custom", seed=0, M=list(prob.M), N=prob.N, K=args.k)
+    return prob
+
+
 def workload_config(name, prob):
     spec = synth.CONFIGS.get(name)
     desc = name
@@ -464,6 +473,8 @@ def workload_config(name, prob):
         else:
             mdesc = f"M_g multiples of {spec.m_step} in [{spec.m_lo},{spec.m_hi}]"
         desc = f"{name}: g={spec.G} N={spec.N} K={spec.K} {mdesc}, seed 0"
+        if prob.K != spec.K:
+            desc = f"{name}'s M list and N (g={spec.G} N={spec.N}) at K={prob.K}, seed 0"
     return {"workload": desc, "M": list(prob.M), "N": prob.N, "K": prob.K,
             "values": "E2M1 codes uniform over 16; E4M3 scales 2^e(1+u), e in [-4,2]",
             "scales": "raw row-major [rows, K/16] E4M3 per call"}
@@ -499,6 +510,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="c4")
+    ap.add_argument("--k", type=int, default=0,
+                    help="time the config's M list and N at another K (a multiple of 64; 0 = the config's K)")
     ap.add_argument("--sf-path", default="fused", choices=["fused", "relayout", "relayout-cached", "atom"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--all-configs", action="store_true",
@@ -536,7 +549,7 @@ def main():
     barrier(world)
     with ClockSampler(local) as clocks:
         r = time_config(args.config, args.sf_path, args.steps, args.warmup, torch=torch, flush=flush,
-                        want_e2e=not args.no_e2e, tuning=tuning)
+                        want_e2e=not args.no_e2e, tuning=tuning, prob=headline_problem(args))
     barrier(world)
     us = max_over_ranks(world, r["us_mean"], device)
     prob = r["prob"]
@@ -578,7 +591,8 @@ def main():
         "roofline_fraction_nominal": t_roof_nominal_us / us,
         "roofline_time_us_nominal": t_roof_nominal_us,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm, "traffic": traffic_for(args.config, args.sf_path),
+                     "frac": achieved_gbs / hbm,
+                     "traffic": traffic_for(args.config, args.sf_path) if not args.k else None,
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_,
                      "kernel": "ggemm_kernel" if args.sf_path != "relayout" else "ggemm_kernel + sf_relayout_kernel"},
         "gpu_launches": r["launches_per_call"] * args.steps,
@@ -596,7 +610,7 @@ def main():
         with ClockSampler(local) as clocks_pc:
             for name in names:
                 for path in paths:
-                    if name == args.config and path == args.sf_path:
+                    if name == args.config and path == args.sf_path and not args.k:
                         q = r
                     else:
                         q = time_config(name, path, args.steps, args.warmup, torch=torch, flush=flush,
@@ -608,16 +622,20 @@ def main():
         # the oracle as it stands, whole problems, all host cores; and c2 on one thread
         by_cfg = {}
         for name in PER_CONFIGS:
-            p = prob if name == args.config else synth.make_problem(name, seed=0)
+            p = prob if name == args.config and not args.k else synth.make_problem(name, seed=0)
             sec, cores = oracle_time(p)
             by_cfg[name] = {"s": round(sec, 3), "threads": cores}
         p2 = synth.make_problem("c2", seed=0)
         sec1, _ = oracle_time(p2, nthreads=1)
         by_cfg["c2_1thread"] = {"s": round(sec1, 3), "threads": 1}
-        line["cpu_baseline"] = {"value": by_cfg[args.config]["s"] * 1e6, "unit": UNIT,
-                                "cores": by_cfg[args.config]["threads"], "kind": "oracle",
+        if args.k:
+            sec, cores = oracle_time(prob)
+            by_cfg[f"{args.config}_k{args.k}"] = {"s": round(sec, 3), "threads": cores}
+        key = f"{args.config}_k{args.k}" if args.k else args.config
+        line["cpu_baseline"] = {"value": by_cfg[key]["s"] * 1e6, "unit": UNIT,
+                                "cores": by_cfg[key]["threads"], "kind": "oracle",
                                 "sample": f"the whole {args.config} problem once (all {len(prob.M)} groups, "
-                                          f"{sum(prob.M)} rows), not scaled"}
+                                          f"{sum(prob.M)} rows, K={prob.K}), not scaled"}
         line["cpu_baseline_by_config"] = by_cfg
     if rank == 0:
         print(json.dumps(line), flush=True)
