@@ -775,42 +775,55 @@ struct Roles {
             if ((issued_mask >> s) & 1u) wait_drain(s_full(s), (issued_parity >> s) & 1u, p, kSiteLoadDrain);
     }
 
-    // Bytes [x, x + kSfRow) of `rows` raw scale rows of row_bytes bytes each,
-    // from row row0 of src on, into consecutive kSfRow-byte rows of shared
-    // memory at dst (the layout a TMA box gives), by the warp's 32 lanes:
-    // cp.async pieces of 8 bytes when row_bytes % 8 == 0, else 4. A lane
-    // keeps one piece position of the row and steps through every
-    // (32 / pieces per row)-th row. Pieces past a row's end (64-k slices past
-    // K_g, which are never issued) are not copied, nor are rows past the
-    // matrix (rows counts only rows inside it).
+    // Bytes [x, x + kSfRow) of rows r_first, r_first + period, ... (< rows)
+    // of raw scale rows of row_bytes bytes each, counted from row row0 of
+    // src, into consecutive kSfRow-byte rows of shared memory at dst (the
+    // layout a TMA box gives), by the warp's 32 lanes in cp.async pieces of
+    // PIECE bytes: a lane keeps one piece position of the row and steps
+    // through the rows. Pieces past a row's end (64-k slices past K_g,
+    // which are never issued) are not copied; every piece copied lies
+    // inside its row.
     template <int PIECE>
-    __device__ __forceinline__ void copy_sf_pieces(uint32_t dst, const uint8_t *src, int row0, int rows,
-                                                   int row_bytes, int x, int lane)
+    __device__ __forceinline__ void copy_sf_pieces(uint32_t dst, const uint8_t *src, int row0, int r_first,
+                                                   int period, int rows, int row_bytes, int x, int lane)
     {
         constexpr int P = C::kSfRow / PIECE;  // pieces per row
         constexpr int R = 32 / P;             // rows per pass of the warp
         const int c = lane % P;
         const int off = x + PIECE * c;
-        if (off >= row_bytes) return;
-        int r = lane / P;
+        if (off + PIECE > row_bytes) return;
+        int r = r_first + period * (lane / P);
         if (r >= rows) return;
+        const int step = period * R;
         const uint8_t *sp = src + (size_t)(row0 + r) * row_bytes + off;
         uint32_t dp = dst + (uint32_t)(r * C::kSfRow + PIECE * c);
-        const size_t s_step = (size_t)R * row_bytes;
+        const size_t s_step = (size_t)step * row_bytes;
 #pragma unroll 4
-        for (; r < rows; r += R) {
-            if (PIECE == 8) cp_async_8(dp, sp);
+        for (; r < rows; r += step) {
+            if (PIECE == 16) cp_async_16(dp, sp);
+            else if (PIECE == 8) cp_async_8(dp, sp);
             else cp_async_4(dp, sp);
             sp += s_step;
-            dp += R * C::kSfRow;
+            dp += step * C::kSfRow;
         }
     }
 
+    // Bytes [x, x + kSfRow) of `rows` raw scale rows (row0 on) of a row
+    // length with row_bytes % 8 == 0 into the stage at dst, rows inside the
+    // matrix only. Row starts (src 16-byte aligned) alternate between 16-byte
+    // and 8-byte alignment, and each of the two classes of rows takes the
+    // widest piece its start allows; a row's last window (past its end) goes
+    // in 4-byte pieces.
     __device__ __forceinline__ void copy_sf_rows(uint32_t dst, const uint8_t *src, int row0, int rows, int row_bytes,
                                                  int x, int lane)
     {
-        if (row_bytes % 8 == 0) copy_sf_pieces<8>(dst, src, row0, rows, row_bytes, x, lane);
-        else copy_sf_pieces<4>(dst, src, row0, rows, row_bytes, x, lane);
+        if (x + C::kSfRow <= row_bytes) {
+            const int r16 = row0 & 1;  // the first row r with (row0 + r) even: 16-byte aligned
+            copy_sf_pieces<16>(dst, src, row0, r16, 2, rows, row_bytes, x, lane);
+            copy_sf_pieces<8>(dst, src, row0, r16 ^ 1, 2, rows, row_bytes, x, lane);
+        } else {
+            copy_sf_pieces<4>(dst, src, row0, 0, 1, rows, row_bytes, x, lane);
+        }
     }
 
     // The scale producer of the raw-scale kernels built for groups whose raw
@@ -868,13 +881,30 @@ struct Roles {
                 const bool sfa_early = !first || (p.early & kEarlySfa);
                 const bool sfb_early = !first || (p.early & kEarlySfb);
                 const int x = ks * C::kSfRow;  // scale bytes [x, x + kSfRow) of each row
-                if (row_bytes != 0) {
+                // Rows whose length is 4 mod 8 bytes go in 4-byte pieces (16- and
+                // 8-byte pieces for the rows that allow them were slower there);
+                // rows of 8-byte multiples in 16- and 8-byte pieces, from a
+                // single copy of that code (four inlined copies were slower)
+                if (row_bytes % 8 != 0) {
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1 && !(sfa_early && sfb_early)) griddep_wait();
                         if (part == 0 ? sfa_early : !sfa_early)
-                            copy_sf_rows(st, sfa_rows, t.mt0 * kTileM, a_rows, row_bytes, x, lane);
+                            copy_sf_pieces<4>(st, sfa_rows, t.mt0 * kTileM, 0, 1, a_rows, row_bytes, x, lane);
                         if (part == 0 ? sfb_early : !sfb_early)
-                            copy_sf_rows(st + C::kSfaBytes, sfb_rows, t.n0, b_rows, row_bytes, x, lane);
+                            copy_sf_pieces<4>(st + C::kSfaBytes, sfb_rows, t.n0, 0, 1, b_rows, row_bytes, x, lane);
+                    }
+                    cp_async_mbar_arrive_noinc(fb);
+                } else if (row_bytes != 0) {
+                    // (part, operand) = (i / 2, i % 2): SFA then SFB, those loaded
+                    // early first
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i) {
+                        const bool sfb = (i & 1) != 0;
+                        const bool early = sfb ? sfb_early : sfa_early;
+                        if (i == 2 && !(sfa_early && sfb_early)) griddep_wait();
+                        if (i < 2 ? early : !early)
+                            copy_sf_rows(sfb ? st + C::kSfaBytes : st, sfb ? sfb_rows : sfa_rows,
+                                         sfb ? t.n0 : t.mt0 * kTileM, sfb ? b_rows : a_rows, row_bytes, x, lane);
                     }
                     cp_async_mbar_arrive_noinc(fb);
                 } else if (lane == 0) {

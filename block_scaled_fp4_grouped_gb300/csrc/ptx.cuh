@@ -65,7 +65,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Copies of 4 or 8 bytes from global to shared memory that complete
+// Copies of 4, 8 or 16 bytes from global to shared memory that complete
 // asynchronously (cp.async): for data whose rows are not whole 16-byte
 // units, which the TMA cannot address. Both addresses aligned to the size.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
@@ -76,6 +76,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
 __device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // Waits until every cp.async this thread issued has landed.

@@ -238,6 +238,30 @@ def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached):
         assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
 
 
+@pytest.mark.parametrize("opts", [dict(tile_n=128), dict(tile_n=64), dict(b_stages=4, a_stages=2),
+                                  dict(row_units=1), dict(max_ctas=7)],
+                         ids=["tile128", "tile64", "stages4x2", "single_rows", "grid7"])
+def test_k_multiple_of_64_fused_with_other_options(O, opts):
+    """A raw-scale FUSED plan with K % 256 != 0 runs the kernels whose scale
+    producer copies the raw rows: the widest-tile kernel with its default
+    ring depths, whatever tile width or depths the options ask for (the tile
+    width still caps the tiles). Every option must still give the oracle's
+    result, and the plan must say which kernel configuration it runs."""
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import run_gpu
+    prob = synth.make_problem("custom", seed=1300, M=[300, 64, 129, 17], N=520, K=1216)
+    with nb.GroupedGemm(prob.M, prob.N, prob.K, **opts) as gg:
+        info = gg.info()
+        assert (info.sf_path, info.kernels_per_run) == (nb.NVFP4_SF_FUSED, 1)
+        assert (info.b_stages, info.a_stages) == (3, 3)
+        assert info.tile_n == opts.get("tile_n", 256)
+    ref, _ = O.grouped(prob)
+    got = run_gpu(prob, **opts)
+    for g in range(prob.G):
+        assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
+        assert_close(got[g], ref[g], f"{opts} group {g}")
+
+
 def test_k_multiple_of_64_uniform_and_exact(O):
     """One K for every group (nvfp4_ggemm_plan), K = 704 = 2 x 256 + 192,
     with power-of-two scales of span 4 so that every fp32 partial sum is
