@@ -216,40 +216,45 @@ def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
         assert_close(got[g], ref, f"group {g} (M={p.M[0]}, N={p.N}, K={p.K})")
 
 
-@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "relayout", False),
-                                                ("raw", "relayout", True), ("atom", "fused", False)])
-def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached):
+@pytest.mark.parametrize("layout,path,cached,K", [("raw", "fused", False, 7104), ("raw", "fused", False, 7040),
+                                                  ("raw", "relayout", False, 7104), ("raw", "relayout", True, 7104),
+                                                  ("atom", "fused", False, 7104)])
+def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached, K):
     """The K % 64 workload that is timed: the 8-group N = 4096 M list at
     K = 7104 (27 whole 256-k tiles and a last tile of three 64-k slices),
     through each path a caller can take (raw scale rows copied by the scale
     producer's lanes, raw scales re-laid out every call,
     with the B scales cached by the plan, and atom-layout scales read by
     3-D tensor-map boxes whose atoms past K are zero-filled); sampled
-    entries and the output's tile edges against the oracle."""
+    entries and the output's tile edges against the oracle. K = 7040 (rows
+    of 440 bytes) takes the FUSED path's 16- and 8-byte row classes."""
     from gpu_util import run_gpu, sample_indices
     M = synth.make_problem("c4", seed=0).M
-    prob = synth.make_problem("custom", seed=1200, M=M, N=4096, K=7104)
+    prob = synth.make_problem("custom", seed=1200, M=M, N=4096, K=K)
     got = run_gpu(prob, sf_layout=layout, sf_path=path, cache_b_scales=cached)
     rng = np.random.default_rng(1200)
     for g in range(prob.G):
         rows, cols = sample_indices(prob.M[g], prob.N, 400, rng)
         ref16, _ = O.group_entries(prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], prob.K, rows, cols)
-        assert_close(got[g][rows, cols], ref16, f"K=7104 {layout}/{path} group {g}")
+        assert_close(got[g][rows, cols], ref16, f"K={K} {layout}/{path} group {g}")
         assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
 
 
+@pytest.mark.parametrize("K", [1216, 1152], ids=["rows_4mod8", "rows_8mod16"])
 @pytest.mark.parametrize("opts", [dict(tile_n=128), dict(tile_n=64), dict(b_stages=4, a_stages=2),
                                   dict(row_units=1), dict(max_ctas=7)],
                          ids=["tile128", "tile64", "stages4x2", "single_rows", "grid7"])
-def test_k_multiple_of_64_fused_with_other_options(O, opts):
+def test_k_multiple_of_64_fused_with_other_options(O, opts, K):
     """A raw-scale FUSED plan with K % 256 != 0 runs the kernels whose scale
     producer copies the raw rows: the widest-tile kernel with its default
     ring depths, whatever tile width or depths the options ask for (the tile
-    width still caps the tiles). Every option must still give the oracle's
-    result, and the plan must say which kernel configuration it runs."""
+    width still caps the tiles). Scale rows of 76 bytes go in 4-byte
+    pieces, rows of 72 bytes in 16- and 8-byte pieces by row class. Every
+    option must still give the oracle's result, and the plan must say which
+    kernel configuration it runs."""
     from block_scaled_fp4_grouped_gb300 import binding as nb
     from gpu_util import run_gpu
-    prob = synth.make_problem("custom", seed=1300, M=[300, 64, 129, 17], N=520, K=1216)
+    prob = synth.make_problem("custom", seed=1300, M=[300, 64, 129, 17], N=520, K=K)
     with nb.GroupedGemm(prob.M, prob.N, prob.K, **opts) as gg:
         info = gg.info()
         assert (info.sf_path, info.kernels_per_run) == (nb.NVFP4_SF_FUSED, 1)
