@@ -870,7 +870,10 @@ struct Roles {
                 if (!NVFP4_CHECK(st >= sbase + C::kOffSRing && st + C::kSStage <= sbase + C::kOffSRing + NS * C::kSStage &&
                                      (uint32_t)t.mtu * kTileM * C::kSfRow <= (uint32_t)C::kSfaBytes &&
                                      (uint32_t)t.ncols * C::kSfRow <= (uint32_t)C::kSfbRegion &&
-                                     ((ks * C::kSfRow) & 15) == 0,
+                                     ((ks * C::kSfRow) & 15) == 0 &&
+                                     (row_bytes == 0 || (row_bytes % 4 == 0 &&
+                                                         ((reinterpret_cast<uintptr_t>(sfa_rows) |
+                                                           reinterpret_cast<uintptr_t>(sfb_rows)) & 15u) == 0)),
                                  kSiteCheckLoadSf)) {
                     ok = false;
                     break;

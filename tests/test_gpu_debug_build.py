@@ -6,9 +6,12 @@ and alignment before the operation it guards; a failed check records
 the kernel through its abort flag. A child process loads that build
 (NVFP4_GGEMM_LIB) and (a) runs problems covering pairs of row tiles,
 single row tiles with split accumulators, ragged and empty groups, K % 64
-(the re-layout path), atom-layout scales and the 128-column kernel, which
-must match the oracle with no check firing; (b) for each check site and for
-the kernels of both unit counts, forces that check to fail through the
+(raw scale rows copied by the scale producer's lanes, in 4-byte pieces and
+in 16- and 8-byte row classes, and the re-layout path), atom-layout scales
+and the 128-column kernel, which must match the oracle with no check
+firing; (b) for each check site, for the kernels of both unit counts and
+for raw scale rows loaded by TMA and copied by lanes, forces that check to
+fail through the
 test-only option debug_check_fail (no invalid operation is issued: the
 check's own skip path runs), which must come back as NVFP4_ERR_DEVICE_FAULT
 naming that site, after which a good call on the same context matches the
@@ -43,11 +46,12 @@ def test_debug_build_matches_the_oracle_with_no_check_firing(child_result):
         assert worst <= 1.0, (name, worst)
 
 
+@pytest.mark.parametrize("kind", ["tma", "lanes"])
 @pytest.mark.parametrize("units", [1, 2])
 @pytest.mark.parametrize("site", range(0x21, 0x27), ids=lambda s: hex(s))
-def test_a_failed_check_is_reported_with_its_site(child_result, site, units):
+def test_a_failed_check_is_reported_with_its_site(child_result, site, units, kind):
     from block_scaled_fp4_grouped_gb300 import binding as nb
-    r = child_result["checks"][f"{units}/{hex(site)}"]
+    r = child_result["checks"][f"{kind}/{units}/{hex(site)}"]
     assert r["units"] == units and r["split"] == (1 if units == 1 else 0), r
     assert r["status"] == nb.NVFP4_ERR_DEVICE_FAULT, r
     assert r["word"] & 0xFF == nb.NVFP4_ERR_DEVICE_FAULT, hex(r["word"])
