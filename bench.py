@@ -424,10 +424,15 @@ def oracle_time(prob, nthreads: int = 0, groups=None):
     return time.perf_counter() - t0, threads
 
 
+REFERENCE_BUDGET_S = 150.0  # wall time the reference arm's measured steps may take
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm (rank 0 only): every timed step is
     the whole problem of the workload; the warm-up steps run its smallest
-    group (they only load the oracle and warm the caches)."""
+    group (they only load the oracle and warm the caches). Steps stop early
+    when the next one would take the measured steps past REFERENCE_BUDGET_S
+    (the line says how many were measured); a step is never a sample."""
     if rank != 0:
         return
     prob = headline_problem(args)
@@ -437,12 +442,18 @@ def run_reference(args, world, rank):
     per_step, cores = [], os.cpu_count() or 1
     t_all = time.perf_counter()
     for _ in range(args.steps):
+        if per_step and time.perf_counter() - t_all + statistics.fmean(per_step) * 1e-6 > REFERENCE_BUDGET_S:
+            break
         sec, cores = oracle_time(prob)
         per_step.append(sec * 1e6)
     wall = time.perf_counter() - t_all
     value = statistics.fmean(per_step)
+    measured = len(per_step)
     sample = (f"the whole {args.config} problem every step ({len(prob.M)} groups, {sum(prob.M)} rows x "
-              f"N={prob.N} x K={prob.K}), {args.steps} steps in {wall:.1f} s; warm-up steps: group {g_small} only")
+              f"N={prob.N} x K={prob.K}), {measured} steps in {wall:.1f} s; warm-up steps: group {g_small} only")
+    if measured < args.steps:
+        sample += (f"; {measured} of the {args.steps} steps asked were measured, the next would have taken the "
+                   f"run past {REFERENCE_BUDGET_S:.0f} s")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
@@ -450,6 +461,7 @@ def run_reference(args, world, rank):
         "config": workload_config(args.config, prob),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "steps_measured": measured,
         "timed_wall_s": wall,
     }
     print(json.dumps(line), flush=True)

@@ -11,12 +11,19 @@ CMD = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "-
        "--config", "c0"]
 
 
-def _run(env_extra):
+def _run(env_extra, extra=(), budget=None):
     env = dict(os.environ, **env_extra)
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         if k not in env_extra:
             env.pop(k, None)
-    return subprocess.run(CMD, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    cmd = CMD + list(extra)
+    if budget is not None:  # the same program with a smaller budget for its measured steps
+        cmd = [sys.executable, "-c",
+               "import runpy, sys; sys.argv = ['bench.py'] + sys.argv[1:]; "
+               "g = runpy.run_path('bench.py', run_name='bench_lib'); "
+               f"g['run_reference'].__globals__['REFERENCE_BUDGET_S'] = {budget}; "
+               "g['main']()"] + CMD[2:] + list(extra)
+    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
 
 
 def test_reference_arm_prints_one_contract_line():
@@ -37,7 +44,18 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"].startswith("c0")
     # every timed step is the whole problem, and the steps fit in the run's own wall time
     assert "whole" in d["cpu_baseline"]["sample"]
-    assert d["timed_wall_s"] >= 0.99 * d["steps"] * d["value"] * 1e-6
+    assert d["steps_measured"] == 3
+    assert d["timed_wall_s"] >= 0.99 * d["steps_measured"] * d["value"] * 1e-6
+
+
+def test_reference_arm_stops_at_its_budget():
+    """Whole-problem steps that would run past the budget are not taken, and
+    the line says how many were measured."""
+    res = _run({}, extra=["--steps", "1000"], budget="0.05")
+    assert res.returncode == 0, res.stderr
+    d = json.loads([l for l in res.stdout.splitlines() if l.startswith("{")][0])
+    assert d["steps"] == 1000 and 1 <= d["steps_measured"] < 1000
+    assert f"{d['steps_measured']} of the 1000 steps asked were measured" in d["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_other_ranks_exit_quietly():
