@@ -85,8 +85,10 @@ enum { NVFP4_SF_RAW = 0, NVFP4_SF_ATOM = 1 };
 
 /* How raw scales reach the tensor cores. */
 enum {
-    NVFP4_SF_FUSED = 0,   /* one kernel: raw 128x16-byte scale tiles are loaded by TMA and
-                             permuted into the atom layout in shared memory */
+    NVFP4_SF_FUSED = 0,   /* one kernel: the raw scale rows of each stage are loaded into shared
+                             memory (by TMA when K_g % 256 == 0, else copied by the scale
+                             producer's lanes) and permuted into the atom layout on their way
+                             to the tensor memory */
     NVFP4_SF_RELAYOUT = 1 /* the re-layout kernel writes atom-layout copies into the plan's
                              workspace, then the GEMM kernel reads those */
 };
