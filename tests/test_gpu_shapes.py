@@ -240,6 +240,22 @@ def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached, K):
         assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
 
 
+@pytest.mark.parametrize("K", [7104, 7040])
+def test_k_multiple_of_64_fused_largest_m_list_every_element(O, K):
+    """The FUSED path with lane-copied raw scale rows on the largest M list
+    at K = 7104 (4-byte pieces) and K = 7040 (16- and 8-byte row classes):
+    every element against the oracle, which does the whole problem in
+    seconds on the host cores."""
+    from gpu_util import run_gpu
+    M = synth.make_problem("c4", seed=0).M
+    prob = synth.make_problem("custom", seed=1400, M=M, N=4096, K=K)
+    got = run_gpu(prob)
+    ref, _ = O.grouped(prob)
+    for g in range(prob.G):
+        assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
+        assert_close(got[g], ref[g], f"K={K} group {g}")
+
+
 @pytest.mark.parametrize("K", [1216, 1152], ids=["rows_4mod8", "rows_8mod16"])
 @pytest.mark.parametrize("opts", [dict(tile_n=128), dict(tile_n=64), dict(b_stages=4, a_stages=2),
                                   dict(row_units=1), dict(max_ctas=7)],
