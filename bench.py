@@ -194,6 +194,8 @@ def _flavour(sf_path: str):
         kw = dict(sf_layout="raw", sf_path="relayout")
     elif sf_path == "relayout-cached":
         kw = dict(sf_layout="raw", sf_path="relayout", cache_b_scales=True)
+    elif sf_path == "fused-cached":
+        kw = dict(sf_layout="raw", sf_path="fused", cache_b_scales=True)
     elif sf_path == "atom":
         kw = dict(sf_layout="atom", sf_path="fused")
     return kw
@@ -524,7 +526,7 @@ def main():
     ap.add_argument("--config", default="c4")
     ap.add_argument("--k", type=int, default=0,
                     help="time the config's M list and N at another K (a multiple of 64; 0 = the config's K)")
-    ap.add_argument("--sf-path", default="fused", choices=["fused", "relayout", "relayout-cached", "atom"])
+    ap.add_argument("--sf-path", default="fused", choices=["fused", "fused-cached", "relayout", "relayout-cached", "atom"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--all-configs", action="store_true",
                     help="also time the pages' M lists and the re-layout paths (extra key)")
@@ -606,7 +608,8 @@ def main():
                      "frac": achieved_gbs / hbm,
                      "traffic": traffic_for(args.config, args.sf_path) if not args.k else None,
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": bytes_,
-                     "kernel": "ggemm_kernel" if args.sf_path != "relayout" else "ggemm_kernel + sf_relayout_kernel"},
+                     "kernel": ("ggemm_kernel + sf_relayout_kernel" if args.sf_path.startswith("relayout")
+                                    else "ggemm_kernel")},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": clocks.summary(),
         "timed_wall_s": r["timed_wall_s"],

@@ -376,7 +376,7 @@ void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_
 }
 
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw, int unit)
+                     const void *SFB, void *C, bool sf_raw, int unit, bool sfb_padded)
 {
     if (!load_encode()) return false;
     const uint64_t Mg = (uint64_t)M;
@@ -399,13 +399,23 @@ bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const voi
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return false;
     d.sf_row_bytes = 0;
+    d.sfb_tma = 0;
     d.sfa_rows = d.sfb_rows = nullptr;
     if (sf_raw && !raw_tma_ok(K)) {
-        // rows of K/16 bytes, not whole 16-byte units: no scale maps, the
-        // kernel's scale producer copies the rows with its lanes
+        // rows of K/16 bytes, not whole 16-byte units: no SFA maps, the
+        // kernel's scale producer copies the rows with its lanes; SFB too,
+        // unless it is a copy with padded rows, which the TMA loads
         d.sf_row_bytes = K / 16;
         d.sfa_rows = static_cast<const uint8_t *>(SFA);
-        d.sfb_rows = static_cast<const uint8_t *>(SFB);
+        if (sfb_padded) {
+            const uint32_t sf_box = kSfKTiles * (kTileK / 16);
+            d.sfb_tma = 1;
+            for (int i = 0; i < kNumRowBoxes && ok; ++i)
+                ok = encode_2d(&d.maps.tmSFB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, K / 16, N,
+                               (uint64_t)sf_padded_row_bytes(K), sf_box, kChunkN << i, CU_TENSOR_MAP_SWIZZLE_NONE);
+        } else {
+            d.sfb_rows = static_cast<const uint8_t *>(SFB);
+        }
     } else if (sf_raw) {
         const uint32_t sf_box = kSfKTiles * (kTileK / 16);  // bytes of one scale row per box
         for (int i = 0; i < 2 && ok; ++i)
@@ -471,6 +481,9 @@ struct nvfp4_ggemm_plan_s {
     bool raw() const { return opt.sf_layout == NVFP4_SF_RAW; }
     bool relayout() const { return raw() && opt.sf_path == NVFP4_SF_RELAYOUT; }
     bool fused() const { return raw() && opt.sf_path == NVFP4_SF_FUSED; }
+    // FUSED with cache_b_scales: SFB is copied once (prepare_b_scales) into
+    // rows padded to 16 bytes, which the TMA loads whatever K_g is
+    bool sfb_padded() const { return fused() && opt.cache_b_scales; }
 };
 
 namespace {
@@ -544,6 +557,8 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
         const int N = p->N[g], K = p->K[g];
         const void *sfa = SFA[g];
         const void *sfb = SFB ? SFB[g] : nullptr;
+        const bool pad = p->sfb_padded() && !force_sfb;
+        if (pad) sfb = p->d_ws + p->ws_sfb[g];
         if (p->relayout()) {
             sfa = p->d_ws + p->ws_sfa[g];
             sfb = p->d_ws + p->ws_sfb[g];
@@ -551,7 +566,7 @@ bool fill_table(nvfp4_ggemm_plan_s *p, uint8_t *tab, uint8_t *dtab, const void *
             items += relayout_items_of(p->M[g], K);
             ++njobs;
         }
-        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->unit)) return false;
+        if (!fill_group_desc(d, p->M[g], N, K, A[g], B[g], sfa, sfb, C[g], p->fused(), p->unit, pad)) return false;
         d.chunk_begin = p->chunk_prefix[g];
         if (ldc) d.ldc = ldc[g];
     }
@@ -611,7 +626,7 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
                           const void *const *SFA, const void *const *SFB, void *const *C, const int32_t *ldc,
                           cudaStream_t stream, bool force_sfb, bool early_ok = true)
 {
-    const bool sfb_cached = p->relayout() && p->opt.cache_b_scales && !force_sfb;
+    const bool sfb_cached = (p->relayout() || p->sfb_padded()) && p->opt.cache_b_scales && !force_sfb;
     if (sfb_cached && !p->b_prepared) return NVFP4_ERR_NOT_PREPARED;
     nvfp4_status_t st = check_group_ptrs(p, A, B, SFA, SFB, C, !sfb_cached);
     if (st != NVFP4_OK) return st;
@@ -686,7 +701,9 @@ nvfp4_status_t run_device(nvfp4_ggemm_plan_s *p, const void *const *A, const voi
     // and nothing behind run_host's own copy of the inputs.
     gp.early = 0;
     if (early_ok && p->opt.b_static) {
-        gp.early = kEarlyB | (p->relayout() ? 0 : kEarlySfb);
+        // (the plan's own copies of the scales are written by this
+        // library's kernels, so those are never loaded early)
+        gp.early = kEarlyB | (p->relayout() || sfb_cached ? 0 : kEarlySfb);
         if (p->opt.b_static == 2) gp.early |= kEarlyA | (p->relayout() ? 0 : kEarlySfa);
     }
 #ifdef NVFP4_TRACE
@@ -891,17 +908,21 @@ nvfp4_status_t nvfp4_ggemm_plan_shapes(nvfp4_ggemm_plan_t *out, int device, int 
              cudaMalloc(&s.d_table, p->table_bytes) == cudaSuccess &&
              cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming) == cudaSuccess;
     }
-    if (ok && p->relayout()) {
+    if (ok && (p->relayout() || p->sfb_padded())) {
+        // RELAYOUT: atom-layout SFA and SFB; FUSED with cache_b_scales: SFB
+        // with rows padded to 16 bytes
         size_t off = 0;
         p->ws_sfa.assign(num_groups, 0);
         p->ws_sfb.assign(num_groups, 0);
-        for (int g = 0; g < num_groups; ++g) {
+        for (int g = 0; g < num_groups && p->relayout(); ++g) {
             p->ws_sfa[g] = off;
             off = align_up(off + atom_bytes(M[g], K[g]), 256);
         }
         for (int g = 0; g < num_groups; ++g) {
             p->ws_sfb[g] = off;
-            off = align_up(off + atom_bytes(N[g], K[g]), 256);
+            off = align_up(off + (p->relayout() ? atom_bytes(N[g], K[g])
+                                                : (uint64_t)N[g] * (uint64_t)sf_padded_row_bytes(K[g])),
+                           256);
         }
         ok = cudaMalloc(&p->d_ws, std::max<size_t>(off, 256)) == cudaSuccess &&
              cudaMalloc(&p->d_prep_jobs, sizeof(RelayoutJob) * (size_t)num_groups) == cudaSuccess &&
@@ -1138,7 +1159,7 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
 {
     if (!plan || !SFB) return NVFP4_ERR_INVALID_ARG;
     nvfp4_ggemm_plan_s *p = plan;
-    if (!p->relayout() || !p->opt.cache_b_scales) return NVFP4_ERR_INVALID_ARG;
+    if (!(p->relayout() || p->sfb_padded()) || !p->opt.cache_b_scales) return NVFP4_ERR_INVALID_ARG;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
         if (!SFB[g]) return NVFP4_ERR_INVALID_ARG;
@@ -1148,12 +1169,14 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
     if (!guard.ok) return NVFP4_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->prep_used && cudaEventSynchronize(p->ev_prep) != cudaSuccess) return NVFP4_ERR_CUDA;
+    // RELAYOUT: atom layout (items of 128 rows x 16 atoms); FUSED: padded
+    // rows (one item per row)
     int nj = 0, items = 0;
     for (int g = 0; g < p->G; ++g) {
         if (p->M[g] == 0) continue;
         p->h_prep_jobs[nj++] =
             RelayoutJob{static_cast<const uint8_t *>(SFB[g]), p->d_ws + p->ws_sfb[g], p->N[g], p->K[g], items, 0};
-        items += relayout_items_of(p->N[g], p->K[g]);
+        items += p->relayout() ? relayout_items_of(p->N[g], p->K[g]) : p->N[g];
     }
     if (nj > 0) {
         if (cudaMemcpyAsync(p->d_prep_jobs, p->h_prep_jobs, sizeof(RelayoutJob) * (size_t)nj, cudaMemcpyHostToDevice,
@@ -1163,7 +1186,7 @@ nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void 
         rp.jobs = p->d_prep_jobs;
         rp.njobs = nj;
         rp.total_items = items;
-        if (relayout_launch(rp, p->sm_count, s) != cudaSuccess) {
+        if ((p->relayout() ? relayout_launch(rp, p->sm_count, s) : sf_pad_launch(rp, p->sm_count, s)) != cudaSuccess) {
             cudaGetLastError();
             return NVFP4_ERR_CUDA;
         }

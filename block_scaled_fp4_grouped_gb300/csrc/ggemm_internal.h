@@ -116,8 +116,9 @@ struct alignas(128) GroupDesc {
     // (K_g % 256 != 0): no scale tensor maps; the scale producer's lanes copy
     // the rows from these pointers. sf_row_bytes = K_g/16 then, else 0.
     int32_t sf_row_bytes;
+    int32_t sfb_tma;          // 1: SFB is a copy with rows padded to 16 bytes, loaded by TMA (tmSFB)
     const uint8_t *sfa_rows;  // SFA_g [M_g][K_g/16]
-    const uint8_t *sfb_rows;  // SFB_g [N_g][K_g/16]
+    const uint8_t *sfb_rows;  // SFB_g [N_g][K_g/16] (unused when sfb_tma)
 };
 static_assert(sizeof(GroupDesc) % 128 == 0, "GroupDesc must keep tensor maps 64-byte aligned");
 
@@ -226,6 +227,9 @@ struct GemmParams {
 // turns them into the kernel's start records (grid + 1 entries).
 void fill_cta_ranges(CtaRange *ranges, const int32_t *cta_begin, int grid, const int32_t *chunk_prefix,
                      const GroupShape *shapes, int G, int unit, int cap_single, int cap_pair);
+// Raw scale rows of K/16 bytes padded to a multiple of 16 bytes (a TMA row).
+__host__ __device__ inline int sf_padded_row_bytes(int K) { return ((K / 16 + 15) / 16) * 16; }
+
 void pack_cta_starts(CtaStart *out, const CtaRange *ranges, int grid, int total_chunks, const GroupShape *shapes);
 
 // Which block walks which range: the ranges sorted by an estimate of their
@@ -290,6 +294,10 @@ cudaError_t ggemm_configure(int index);  // raises the dynamic shared-memory lim
 cudaError_t ggemm_launch(int index, const GemmParams &p, int grid, cudaStream_t stream, bool overlap_prev);
 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream);
+// Copies raw scale rows into padded rows (the pad zero) for the jobs of p
+// (item_begin: the prefix of rows over the jobs; dst rows of
+// sf_padded_row_bytes(K) bytes).
+cudaError_t sf_pad_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream);
 
 // Host helpers shared by the plan path and the allocation-free entry point.
 
@@ -330,7 +338,9 @@ TensorMapEncodeFn tensor_map_encoder();  // nullptr when the driver has none
 
 // Fills one table entry (tensor maps, pointers, counts) for group g with
 // M_g > 0. sf_raw: encode the raw-scale maps; else the atom-layout maps.
+// sfb_padded (raw scales): SFB is a copy whose rows are padded to
+// sf_padded_row_bytes(K), loaded by TMA whatever K is.
 bool fill_group_desc(GroupDesc &d, int M, int N, int K, const void *A, const void *B, const void *SFA,
-                     const void *SFB, void *C, bool sf_raw, int unit);
+                     const void *SFB, void *C, bool sf_raw, int unit, bool sfb_padded = false);
 
 }  // namespace nvfp4

@@ -853,10 +853,12 @@ struct Roles {
             const int row_bytes = gd->sf_row_bytes;
             const uint8_t *sfa_rows = gd->sfa_rows;
             const uint8_t *sfb_rows = gd->sfb_rows;
+            // SFB a copy with rows padded to 16 bytes: loaded by TMA even here
+            const bool sfb_tma = row_bytes != 0 && gd->sfb_tma != 0;
             const int a_rows = min(t.mtu * kTileM, t.M - t.mt0 * kTileM);  // rows inside the matrices
             const int b_rows = min(t.ncols, t.N - t.n0);
-            if (lane == 0 && row_bytes == 0) {
-                maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
+            if (lane == 0 && (row_bytes == 0 || sfb_tma)) {
+                if (row_bytes == 0) maps.use(gm, t.g, &gm->tmSFA[t.mtu - 1]);
                 maps.use_rows(gm, t.g, gm->tmSFB, chunks);
             }
             const int s_tiles = (t.k_tiles + C::kKS - 1) / C::kKS;  // scale stages of this tile
@@ -873,7 +875,8 @@ struct Roles {
                                      ((ks * C::kSfRow) & 15) == 0 &&
                                      (row_bytes == 0 || (row_bytes % 4 == 0 &&
                                                          ((reinterpret_cast<uintptr_t>(sfa_rows) |
-                                                           reinterpret_cast<uintptr_t>(sfb_rows)) & 15u) == 0)),
+                                                           reinterpret_cast<uintptr_t>(sfb_tma ? nullptr : sfb_rows)) &
+                                                          15u) == 0)),
                                  kSiteCheckLoadSf)) {
                     ok = false;
                     break;
@@ -888,13 +891,20 @@ struct Roles {
                 // 8-byte pieces for the rows that allow them were slower there);
                 // rows of 8-byte multiples in 16- and 8-byte pieces, from a
                 // single copy of that code (four inlined copies were slower)
+                // An SFB loaded by TMA adds its bytes to the stage barrier (lane 0,
+                // before its own arrive below, so the phase cannot complete first).
+                if (sfb_tma && lane == 0) mbar_expect_tx(fb, (uint32_t)t.ncols * C::kSfRow);
                 if (row_bytes % 8 != 0) {
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1 && !(sfa_early && sfb_early)) griddep_wait();
                         if (part == 0 ? sfa_early : !sfa_early)
                             copy_sf_pieces<4>(st, sfa_rows, t.mt0 * kTileM, 0, 1, a_rows, row_bytes, x, lane);
-                        if (part == 0 ? sfb_early : !sfb_early)
-                            copy_sf_pieces<4>(st + C::kSfaBytes, sfb_rows, t.n0, 0, 1, b_rows, row_bytes, x, lane);
+                        if (part == 0 ? sfb_early : !sfb_early) {
+                            if (!sfb_tma)
+                                copy_sf_pieces<4>(st + C::kSfaBytes, sfb_rows, t.n0, 0, 1, b_rows, row_bytes, x, lane);
+                            else if (lane == 0)
+                                tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
+                        }
                     }
                     cp_async_mbar_arrive_noinc(fb);
                 } else if (row_bytes != 0) {
@@ -905,9 +915,13 @@ struct Roles {
                         const bool sfb = (i & 1) != 0;
                         const bool early = sfb ? sfb_early : sfa_early;
                         if (i == 2 && !(sfa_early && sfb_early)) griddep_wait();
-                        if (i < 2 ? early : !early)
+                        if (!(i < 2 ? early : !early)) continue;
+                        if (sfb && sfb_tma) {
+                            if (lane == 0) tma_rows(st + C::kSfaBytes, gm->tmSFB, x, t.n0, chunks, C::kSfRow, fb, pol);
+                        } else {
                             copy_sf_rows(sfb ? st + C::kSfaBytes : st, sfb ? sfb_rows : sfa_rows,
                                          sfb ? t.n0 : t.mt0 * kTileM, sfb ? b_rows : a_rows, row_bytes, x, lane);
+                        }
                     }
                     cp_async_mbar_arrive_noinc(fb);
                 } else if (lane == 0) {

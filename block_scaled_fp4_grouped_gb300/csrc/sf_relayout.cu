@@ -73,7 +73,44 @@ __global__ void __launch_bounds__(kRelayoutThreads) sf_relayout_kernel(const __g
     }
 }
 
+// One warp per row of one job: the row's K/16 raw bytes as 4-byte words,
+// then zero words up to sf_padded_row_bytes(K). The job is found by a
+// 32-way search of the job table as above.
+__global__ void __launch_bounds__(256) sf_pad_kernel(const __grid_constant__ RelayoutParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps = (int)(blockDim.x >> 5);
+    for (int item = blockIdx.x * warps + (int)(threadIdx.x >> 5); item < p.total_items; item += gridDim.x * warps) {
+        int lo = 0, n = p.njobs;
+        while (n > 1) {
+            const int step = (n + 31) / 32;
+            const int idx = lo + lane * step;
+            const bool ok = lane * step < n && p.jobs[idx].item_begin <= item;
+            const int k = 31 - __clz(__ballot_sync(0xFFFFFFFFu, ok));
+            lo += k * step;
+            n = min(step, n - k * step);
+        }
+        const RelayoutJob job = p.jobs[lo];
+        const int r = item - job.item_begin;
+        const int in_words = job.K / 64;  // K/16 bytes, a multiple of 4
+        const int out_words = sf_padded_row_bytes(job.K) / 4;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(job.src + (size_t)r * (size_t)(job.K / 16));
+        uint32_t *dst = reinterpret_cast<uint32_t *>(job.dst + (size_t)r * (size_t)sf_padded_row_bytes(job.K));
+        for (int w = lane; w < out_words; w += 32) dst[w] = w < in_words ? __ldg(src + w) : 0u;
+    }
+}
+
 }  // namespace
+
+cudaError_t sf_pad_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream)
+{
+    if (p.total_items <= 0 || p.jobs == nullptr) return cudaSuccess;
+    const int warps = 8;
+    int blocks = (p.total_items + warps - 1) / warps;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
+    sf_pad_kernel<<<blocks, warps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t relayout_launch(const RelayoutParams &p, int sm_count, cudaStream_t stream)
 {

@@ -97,8 +97,10 @@ typedef struct {
     uint32_t struct_size;     /* sizeof(nvfp4_ggemm_options_t) */
     int32_t sf_layout;        /* NVFP4_SF_RAW (default) or NVFP4_SF_ATOM */
     int32_t sf_path;          /* NVFP4_SF_FUSED (default) or NVFP4_SF_RELAYOUT; raw scales only */
-    int32_t cache_b_scales;   /* RELAYOUT path: SFB is re-laid out once by
-                                 nvfp4_ggemm_prepare_b_scales and run skips it */
+    int32_t cache_b_scales;   /* SFB is copied once by nvfp4_ggemm_prepare_b_scales and run
+                                 skips it: re-laid out into the atom layout (RELAYOUT path),
+                                 or into rows padded to 16 bytes that the TMA loads whatever
+                                 K_g is (FUSED path) */
     uint64_t wait_timeout_ns; /* bound on every device pipeline wait (default 2e9) */
     int32_t tile_n;           /* widest output tile in columns: 0 = 256, else a multiple of 32
                                  up to 256 (kernels exist for 128 and 256; a smaller value
@@ -263,10 +265,13 @@ NVFP4_API nvfp4_status_t nvfp4_ggemm_run_host(nvfp4_ggemm_plan_t plan, const voi
                                     const void *const *SFB, void *const *C, void *stream);
 
 /*
- * RELAYOUT path with cache_b_scales: re-lay out the G raw SFB tensors into
- * the plan's workspace once (B's scales are fixed, e.g. MoE expert
- * weights). Later runs read the cached copy and ignore their SFB argument.
- * Asynchronous on `stream`.
+ * A plan with cache_b_scales: copy the G raw SFB tensors into the plan's
+ * workspace once (B's scales are fixed, e.g. MoE expert weights): in the
+ * atom layout on the RELAYOUT path, as rows padded to a multiple of 16
+ * bytes on the FUSED path (so the TMA loads them even when K_g % 256 != 0,
+ * instead of the scale producer's lanes copying them every call). Later
+ * runs read the cached copy and ignore their SFB argument; a run before the
+ * first prepare returns NVFP4_ERR_NOT_PREPARED. Asynchronous on `stream`.
  */
 NVFP4_API nvfp4_status_t nvfp4_ggemm_prepare_b_scales(nvfp4_ggemm_plan_t plan, const void *const *SFB,
                                             void *stream);

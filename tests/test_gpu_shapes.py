@@ -189,8 +189,8 @@ SHAPES_K64 = [  # (M_g, N_g, K_g): most K_g are not multiples of 256
 ]
 
 
-@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "relayout", True),
-                                                ("atom", "fused", False)])
+@pytest.mark.parametrize("layout,path,cached", [("raw", "fused", False), ("raw", "fused", True),
+                                                ("raw", "relayout", True), ("atom", "fused", False)])
 def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
     """K_g % 64 == 0 with a partial last 256-k tile: A and B past K_g come
     from the TMA's zero fill, the last tile issues only its live 64-k MMA
@@ -217,6 +217,7 @@ def test_k_multiple_of_64_matches_the_oracle(O, layout, path, cached):
 
 
 @pytest.mark.parametrize("layout,path,cached,K", [("raw", "fused", False, 7104), ("raw", "fused", False, 7040),
+                                                  ("raw", "fused", True, 7104), ("raw", "fused", True, 7040),
                                                   ("raw", "relayout", False, 7104), ("raw", "relayout", True, 7104),
                                                   ("atom", "fused", False, 7104)])
 def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached, K):
@@ -240,16 +241,17 @@ def test_k7104_on_the_largest_m_list_sampled(O, layout, path, cached, K):
         assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
 
 
-@pytest.mark.parametrize("K", [7104, 7040])
-def test_k_multiple_of_64_fused_largest_m_list_every_element(O, K):
+@pytest.mark.parametrize("K,cached", [(7104, False), (7040, False), (7104, True)])
+def test_k_multiple_of_64_fused_largest_m_list_every_element(O, K, cached):
     """The FUSED path with lane-copied raw scale rows on the largest M list
     at K = 7104 (4-byte pieces) and K = 7040 (16- and 8-byte row classes):
     every element against the oracle, which does the whole problem in
-    seconds on the host cores."""
+    seconds on the host cores. With cache_b_scales the B scales are copied
+    once into rows padded to 16 bytes and loaded by TMA."""
     from gpu_util import run_gpu
     M = synth.make_problem("c4", seed=0).M
     prob = synth.make_problem("custom", seed=1400, M=M, N=4096, K=K)
-    got = run_gpu(prob)
+    got = run_gpu(prob, cache_b_scales=cached)
     ref, _ = O.grouped(prob)
     for g in range(prob.G):
         assert not np.isnan(got[g]).any(), f"group {g}: an element was never written"
@@ -300,8 +302,8 @@ def test_k_multiple_of_64_uniform_and_exact(O):
         assert np.array_equal(got[g].view(np.uint16), ref[g].view(np.uint16)), f"group {g}"
 
 
-@pytest.mark.parametrize("path", ["fused", "relayout"])
-def test_k_multiple_of_64_mixed_with_256_bit_exact(O, path):
+@pytest.mark.parametrize("path,cached", [("fused", False), ("fused", True), ("relayout", False)])
+def test_k_multiple_of_64_mixed_with_256_bit_exact(O, path, cached):
     """One plan whose groups mix K_g % 256 == 0 and K_g % 256 != 0 (on the
     FUSED path the scale producer loads the first kind by TMA and copies the
     second with its lanes, K_g % 128 == 0 in 8-byte pieces and the rest in
@@ -319,7 +321,7 @@ def test_k_multiple_of_64_mixed_with_256_bit_exact(O, path):
     with nb.GroupedGemm([p.M[0] for p in parts], [p.N for p in parts], [p.K for p in parts], sf_path=path) as gg:
         want = (nb.NVFP4_SF_RELAYOUT, 2) if path == "relayout" else (nb.NVFP4_SF_FUSED, 1)
         assert (gg.info().sf_path, gg.info().kernels_per_run) == want
-    got = _run(parts, sf_path=path)
+    got = _run(parts, sf_path=path, cache_b_scales=cached)
     for g, p in enumerate(parts):
         ref, _, _ = O.group_gemm(p.A[0], p.B[0], p.SFA[0], p.SFB[0], p.K)
         assert np.array_equal(got[g].view(np.uint16), ref.view(np.uint16)), f"group {g} {shapes[g]}"

@@ -93,8 +93,8 @@ def test_second_gemm_reads_what_the_first_wrote(serial, b_static):
         g2.close()
 
 
-@pytest.mark.parametrize("path,cached", [("fused", False), ("relayout", False), ("relayout", True)],
-                         ids=["fused_lanes", "relayout", "relayout_cached_b_scales"])
+@pytest.mark.parametrize("path,cached", [("fused", False), ("fused", True), ("relayout", False), ("relayout", True)],
+                         ids=["fused_lanes", "fused_lanes_cached_b_scales", "relayout", "relayout_cached_b_scales"])
 def test_relayout_reads_scales_the_previous_kernel_wrote(path, cached):
     """K % 256 != 0: on the FUSED path the GEMM's scale producer copies the
     raw scale rows with its lanes; on the RELAYOUT path the re-layout kernel
