@@ -66,12 +66,35 @@ def test_ragged_host_buffers_equal_device(O):
         assert np.array_equal(dev[g].view(np.uint16), host[g].view(np.uint16))
 
 
-def test_cached_b_scales_equal_uncached(O):
-    prob = synth.make_problem("custom", seed=7, **RAGGED)
-    a = run_gpu(prob, sf_path="relayout")
-    b = run_gpu(prob, sf_path="relayout", cache_b_scales=True)
+@pytest.mark.parametrize("path,K", [("relayout", None), ("fused", None), ("fused", 1216), ("fused", 1152)])
+def test_cached_b_scales_equal_uncached(O, path, K):
+    """B scales cached by the plan (re-laid out, or copied into rows padded to
+    16 bytes on the FUSED path) give the same bits as the B scales read on
+    every call; K % 256 != 0 puts the lane-copy kernels on the FUSED path."""
+    kw = dict(RAGGED, K=K) if K else RAGGED
+    prob = synth.make_problem("custom", seed=7, **kw)
+    a = run_gpu(prob, sf_path=path)
+    b = run_gpu(prob, sf_path=path, cache_b_scales=True)
     for g in range(prob.G):
         assert np.array_equal(a[g].view(np.uint16), b[g].view(np.uint16))
+
+
+@pytest.mark.parametrize("path", ["relayout", "fused"])
+def test_cached_b_scales_need_prepare(path):
+    """A plan that caches the B scales refuses to run before they are prepared,
+    and enqueues nothing."""
+    import torch
+    from block_scaled_fp4_grouped_gb300 import binding as nb
+    from gpu_util import to_device
+    prob = synth.make_problem("custom", seed=9, M=[64, 130], N=256, K=704)
+    A, B, SFA, SFB = to_device(prob.A), to_device(prob.B), to_device(prob.SFA), to_device(prob.SFB)
+    C = [torch.full((m, prob.N), float("nan"), dtype=torch.float16, device="cuda") for m in prob.M]
+    with nb.GroupedGemm(prob.M, prob.N, prob.K, sf_path=path, cache_b_scales=True) as gg:
+        with pytest.raises(nb.Nvfp4Error) as e:
+            gg.run(A, B, SFA, SFB, C)
+        assert e.value.status == nb.NVFP4_ERR_NOT_PREPARED
+    torch.cuda.synchronize()
+    assert all(torch.isnan(c).all().item() for c in C)
 
 
 @pytest.mark.parametrize("layout,path", PATHS)
